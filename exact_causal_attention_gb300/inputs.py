@@ -1,0 +1,98 @@
+"""Seeded synthetic inputs shared by the tests, the smoke check and the benchmark.
+
+This module holds no attention arithmetic: it only draws Q, K, V.  The recipe
+stands in for the workloads of "CUDA FlashAttention：从在线 Softmax 到长序列 IO 极限"
+(section 1 and the section 8 benchmark: B=1, H=32, D=128, N from 512 to 8192):
+
+* one CPU ``torch.Generator`` seeded with the workload's seed;
+* ``torch.randn(B, H, N, D)`` in float32 three times, in the order q, k, v;
+* q and k multiplied by ``qk_std`` (3 for the stress case so that scores reach
+  tens and the max subtraction matters), v left at N(0, 1);
+* one round-to-nearest-even cast to fp16 or bf16.
+
+The tensors stay on the CPU; callers move them to the device.
+"""
+from __future__ import annotations
+
+import dataclasses
+import hashlib
+import math
+
+import torch
+
+TORCH_DTYPES = {"fp16": torch.float16, "bf16": torch.bfloat16}
+
+
+@dataclasses.dataclass(frozen=True)
+class Workload:
+    name: str
+    B: int
+    H: int
+    N: int
+    D: int
+    dtype: str
+    causal: bool
+    seed: int
+    qk_std: float = 1.0
+
+    @property
+    def scale(self) -> float:
+        return 1.0 / math.sqrt(self.D)
+
+    @property
+    def flops(self) -> float:
+        """Algorithmic FLOPs: 2BHN^2D causal, 4BHN^2D non-causal (section 1 of the page)."""
+        f = 2.0 * self.B * self.H * self.N * self.N * self.D
+        return f if self.causal else 2.0 * f
+
+    def with_causal(self, causal: bool) -> "Workload":
+        return dataclasses.replace(self, causal=causal, name=self.name + ("" if causal else "_noncausal"))
+
+
+# The five workloads: a small one the oracle finishes in seconds, the page's
+# benchmark geometry at N = 512, 2048 (causal and not), 8192, and a bf16 stress
+# case whose length is not a multiple of the 128-row tile.
+WORKLOADS = {
+    w.name: w
+    for w in [
+        Workload("causal_b1_h2_n256_d64_fp16", 1, 2, 256, 64, "fp16", True, 0),
+        Workload("causal_b1_h32_n512_d128_fp16", 1, 32, 512, 128, "fp16", True, 1),
+        Workload("causal_b1_h32_n2048_d128_fp16", 1, 32, 2048, 128, "fp16", True, 2),
+        Workload("noncausal_b1_h32_n2048_d128_fp16", 1, 32, 2048, 128, "fp16", False, 2),
+        Workload("causal_b1_h32_n8192_d128_fp16", 1, 32, 8192, 128, "fp16", True, 3),
+        Workload("causal_b4_h32_n1000_d64_bf16", 4, 32, 1000, 64, "bf16", True, 4, qk_std=3.0),
+    ]
+}
+
+# The sweep of the page's benchmark table (causal fp16, B=1, H=32, D=128).
+SWEEP_N = (512, 1024, 2048, 4096, 8192)
+
+
+def sweep_workload(n: int, seed: int = 1) -> Workload:
+    return Workload(f"causal_b1_h32_n{n}_d128_fp16", 1, 32, n, 128, "fp16", True, seed)
+
+
+def make_qkv(B: int, H: int, N: int, D: int, dtype: str, seed: int, qk_std: float = 1.0):
+    """Return CPU tensors (q, k, v) of shape [B, H, N, D] in fp16 or bf16."""
+    g = torch.Generator(device="cpu").manual_seed(int(seed))
+    q = torch.randn(B, H, N, D, generator=g, dtype=torch.float32)
+    k = torch.randn(B, H, N, D, generator=g, dtype=torch.float32)
+    v = torch.randn(B, H, N, D, generator=g, dtype=torch.float32)
+    if qk_std != 1.0:
+        q.mul_(qk_std)
+        k.mul_(qk_std)
+    t = TORCH_DTYPES[dtype]
+    return q.to(t), k.to(t), v.to(t)
+
+
+def workload_qkv(w: Workload):
+    return make_qkv(w.B, w.H, w.N, w.D, w.dtype, w.seed, w.qk_std)
+
+
+def bits(t: torch.Tensor):
+    """The raw 16-bit patterns of a CPU fp16/bf16 tensor as a numpy uint16 array."""
+    return t.contiguous().view(torch.int16).numpy().view("uint16")
+
+
+def sha256(t: torch.Tensor) -> str:
+    return hashlib.sha256(bits(t).tobytes()).hexdigest()

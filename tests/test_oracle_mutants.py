@@ -1,0 +1,72 @@
+"""The oracle's pins must catch plausible mistakes.
+
+Each case plants one mistake in a copy of the oracle source (a dropped term, a
+wrong sign or index, a transposed operand, a flipped mask, a wrong decoder
+constant), builds it on the CPU and runs the pin suite against the copy: the
+suite has to fail.  The real oracle is never modified.
+"""
+import os
+import shutil
+import subprocess
+import sys
+import tempfile
+from concurrent.futures import ThreadPoolExecutor
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+SRC = os.path.join(ROOT, "oracle", "attn_ref.cpp")
+
+MUTANTS = {
+    "scale_dropped": ("s[j] = p.scale * dot;", "s[j] = dot;"),
+    "key_transposed": ("for (long d = 0; d < p.D; ++d) dot += qi[d] * kj[d];",
+                       "for (long d = 0; d < p.D; ++d) dot += qi[d] * kb[(d * p.N + j) % (p.N * p.D)];"),
+    "exp_sign_flipped": ("for (long j = 0; j <= last; ++j) l += std::exp(s[j] - m);",
+                         "for (long j = 0; j <= last; ++j) l += std::exp(m - s[j]);"),
+    "mask_strict": ("const long last = p.causal ? i : p.N - 1;\n  score_row(p, bh, i, last, s);\n  double m",
+                    "const long last = p.causal ? i - 1 : p.N - 1;\n  score_row(p, bh, i, last, s);\n  double m"),
+    "no_normalisation": ("const double w = std::exp(s[j] - m) / l;", "const double w = std::exp(s[j] - m);"),
+    "lse_without_max": ("  *lse = m + std::log(l);\n}\n\n// Online", "  *lse = std::log(l);\n}\n\n// Online"),
+    "value_row_index": ("const double w = std::exp(s[j] - m) / l;\n    const double* vj = vb + j * p.D;",
+                        "const double w = std::exp(s[j] - m) / l;\n    const double* vj = vb + i * p.D;"),
+    "no_max_subtraction": ("const double w = std::exp(s[j] - m) / l;", "const double w = std::exp(s[j]) / l;"),
+    "online_no_rescale": ("for (long d = 0; d < p.D; ++d) acc[d] *= alpha;", ""),
+    "online_beta_dropped": ("l = alpha * l + beta * l_tile;", "l = alpha * l + l_tile;"),
+    "fp16_exponent_bias": ("exponent - 25);", "exponent - 24);"),
+    "bf16_hidden_bit": ("static_cast<double>(128 + mantissa)", "static_cast<double>(mantissa)"),
+}
+
+
+def _build_and_run(name, old, new, workdir):
+    src = open(SRC).read()
+    assert old == "" or src.count(old) == 1, f"{name}: pattern must occur exactly once"
+    mutant = os.path.join(workdir, f"{name}.cpp")
+    lib = os.path.join(workdir, f"lib{name}.so")
+    with open(mutant, "w") as f:
+        f.write(src.replace(old, new))
+    subprocess.run(["g++", "-O2", "-std=c++17", "-shared", "-fPIC", "-pthread", "-o", lib, mutant],
+                   check=True)
+    env = dict(os.environ, ORACLE_LIB_OVERRIDE=lib)
+    r = subprocess.run([sys.executable, "-m", "pytest", "-x", "-q", "-p", "no:cacheprovider",
+                        os.path.join(ROOT, "tests", "test_oracle.py")],
+                       cwd=ROOT, env=env, capture_output=True, text=True)
+    return name, r.returncode
+
+
+def test_unmodified_copy_passes_through_the_same_harness():
+    workdir = tempfile.mkdtemp(prefix="oracle_control_")
+    try:
+        assert _build_and_run("control", "", "", workdir)[1] == 0
+    finally:
+        shutil.rmtree(workdir, ignore_errors=True)
+
+
+def test_every_planted_mistake_fails_a_pin():
+    workdir = tempfile.mkdtemp(prefix="oracle_mutants_")
+    try:
+        with ThreadPoolExecutor(max_workers=min(8, os.cpu_count() or 1)) as ex:
+            results = list(ex.map(lambda kv: _build_and_run(kv[0], *kv[1], workdir), MUTANTS.items()))
+    finally:
+        shutil.rmtree(workdir, ignore_errors=True)
+    survivors = [name for name, rc in results if rc == 0]
+    assert not survivors, f"pins did not catch: {survivors}"
