@@ -1,0 +1,394 @@
+"""Benchmark: causal attention forward TFLOP/s (2BHN^2D) on one GB300 per rank.
+
+Workload: causal fp16, B=1, H=32, N=8192, D=128 (the long end of the N = 512..8192
+sweep of "CUDA FlashAttention：从在线 Softmax 到长序列 IO 极限", section 8), inputs
+synthetic N(0, 1) from seed 3.  One step = one attn_fwd call over the whole batch.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Prints one JSON line on rank 0.  `value` is device time (CUDA events on the
+launching stream, L2 flushed between steps); `e2e` is the same metric through the
+C ABI with pinned host buffers, copies in and out included.  The reference arm
+(--impl reference) is the FP64 CPU oracle on the host cores, timed on a bounded
+sample of query rows of the same workload.
+Multi-GPU runs are independent replicas (every (batch, head) slice is
+independent; there is no exchange step): value = all ranks' FLOPs / max time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "causal attn fwd TFLOP/s (2BHN^2D) at N=512..8192, % of GB300 dense FP16 peak"
+WORKLOAD = "causal_b1_h32_n8192_d128_fp16"
+# The page's own number for this workload (PyTorch SDPA FLASH backend, RTX 3060 Laptop, SM86):
+# 25.854 ms at B=1, H=32, N=8192, D=128 causal fp16 -> 2BHN^2D / t.
+PAGE_MS_N8192 = 25.854
+L2_FLUSH_BYTES = 256 << 20  # twice the 129 MB L2
+PROFILES = os.path.join(ROOT, "profiles")
+
+
+def rank_env():
+    return (int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")),
+            int(os.environ.get("LOCAL_RANK", "0")))
+
+
+def host_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            return json.load(f), "measured"
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
+
+
+def kernel_source_hash():
+    csrc = os.path.join(ROOT, "exact_causal_attention_gb300", "csrc")
+    h = hashlib.sha256()
+    for name in sorted(os.listdir(csrc)):
+        if name.endswith((".cu", ".cuh")):
+            with open(os.path.join(csrc, name), "rb") as f:
+                h.update(name.encode() + f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic():
+    """DRAM bytes per launch from the committed ncu summary, if it matches the current kernel."""
+    path = os.path.join(PROFILES, "attn_fwd_n8192_traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        rec = json.load(f)
+    if rec.get("kernel_source_sha256_16") != kernel_source_hash() or rec.get("workload") != WORKLOAD:
+        return None
+    return rec.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons while the timed region runs."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+        self.t = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, ValueError):
+            self.proc = None
+            return
+        self.t = threading.Thread(target=self._read, daemon=True)
+        self.t.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.t.join(timeout=5)
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[4:8]):
+                if val.lower().startswith("active"):
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        sm_sorted = sorted(sm)
+        return {"sm_mhz": sm_sorted[len(sm_sorted) // 2], "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def oracle_rows_tflops(q, k, v, w, seconds_target, seed):
+    """Time the FP64 oracle on random query rows of the workload; returns (TFLOP/s, rows, seconds)."""
+    import numpy as np
+
+    import oracle
+    from exact_causal_attention_gb300 import inputs
+
+    qd, kd, vd = (oracle.decode(inputs.bits(x), w.dtype) for x in (q, k, v))
+    rng = np.random.default_rng(seed)
+
+    def flops(rows):
+        return float(sum(4.0 * w.D * ((i + 1) if w.causal else w.N) for _, i in rows))
+
+    def run(count):
+        rows = [(int(rng.integers(0, w.B * w.H)), int(rng.integers(0, w.N))) for _ in range(count)]
+        t0 = time.perf_counter()
+        oracle.attention_rows(qd, kd, vd, w.causal, w.scale, rows)
+        return rows, time.perf_counter() - t0
+
+    rows, dt = run(4 * host_cores())
+    rate = flops(rows) / max(dt, 1e-9)
+    per_row = flops(rows) / len(rows)
+    count = max(host_cores(), int(seconds_target * rate / per_row))
+    rows, dt = run(count)
+    return flops(rows) / dt / 1e12, len(rows), dt
+
+
+def bench_reference(args, w):
+    rank, world, _ = rank_env()
+    if rank != 0:
+        return
+    from exact_causal_attention_gb300 import inputs
+
+    q, k, v = inputs.workload_qkv(w)
+    per_step = max(1.0, 60.0 / max(1, args.steps + args.warmup))
+    for s in range(args.warmup):
+        oracle_rows_tflops(q, k, v, w, min(per_step, 2.0), seed=100 + s)
+    vals, secs, nrows = [], 0.0, 0
+    for s in range(args.steps):
+        tf, n, dt = oracle_rows_tflops(q, k, v, w, per_step, seed=200 + s)
+        vals.append(tf)
+        secs += dt
+        nrows += n
+    value = sum(vals) / len(vals)
+    cores = host_cores()
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000.0 * secs / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "D": w.D, "causal": w.causal,
+                   "seed": w.seed},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+                         "sample": f"{nrows} random query rows of the workload over {args.steps} steps "
+                                   f"(two-pass FP64 oracle, {cores} threads)"},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def bench_ours(args, w):
+    import torch
+    import torch.distributed as dist
+
+    import exact_causal_attention_gb300 as eca
+    from exact_causal_attention_gb300 import inputs
+
+    rank, world, local = rank_env()
+    torch.cuda.set_device(local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    eca.load_library()
+    dev = torch.device("cuda", local)
+    stream = torch.cuda.current_stream(dev)
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize(dev)
+
+    q, k, v = inputs.workload_qkv(w)
+    dq, dk, dv = (x.to(dev) for x in (q, k, v))
+    o = torch.empty_like(dq)
+    lse = torch.empty((w.B, w.H, w.N), dtype=torch.float32, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+
+    def step():
+        eca.attn_fwd_into(dq, dk, dv, o, lse, causal=w.causal, scale=w.scale, stream=stream)
+
+    for _ in range(max(3, args.warmup)):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize(dev)
+    if eca.device_status() != 0:
+        raise RuntimeError("a kernel wait timed out during warm-up")
+
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    sampler = ClockSampler(local)
+    sampler.start()
+    time.sleep(0.3)
+    barrier()
+    for i in range(args.steps):
+        flush.zero_()  # untimed: evicts q, k, v, o from L2 between steps
+        starts[i].record(stream)
+        step()
+        ends[i].record(stream)
+    barrier()
+    clocks = sampler.stop()
+    step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    total_ms = sum(step_ms)
+    if world > 1:
+        t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    status = eca.device_status()
+    if status != 0:
+        raise RuntimeError("a kernel wait timed out in the timed region")
+    flops = w.flops
+    value = flops * args.steps * world / (total_ms * 1e-3) / 1e12
+    kernel_ms = total_ms / args.steps
+
+    # End to end through the C ABI: pinned host q, k, v in, o and lse out, every step.
+    hq, hk, hv = (x.pin_memory() for x in (q, k, v))
+    ho = torch.empty(o.shape, dtype=o.dtype).pin_memory()
+    hl = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
+    e2e_steps = max(3, min(args.steps, 20))
+
+    def e2e_step():
+        dq.copy_(hq, non_blocking=True)
+        dk.copy_(hk, non_blocking=True)
+        dv.copy_(hv, non_blocking=True)
+        step()
+        ho.copy_(o, non_blocking=True)
+        hl.copy_(lse, non_blocking=True)
+
+    e2e_step()
+    barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    barrier()
+    e2e_ms = e0.elapsed_time(e1) / e2e_steps
+    if world > 1:
+        t = torch.tensor([e2e_ms], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    h2d = sum(x.numel() * x.element_size() for x in (hq, hk, hv))
+    d2h = ho.numel() * ho.element_size() + hl.numel() * hl.element_size()
+
+    sweep = {}
+    if not args.no_sweep and rank == 0:
+        for n in inputs.SWEEP_N:
+            sw = inputs.sweep_workload(n)
+            sq, sk, sv = (x.to(dev) for x in inputs.workload_qkv(sw))
+            so = torch.empty_like(sq)
+            sl = torch.empty((sw.B, sw.H, sw.N), dtype=torch.float32, device=dev)
+            times = []
+            for i in range(13):
+                flush.zero_()
+                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a.record(stream)
+                eca.attn_fwd_into(sq, sk, sv, so, sl, causal=True, scale=sw.scale, stream=stream)
+                b.record(stream)
+                times.append((a, b))
+            torch.cuda.synchronize(dev)
+            ms = sorted(a.elapsed_time(b) for a, b in times[3:])
+            med = ms[len(ms) // 2]
+            sweep[str(n)] = {"ms": round(med, 4), "tflops": round(sw.flops / (med * 1e-3) / 1e12, 1)}
+            del sq, sk, sv, so, sl
+
+    fp16_peak = None
+    if not args.no_peak and rank == 0:
+        a = torch.randn(8192, 8192, device=dev, dtype=torch.float16)
+        b = torch.randn(8192, 8192, device=dev, dtype=torch.float16)
+        for _ in range(3):
+            a @ b
+        best = float("inf")
+        for _ in range(10):
+            s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            s0.record(stream)
+            a @ b
+            s1.record(stream)
+            s1.synchronize()
+            best = min(best, s0.elapsed_time(s1))
+        fp16_peak = 2 * 8192 ** 3 / (best * 1e-3) / 1e12
+        del a, b
+
+    cpu = None
+    if rank == 0 and not args.no_cpu:
+        tf, nrows, secs = oracle_rows_tflops(q, k, v, w, args.cpu_seconds, seed=7)
+        cpu = {"value": tf, "unit": "TFLOP/s", "cores": host_cores(), "kind": "oracle",
+               "sample": f"{nrows} random query rows of the workload ({secs:.1f} s, two-pass FP64 oracle, "
+                         f"{host_cores()} threads)"}
+
+    if world > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+    if rank != 0:
+        return
+    peaks, kind = measured_peaks()
+    peak = float(peaks["bf16_tflops"])  # fp16 and bf16 share one nominal dense rate (ratio 1.0)
+    achieved = flops / (kernel_ms * 1e-3) / 1e12
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": kernel_ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": value / world / (flops / (PAGE_MS_N8192 * 1e-3) / 1e12),
+        "dtype": "fp16", "data": "synthetic",
+        "config": {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "D": w.D, "causal": w.causal,
+                   "seed": w.seed, "flops_per_step": flops,
+                   "l2": "flushed between timed steps (256 MiB write, outside the events)",
+                   "parallelism": f"replicas x{world}"},
+        "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                     "frac": achieved / peak, "peak_source": f"{kind} bf16 burst (fp16/bf16 nominal ratio 1.0)",
+                     "traffic": recorded_traffic()},
+        "cpu_baseline": cpu,
+        "e2e": {"value": flops / (e2e_ms * 1e-3) / 1e12 * world, "unit": "TFLOP/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+        "gpu_launches": args.steps,
+        "clocks": clocks,
+        "sweep": sweep,
+        "fp16_matmul_peak_tflops": fp16_peak,
+        "frac_of_measured_fp16_matmul": (achieved / fp16_peak) if fp16_peak else None,
+        "frac_of_datasheet_dense_fp16": achieved / 2250.0,
+        "vs_baseline_ref": "page's PyTorch SDPA FLASH on RTX 3060 Laptop (SM86): 25.854 ms",
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=300)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-sweep", action="store_true")
+    ap.add_argument("--no-peak", action="store_true")
+    ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    args = ap.parse_args()
+    args.warmup = max(3, args.warmup)
+    from exact_causal_attention_gb300 import inputs
+
+    w = inputs.WORKLOADS[WORKLOAD]
+    if args.impl == "reference":
+        bench_reference(args, w)
+    else:
+        bench_ours(args, w)
+
+
+if __name__ == "__main__":
+    main()

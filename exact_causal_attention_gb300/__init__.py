@@ -1,0 +1,150 @@
+"""Exact causal / non-causal attention forward on sm_103a (GB300).
+
+Thin ctypes binding over the C ABI in ``include/attn.h``: it checks and marshals
+torch tensors into pointers and sizes and calls the library; every step of the
+computation runs in the library's CUDA kernels.  There is no fallback: if the
+shared library is missing or the device is not sm_103, calls raise.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+import threading
+
+__all__ = ["attn_fwd", "attn_fwd_into", "load_library", "device_status", "watchdog_selftest",
+           "AttnError", "STATUS"]
+
+_LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "_build", "libeca_attn.so")
+_lock = threading.Lock()
+_lib = None
+
+STATUS = {
+    0: "ATTN_OK",
+    -1: "ATTN_ERR_INVALID_ARG",
+    -2: "ATTN_ERR_UNALIGNED",
+    -3: "ATTN_ERR_UNSUPPORTED_D",
+    -4: "ATTN_ERR_ARCH",
+    -5: "ATTN_ERR_LAUNCH",
+    -6: "ATTN_ERR_TIMEOUT",
+    -7: "ATTN_ERR_CUDA",
+}
+
+# Every exported symbol of include/attn.h with its ctypes signature.
+_VP, _I, _F, _U = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_uint
+SIGNATURES = {
+    "attn_fwd": (_I, [_VP, _VP, _VP, _VP, _VP, _I, _I, _I, _I, _I, _F, _VP]),
+    "attn_fwd_bf16": (_I, [_VP, _VP, _VP, _VP, _VP, _I, _I, _I, _I, _I, _F, _VP]),
+    "attn_device_status": (_I, [_VP]),
+    "attn_watchdog_selftest": (_I, [_U, _VP]),
+    "attn_status_string": (ctypes.c_char_p, [_I]),
+    "attn_version": (_I, []),
+}
+
+
+class AttnError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {STATUS.get(status, status)} ({_status_text(status)})")
+
+
+def _status_text(status: int) -> str:
+    try:
+        return load_library().attn_status_string(status).decode()
+    except Exception:  # library missing while formatting an error
+        return "?"
+
+
+def library_path() -> str:
+    return _LIB_PATH
+
+
+def load_library(path: str | None = None):
+    """Load the CUDA library (built by ``exact_causal_attention_gb300.build``)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            p = path or _LIB_PATH
+            if not os.path.exists(p):
+                raise RuntimeError(f"CUDA library not built: {p} is missing "
+                                   "(run python -c 'import __graft_entry__ as g; g.build()')")
+            lib = ctypes.CDLL(p)
+            for name, (res, args) in SIGNATURES.items():
+                fn = getattr(lib, name)
+                fn.restype = res
+                fn.argtypes = args
+            _lib = lib
+    return _lib
+
+
+def _stream_handle(stream):
+    import torch
+
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+
+
+def _check_qkv(q, k, v):
+    import torch
+
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        if not isinstance(t, torch.Tensor) or not t.is_cuda:
+            raise TypeError(f"{name} must be a CUDA tensor")
+        if t.dim() != 4:
+            raise ValueError(f"{name} must be [B, H, N, D]")
+        if not t.is_contiguous():
+            raise ValueError(f"{name} must be contiguous")
+    if not (q.shape == k.shape == v.shape):
+        raise ValueError("q, k, v must have the same shape [B, H, N, D]")
+    if not (q.dtype == k.dtype == v.dtype) or q.dtype not in (torch.float16, torch.bfloat16):
+        raise TypeError("q, k, v must all be float16 or all bfloat16")
+    if not (q.device == k.device == v.device):
+        raise ValueError("q, k, v must be on one device")
+
+
+def attn_fwd_into(q, k, v, o, lse, causal: bool = True, scale: float | None = None, stream=None) -> None:
+    """Write O into ``o`` ([B,H,N,D], q's dtype) and the natural-log LSE into ``lse``
+    ([B,H,N] float32, or None) on ``stream`` (default: torch's current stream)."""
+    import torch
+
+    _check_qkv(q, k, v)
+    B, H, N, D = q.shape
+    if o.shape != q.shape or o.dtype != q.dtype or not o.is_contiguous() or o.device != q.device:
+        raise ValueError("o must be a contiguous tensor shaped and typed like q")
+    if lse is not None and (lse.shape != (B, H, N) or lse.dtype != torch.float32 or not lse.is_contiguous()
+                            or lse.device != q.device):
+        raise ValueError("lse must be a contiguous float32 [B, H, N] tensor on q's device")
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    lib = load_library()
+    fn = lib.attn_fwd_bf16 if q.dtype == torch.bfloat16 else lib.attn_fwd
+    with torch.cuda.device(q.device):
+        rc = fn(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                lse.data_ptr() if lse is not None else None, B, H, N, D, int(bool(causal)),
+                float(scale), _stream_handle(stream))
+    if rc != 0:
+        raise AttnError(rc, "attn_fwd")
+
+
+def attn_fwd(q, k, v, causal: bool = True, scale: float | None = None, return_lse: bool = True,
+             stream=None):
+    """O = softmax(scale * q k^T + mask) v (and the row LSE) for [B, H, N, D] CUDA tensors."""
+    import torch
+
+    _check_qkv(q, k, v)
+    o = torch.empty_like(q)
+    lse = torch.empty(q.shape[:3], dtype=torch.float32, device=q.device) if return_lse else None
+    attn_fwd_into(q, k, v, o, lse, causal=causal, scale=scale, stream=stream)
+    return (o, lse) if return_lse else o
+
+
+def device_status(stream=None) -> int:
+    """Synchronise the stream, then read and clear the device status word (0 = ok)."""
+    return load_library().attn_device_status(_stream_handle(stream))
+
+
+def watchdog_selftest(timeout_us: int, stream=None) -> None:
+    rc = load_library().attn_watchdog_selftest(int(timeout_us), _stream_handle(stream))
+    if rc != 0:
+        raise AttnError(rc, "attn_watchdog_selftest")

@@ -1,0 +1,249 @@
+// Host side of the C ABI declared in include/attn.h: argument checks, TMA tensor
+// maps, launch on the caller's stream, and the device status word.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "attn.h"
+#include "attn_fwd_kernel.cuh"
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+constexpr unsigned long long kWaitLimitNs = 2000000000ull;  // 2 s per single wait
+
+// Device status word: 0, or the code of the last bounded wait that gave up.
+__device__ int g_device_status = 0;
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+struct DeviceState {
+  bool probed = false;
+  bool sm103 = false;
+  int* status = nullptr;    // address of g_device_status on this device
+  unsigned configured = 0;  // bitmask of kernel instantiations with smem attribute set
+};
+
+std::mutex g_mutex;
+DeviceState g_devices[kMaxDevices];
+EncodeTiledFn g_encode = nullptr;
+
+int get_encode_fn(EncodeTiledFn* out) {
+  if (g_encode == nullptr) {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) !=
+            cudaSuccess ||
+        q != cudaDriverEntryPointSuccess || fn == nullptr) {
+      return ATTN_ERR_CUDA;
+    }
+    g_encode = reinterpret_cast<EncodeTiledFn>(fn);
+  }
+  *out = g_encode;
+  return ATTN_OK;
+}
+
+// Per-device checks and the status word's device address; call with g_mutex held.
+int device_state(DeviceState** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return ATTN_ERR_CUDA;
+  DeviceState& st = g_devices[dev];
+  if (!st.probed) {
+    int major = 0, minor = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess) {
+      return ATTN_ERR_CUDA;
+    }
+    st.sm103 = (major == 10 && minor == 3);
+    if (st.sm103) {
+      void* addr = nullptr;
+      if (cudaGetSymbolAddress(&addr, g_device_status) != cudaSuccess) return ATTN_ERR_CUDA;
+      st.status = static_cast<int*>(addr);
+    }
+    st.probed = true;
+  }
+  if (!st.sm103) return ATTN_ERR_ARCH;
+  *out = &st;
+  return ATTN_OK;
+}
+
+// [B*H, N, D] 16-bit tensor as a rank-3 map (D, N, B*H) with 64 x 128 x 1 boxes,
+// 128-byte swizzle; rows past N read as zero.
+int encode_qkv_map(EncodeTiledFn encode, CUtensorMap* map, const void* ptr, bool bf16, int D, int N,
+                   int BH) {
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(N),
+                              static_cast<cuuint64_t>(BH)};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(D) * 2,
+                                 static_cast<cuuint64_t>(N) * static_cast<cuuint64_t>(D) * 2};
+  const cuuint32_t box[3] = {64, 128, 1};
+  const cuuint32_t elem_strides[3] = {1, 1, 1};
+  const CUresult r =
+      encode(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3,
+             const_cast<void*>(ptr), dims, strides, box, elem_strides, CU_TENSOR_MAP_INTERLEAVE_NONE,
+             CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? ATTN_OK : ATTN_ERR_INVALID_ARG;
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+bool overlaps(const void* a, const void* b, uint64_t bytes) {
+  const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
+  return x < y + bytes && y < x + bytes;
+}
+
+// Checks that need no GPU.  Order: pointers, sizes, head dim, scale, alignment, overlap.
+int check_args(const void* q, const void* k, const void* v, const void* o, const float* lse, int B,
+               int H, int N, int D, float scale) {
+  if (!q || !k || !v || !o) return ATTN_ERR_INVALID_ARG;
+  if (B < 1 || H < 1 || N < 1) return ATTN_ERR_INVALID_ARG;
+  if (D != 64 && D != 128) return ATTN_ERR_UNSUPPORTED_D;
+  if (!std::isfinite(scale) || !(scale > 0.f)) return ATTN_ERR_INVALID_ARG;
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16)) return ATTN_ERR_UNALIGNED;
+  if (lse && !aligned(lse, 4)) return ATTN_ERR_UNALIGNED;
+  const uint64_t bh = static_cast<uint64_t>(B) * static_cast<uint64_t>(H);
+  const uint64_t n_tiles = (static_cast<uint64_t>(N) + 127) / 128;
+  const uint64_t n_pairs = (n_tiles + 1) / 2;
+  // Grid (pairs x heads) and tensor-map extents must fit; byte sizes stay far below 2^63.
+  if (bh > 0x7fffffffull || n_pairs * bh > 0x7fffffffull) return ATTN_ERR_INVALID_ARG;
+  const uint64_t bytes = bh * static_cast<uint64_t>(N) * static_cast<uint64_t>(D) * 2;
+  if (static_cast<uint64_t>(N) * D * 2 >= (1ull << 40) || bytes >= (1ull << 62)) return ATTN_ERR_INVALID_ARG;
+  if (overlaps(o, q, bytes) || overlaps(o, k, bytes) || overlaps(o, v, bytes)) return ATTN_ERR_INVALID_ARG;
+  return ATTN_OK;
+}
+
+template <int D, bool BF16>
+int launch(const void* q, const void* k, const void* v, void* o, float* lse, int BH, int N, int causal,
+           float scale, cudaStream_t stream, DeviceState* st, EncodeTiledFn encode) {
+  using L = eca::FwdSmem<D>;
+  auto kernel = eca::attn_fwd_kernel<D, BF16>;
+  const unsigned bit = 1u << ((D == 128 ? 2 : 0) + (BF16 ? 1 : 0));
+  if (!(st->configured & bit)) {
+    if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kDynamicBytes) !=
+        cudaSuccess) {
+      return ATTN_ERR_CUDA;
+    }
+    st->configured |= bit;
+  }
+  CUtensorMap tq, tk, tv;
+  int rc = encode_qkv_map(encode, &tq, q, BF16, D, N, BH);
+  if (rc == ATTN_OK) rc = encode_qkv_map(encode, &tk, k, BF16, D, N, BH);
+  if (rc == ATTN_OK) rc = encode_qkv_map(encode, &tv, v, BF16, D, N, BH);
+  if (rc != ATTN_OK) return rc;
+
+  eca::FwdParams p;
+  p.o = o;
+  p.lse = lse;
+  p.status = st->status;
+  p.N = N;
+  p.n_tiles = (N + eca::kBlockM - 1) / eca::kBlockM;
+  p.n_pairs = (p.n_tiles + 1) / 2;
+  p.BH = BH;
+  p.causal = causal ? 1 : 0;
+  p.scale_log2e = scale * 1.4426950408889634f;
+  p.wait_limit_ns = kWaitLimitNs;
+  p.timeout_code = ATTN_ERR_TIMEOUT;
+  const unsigned grid = static_cast<unsigned>(p.n_pairs) * static_cast<unsigned>(BH);
+  kernel<<<grid, eca::kThreads, L::kDynamicBytes, stream>>>(tq, tk, tv, p);
+  return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_LAUNCH;
+}
+
+int attn_fwd_impl(bool bf16, const void* q, const void* k, const void* v, void* o, float* lse, int B,
+                  int H, int N, int D, int causal, float scale, attn_stream_t stream) {
+  const int rc = check_args(q, k, v, o, lse, B, H, N, D, scale);
+  if (rc != ATTN_OK) return rc;
+  std::lock_guard<std::mutex> lock(g_mutex);
+  DeviceState* st = nullptr;
+  int r = device_state(&st);
+  if (r != ATTN_OK) return r;
+  EncodeTiledFn encode = nullptr;
+  r = get_encode_fn(&encode);
+  if (r != ATTN_OK) return r;
+  const int BH = B * H;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (D == 128) {
+    return bf16 ? launch<128, true>(q, k, v, o, lse, BH, N, causal, scale, s, st, encode)
+                : launch<128, false>(q, k, v, o, lse, BH, N, causal, scale, s, st, encode);
+  }
+  return bf16 ? launch<64, true>(q, k, v, o, lse, BH, N, causal, scale, s, st, encode)
+              : launch<64, false>(q, k, v, o, lse, BH, N, causal, scale, s, st, encode);
+}
+
+// One thread waits on a barrier that nothing ever arrives on, with a bounded wait.
+__global__ void watchdog_selftest_kernel(int* status, unsigned long long limit_ns, int code) {
+  __shared__ __align__(8) uint64_t barrier;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    abort_flag = 0;
+    eca::mbar_init(eca::smem_u32(&barrier), 1);
+    eca::fence_barrier_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    const eca::Watchdog wd{&abort_flag, status, limit_ns, code};
+    wd.wait(eca::smem_u32(&barrier), 0);
+  }
+}
+
+}  // namespace
+
+extern "C" {
+
+int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N, int D,
+             int causal, float scale, attn_stream_t stream) {
+  return attn_fwd_impl(false, q, k, v, o, lse, B, H, N, D, causal, scale, stream);
+}
+
+int attn_fwd_bf16(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N,
+                  int D, int causal, float scale, attn_stream_t stream) {
+  return attn_fwd_impl(true, q, k, v, o, lse, B, H, N, D, causal, scale, stream);
+}
+
+int attn_device_status(attn_stream_t stream) {
+  std::lock_guard<std::mutex> lock(g_mutex);
+  DeviceState* st = nullptr;
+  const int r = device_state(&st);
+  if (r != ATTN_OK) return r;
+  if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) return ATTN_ERR_CUDA;
+  int value = 0;
+  const int zero = 0;
+  if (cudaMemcpy(&value, st->status, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return ATTN_ERR_CUDA;
+  if (cudaMemcpy(st->status, &zero, sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess) return ATTN_ERR_CUDA;
+  return value == 0 ? ATTN_OK : value;
+}
+
+int attn_watchdog_selftest(unsigned int timeout_us, attn_stream_t stream) {
+  if (timeout_us < 1 || timeout_us > 10000000u) return ATTN_ERR_INVALID_ARG;
+  std::lock_guard<std::mutex> lock(g_mutex);
+  DeviceState* st = nullptr;
+  const int r = device_state(&st);
+  if (r != ATTN_OK) return r;
+  watchdog_selftest_kernel<<<1, 32, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
+      st->status, static_cast<unsigned long long>(timeout_us) * 1000ull, ATTN_ERR_TIMEOUT);
+  return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_LAUNCH;
+}
+
+const char* attn_status_string(int status) {
+  switch (status) {
+    case ATTN_OK: return "ok";
+    case ATTN_ERR_INVALID_ARG: return "invalid argument";
+    case ATTN_ERR_UNALIGNED: return "tensor pointer not 16-byte aligned";
+    case ATTN_ERR_UNSUPPORTED_D: return "unsupported head dimension (D must be 64 or 128)";
+    case ATTN_ERR_ARCH: return "current device is not sm_103";
+    case ATTN_ERR_LAUNCH: return "kernel launch failed";
+    case ATTN_ERR_TIMEOUT: return "a bounded device wait timed out";
+    case ATTN_ERR_CUDA: return "CUDA runtime/driver call failed";
+    default: return "unknown status";
+  }
+}
+
+int attn_version(void) { return 100; }
+
+}  // extern "C"

@@ -1,0 +1,389 @@
+// Fused attention forward for sm_103a: TMA-fed K/V ring, tcgen05 MMAs with TMEM
+// accumulators for S = Q K^T and O += P V, FP32 online softmax.
+//
+// Method: "CUDA FlashAttention：从在线 Softmax 到长序列 IO 极限" (chengzipai.xyz):
+// section 1 (the operation and its causal mask), section 4 (the online
+// recurrence over key tiles: running max m, running sum l, unnormalised o,
+// rescaled by exp(m_old - m_new) at every merge), section 5.1 (one CTA owns a
+// block of query rows and streams K/V tiles so each tile is read once for all of
+// them), section 6 (rescale the old O before adding this tile's P V; mask before
+// the max; never form -inf - (-inf)), section 7 (skip key tiles entirely above
+// the diagonal, mask element-wise only on the diagonal tile; keep the LSE).
+//
+// GB300 mapping (differs from the page's mma.sync / cp.async design):
+//   * one CTA = two 128-row query tiles of one (batch, head); 320 threads:
+//       warps 0-3  softmax for query tile 0     warps 4-7  softmax for query tile 1
+//       warp 8     TMA producer (Q once, then K_j, V_j into a ring of smem slots)
+//       warp 9     TMEM owner and single-thread tcgen05.mma issuer
+//   * TMEM (512 columns x 128 lanes): S_t at column 128 t (128 fp32 columns),
+//     O_t at column 256 + D t.  P_t (16-bit, two per column) is written over the
+//     first 64 columns of S_t and read by the P V MMA straight from TMEM.
+//   * a query row is a TMEM lane, so each softmax thread owns one full score row:
+//     the row max and row sum need no shuffles.
+//   * exp is computed as 2^(s * scale * log2 e - m) with the MUFU ex2.
+//   * conditional rescaling: the reference max m is only moved (and O, l
+//     rescaled) when the new row max exceeds it by more than 2^8 in the base-2
+//     domain; otherwise probabilities are formed against the stale, smaller
+//     reference, which is exact algebra (o and l share that reference) and keeps
+//     every p below 256.
+#pragma once
+#include <cuda.h>
+#include <cstdint>
+
+#include "ptx.cuh"
+
+namespace eca {
+
+constexpr int kBlockM = 128;            // query rows per tile (one per TMEM lane)
+constexpr int kBlockN = 128;            // keys per K/V tile
+constexpr int kSubTileBytes = 128 * 128;  // 128 rows x 64 16-bit elements (one 128-B swizzle span)
+constexpr int kThreads = 320;
+constexpr int kTmemCols = 512;
+constexpr float kRescaleThreshold = 8.0f;  // log2 units
+
+struct FwdParams {
+  void* o;        // [BH, N, D] 16-bit
+  float* lse;     // [BH, N] or null
+  int* status;    // device status word
+  int N;
+  int n_tiles;    // ceil(N / 128), for queries and keys alike
+  int n_pairs;    // ceil(n_tiles / 2)
+  int BH;
+  int causal;
+  float scale_log2e;  // scale * log2(e)
+  unsigned long long wait_limit_ns;
+  int timeout_code;
+};
+
+template <int D>
+struct FwdSmem {
+  static constexpr int kSub = D / 64;                      // 64-element column blocks per row
+  static constexpr int kTileBytes = kSub * kSubTileBytes;  // one 128 x D tile
+  static constexpr int kStages = D == 128 ? 4 : 8;         // K/V ring slots
+  static constexpr int kQOff = 0;
+  static constexpr int kKVOff = 2 * kTileBytes;
+  static constexpr int kBarOff = kKVOff + kStages * kTileBytes;
+  // barrier indices
+  static constexpr int kBarQ = 0;
+  static constexpr int kBarFull = 1;
+  static constexpr int kBarEmpty = kBarFull + kStages;
+  static constexpr int kBarS = kBarEmpty + kStages;  // + t
+  static constexpr int kBarP = kBarS + 2;            // + t
+  static constexpr int kBarO = kBarP + 2;            // + t
+  static constexpr int kBarDrain = kBarO + 2;
+  static constexpr int kNumBars = kBarDrain + 1;
+  static constexpr int kMiscOff = kBarOff + kNumBars * 8;  // TMEM base, abort flag
+  static constexpr int kBytes = kMiscOff + 16;
+  static constexpr int kDynamicBytes = kBytes + 1024;  // slack for 1024-B alignment
+};
+
+template <int D, bool BF16>
+__device__ __forceinline__ void issue_qk(uint32_t s_tmem, uint32_t q_smem, uint32_t k_smem) {
+  constexpr uint32_t idesc = idesc_f16_f32acc(kBlockM, kBlockN, BF16, false);
+#pragma unroll
+  for (int kk = 0; kk < D / 16; ++kk) {
+    const uint32_t off = (kk / 4) * kSubTileBytes + (kk % 4) * 32;
+    mma_ss(s_tmem, smem_desc_sw128(q_smem + off, 16, 1024), smem_desc_sw128(k_smem + off, 16, 1024),
+           idesc, kk > 0 ? 1u : 0u);
+  }
+}
+
+template <int D, bool BF16>
+__device__ __forceinline__ void issue_pv(uint32_t o_tmem, uint32_t p_tmem, uint32_t v_smem,
+                                         bool accumulate) {
+  constexpr uint32_t idesc = idesc_f16_f32acc(kBlockM, D, BF16, true);
+#pragma unroll
+  for (int kk = 0; kk < kBlockN / 16; ++kk) {
+    // P: 16 keys = 8 TMEM columns.  V: 16 keys = 16 rows of 128 B.
+    mma_ts(o_tmem, p_tmem + kk * 8, smem_desc_sw128(v_smem + kk * 16 * 128, kSubTileBytes, 1024),
+           idesc, (accumulate || kk > 0) ? 1u : 0u);
+  }
+}
+
+template <int D, bool BF16>
+__global__ void __launch_bounds__(kThreads, 1)
+    attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                    const __grid_constant__ CUtensorMap tm_v, const FwdParams p) {
+  using L = FwdSmem<D>;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_base = smem_u32(smem_raw);
+  const uint32_t sbase = (raw_base + 1023u) & ~1023u;
+  uint8_t* smem = smem_raw + (sbase - raw_base);
+  auto bar = [&](int i) -> uint32_t { return sbase + L::kBarOff + 8u * static_cast<uint32_t>(i); };
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kMiscOff);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kMiscOff + 4);
+
+  const int warp = threadIdx.x / 32;
+  const int lane = threadIdx.x % 32;
+
+  // Work unit: heaviest query-tile pairs first across all heads.
+  const int bh = blockIdx.x % p.BH;
+  const int pair = p.n_pairs - 1 - static_cast<int>(blockIdx.x / p.BH);
+  const int tile0 = 2 * pair;
+  const bool has1 = tile0 + 1 < p.n_tiles;
+  int n_kv[2];
+  n_kv[0] = p.causal ? tile0 + 1 : p.n_tiles;
+  n_kv[1] = has1 ? (p.causal ? tile0 + 2 : p.n_tiles) : 0;
+  const int n_max = n_kv[0] > n_kv[1] ? n_kv[0] : n_kv[1];
+
+  if (threadIdx.x == 0) {
+    mbar_init(bar(L::kBarQ), 1);
+    for (int s = 0; s < L::kStages; ++s) {
+      mbar_init(bar(L::kBarFull + s), 1);
+      mbar_init(bar(L::kBarEmpty + s), 1);
+    }
+    for (int t = 0; t < 2; ++t) {
+      mbar_init(bar(L::kBarS + t), 1);
+      mbar_init(bar(L::kBarP + t), 4);
+      mbar_init(bar(L::kBarO + t), 1);
+    }
+    mbar_init(bar(L::kBarDrain), 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 9) {
+    tmem_alloc(smem_u32(tmem_slot), kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  const uint32_t tmem = *tmem_slot;
+  const Watchdog wd{abort_flag, p.status, p.wait_limit_ns, p.timeout_code};
+
+  if (warp == 8) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      tma_prefetch_map(&tm_q);
+      tma_prefetch_map(&tm_k);
+      tma_prefetch_map(&tm_v);
+      const uint64_t pol_q = policy_evict_first();
+      const uint64_t pol_kv = policy_evict_last();
+      mbar_arrive_expect_tx(bar(L::kBarQ), (has1 ? 2 : 1) * L::kTileBytes);
+      for (int t = 0; t < (has1 ? 2 : 1); ++t) {
+        for (int s = 0; s < L::kSub; ++s) {
+          tma_load_3d(sbase + L::kQOff + t * L::kTileBytes + s * kSubTileBytes, &tm_q, bar(L::kBarQ),
+                      64 * s, (tile0 + t) * kBlockM, bh, pol_q);
+        }
+      }
+      int u = 0;  // ring uses issued: K_j is use 2j, V_j is use 2j + 1
+      bool ok = true;
+      for (int j = 0; j < n_max && ok; ++j) {
+        for (int which = 0; which < 2; ++which) {
+          const int slot = u % L::kStages;
+          const uint32_t phase = static_cast<uint32_t>(u / L::kStages) & 1u;
+          if (!wd.wait(bar(L::kBarEmpty + slot), phase ^ 1u)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(bar(L::kBarFull + slot), L::kTileBytes);
+          const CUtensorMap* map = which ? &tm_v : &tm_k;
+          for (int s = 0; s < L::kSub; ++s) {
+            tma_load_3d(sbase + L::kKVOff + slot * L::kTileBytes + s * kSubTileBytes, map,
+                        bar(L::kBarFull + slot), 64 * s, j * kBlockN, bh, pol_kv);
+          }
+          ++u;
+        }
+      }
+      // Let every copy this thread started land before the block can exit.
+      wd.drain(bar(L::kBarQ), 0);
+      for (int k = (u > L::kStages ? u - L::kStages : 0); k < u; ++k) {
+        wd.drain(bar(L::kBarFull + k % L::kStages), static_cast<uint32_t>(k / L::kStages) & 1u);
+      }
+    }
+  } else if (warp == 9) {
+    // ------------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      const uint32_t q_smem[2] = {sbase + L::kQOff, sbase + L::kQOff + L::kTileBytes};
+      const uint32_t s_tmem[2] = {tmem + 0, tmem + 128};
+      const uint32_t o_tmem[2] = {tmem + 256, tmem + 256 + D};
+      auto slot_smem = [&](int u) { return sbase + L::kKVOff + (u % L::kStages) * L::kTileBytes; };
+      auto full_parity = [&](int u) { return static_cast<uint32_t>(u / L::kStages) & 1u; };
+      do {
+        if (!wd.wait(bar(L::kBarQ), 0)) break;
+        if (!wd.wait(bar(L::kBarFull + 0), 0)) break;
+        tc_fence_after_sync();
+        for (int t = 0; t < 2; ++t) {
+          if (n_kv[t] > 0) {
+            issue_qk<D, BF16>(s_tmem[t], q_smem[t], slot_smem(0));
+            tc_commit(bar(L::kBarS + t));
+          }
+        }
+        tc_commit(bar(L::kBarEmpty + 0));
+        bool ok = true;
+        for (int j = 0; j < n_max && ok; ++j) {
+          const int uv = 2 * j + 1, uk = 2 * j + 2;
+          if (!wd.wait(bar(L::kBarFull + uv % L::kStages), full_parity(uv))) break;
+          tc_fence_after_sync();
+          bool k_ready = false;
+          for (int t = 0; t < 2 && ok; ++t) {
+            if (j >= n_kv[t]) continue;
+            if (!wd.wait(bar(L::kBarP + t), static_cast<uint32_t>(j) & 1u)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after_sync();
+            issue_pv<D, BF16>(o_tmem[t], s_tmem[t], slot_smem(uv), j > 0);
+            if (j + 1 < n_kv[t]) {
+              if (!k_ready) {
+                if (!wd.wait(bar(L::kBarFull + uk % L::kStages), full_parity(uk))) {
+                  ok = false;
+                  break;
+                }
+                tc_fence_after_sync();
+                k_ready = true;
+              }
+              issue_qk<D, BF16>(s_tmem[t], q_smem[t], slot_smem(uk));
+              tc_commit(bar(L::kBarS + t));
+            }
+          }
+          if (!ok) break;
+          tc_commit(bar(L::kBarEmpty + uv % L::kStages));
+          if (k_ready) tc_commit(bar(L::kBarEmpty + uk % L::kStages));
+          for (int t = 0; t < 2; ++t) {
+            if (j + 1 == n_kv[t]) tc_commit(bar(L::kBarO + t));
+          }
+        }
+      } while (false);
+      // Every MMA issued above must finish before TMEM is released.
+      tc_commit(bar(L::kBarDrain));
+      wd.drain(bar(L::kBarDrain), 0);
+    }
+  } else {
+    // ------------------------------------------------------------------ softmax
+    const int t = warp / 4;
+    const int wq = warp % 4;
+    const int r_local = wq * 32 + lane;
+    const int row = (tile0 + t) * kBlockM + r_local;
+    const uint32_t lane_base = static_cast<uint32_t>(wq * 32) << 16;
+    const uint32_t t_s = tmem + lane_base + 128u * t;
+    const uint32_t t_o = tmem + lane_base + 256u + static_cast<uint32_t>(D) * t;
+    const float c = p.scale_log2e;
+    float m_ref = -INFINITY;  // reference max, base-2 domain (already multiplied by c)
+    float l = 0.f;
+    bool ok = n_kv[t] > 0;
+    const bool ragged_keys = !p.causal && (p.N % kBlockN) != 0;
+    // Waits stay warp-uniform: the tcgen05.ld/st below are warp-collective.
+    auto warp_wait = [&](uint32_t b, uint32_t parity) -> bool {
+      const bool got = wd.wait(b, parity);
+      return __all_sync(0xffffffffu, got) != 0;
+    };
+    for (int j = 0; j < n_kv[t] && ok; ++j) {
+      if (!warp_wait(bar(L::kBarS + t), static_cast<uint32_t>(j) & 1u)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after_sync();
+      uint32_t s[4][32];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) tmem_ld_x32(t_s + 32u * q, s[q]);
+#pragma unroll
+      for (int q = 0; q < 4; ++q) tmem_wait_ld_x32(s[q]);
+
+      // Mask before the max: the diagonal tile (causal) or the ragged last tile (non-causal).
+      if (p.causal && j == tile0 + t) {
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+#pragma unroll
+          for (int i = 0; i < 32; ++i)
+            if (32 * q + i > r_local) s[q][i] = __float_as_uint(-INFINITY);
+      } else if (ragged_keys && j == p.n_tiles - 1) {
+        const int valid = p.N - j * kBlockN;
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+#pragma unroll
+          for (int i = 0; i < 32; ++i)
+            if (32 * q + i >= valid) s[q][i] = __float_as_uint(-INFINITY);
+      }
+
+      float mx0 = -INFINITY, mx1 = -INFINITY, mx2 = -INFINITY, mx3 = -INFINITY;
+#pragma unroll
+      for (int i = 0; i < 32; i += 2) {
+        mx0 = fmax3(mx0, __uint_as_float(s[0][i]), __uint_as_float(s[0][i + 1]));
+        mx1 = fmax3(mx1, __uint_as_float(s[1][i]), __uint_as_float(s[1][i + 1]));
+        mx2 = fmax3(mx2, __uint_as_float(s[2][i]), __uint_as_float(s[2][i + 1]));
+        mx3 = fmax3(mx3, __uint_as_float(s[3][i]), __uint_as_float(s[3][i + 1]));
+      }
+      const float m_tile = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * c;
+      float alpha = 1.f;
+      if (m_tile > m_ref + kRescaleThreshold) {
+        alpha = ex2(m_ref - m_tile);  // 0 on the first tile (m_ref = -inf)
+        m_ref = m_tile;
+      }
+      const float neg_m = m_ref == -INFINITY ? 0.f : -m_ref;
+
+      float sum0 = 0.f, sum1 = 0.f, sum2 = 0.f, sum3 = 0.f;
+      uint32_t pk[2][32];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+#pragma unroll
+        for (int i = 0; i < 32; i += 2) {
+          const float a = ex2(fmaf(__uint_as_float(s[q][i]), c, neg_m));
+          const float b = ex2(fmaf(__uint_as_float(s[q][i + 1]), c, neg_m));
+          if (q == 0) sum0 += a + b;
+          if (q == 1) sum1 += a + b;
+          if (q == 2) sum2 += a + b;
+          if (q == 3) sum3 += a + b;
+          pk[q / 2][(q % 2) * 16 + i / 2] = pack2<BF16>(a, b);
+        }
+      }
+      l = l * alpha + ((sum0 + sum1) + (sum2 + sum3));
+      tmem_st_x32(t_s, pk[0]);
+      tmem_st_x32(t_s + 32u, pk[1]);
+
+      // Rescale the running O before this tile's P V is added (PV of tile j-1 is
+      // complete: S of tile j was committed after it).
+      if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+#pragma unroll
+        for (int c0 = 0; c0 < D; c0 += 32) {
+          uint32_t o[32];
+          tmem_ld_x32(t_o + c0, o);
+          tmem_wait_ld_x32(o);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+          tmem_st_x32(t_o + c0, o);
+        }
+      }
+      tmem_wait_st();
+      tc_fence_before_sync();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(L::kBarP + t));
+    }
+
+    if (ok && warp_wait(bar(L::kBarO + t), 0)) {
+      tc_fence_after_sync();
+      const float inv_l = 1.f / l;
+      uint16_t* orow = static_cast<uint16_t*>(p.o) +
+                       (static_cast<size_t>(bh) * p.N + static_cast<size_t>(row)) * D;
+#pragma unroll
+      for (int c0 = 0; c0 < D; c0 += 32) {
+        uint32_t o[32];
+        tmem_ld_x32(t_o + c0, o);
+        tmem_wait_ld_x32(o);
+        uint32_t h[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i)
+          h[i] = pack2<BF16>(__uint_as_float(o[2 * i]) * inv_l, __uint_as_float(o[2 * i + 1]) * inv_l);
+        if (row < p.N) {
+          uint4* dst = reinterpret_cast<uint4*>(orow + c0);
+#pragma unroll
+          for (int v4 = 0; v4 < 4; ++v4)
+            dst[v4] = make_uint4(h[4 * v4], h[4 * v4 + 1], h[4 * v4 + 2], h[4 * v4 + 3]);
+        }
+      }
+      if (p.lse != nullptr && row < p.N) {
+        p.lse[static_cast<size_t>(bh) * p.N + row] = (m_ref + log2f(l)) * 0.69314718055994530942f;
+      }
+    }
+  }
+
+  tc_fence_before_sync();
+  __syncthreads();
+  if (warp == 9) {
+    __syncwarp();
+    tc_fence_after_sync();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+}  // namespace eca

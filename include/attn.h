@@ -1,0 +1,103 @@
+/*
+ * exact_causal_attention_gb300 -- C ABI of the attention forward library.
+ *
+ * The operation (page "CUDA FlashAttention：从在线 Softmax 到长序列 IO 极限",
+ * chengzipai.xyz, section 1) is the exact scaled-dot-product attention forward
+ *
+ *     O = softmax(scale * Q K^T + M) V,     M_ij = 0 if j <= i, else -inf  (causal)
+ *
+ * computed with the tiled online-softmax recurrence of that page's section 4,
+ * so the N x N score matrix is never written to memory.  It also returns the
+ * natural-log log-sum-exp of every score row, lse_i = ln sum_j exp(s_ij) with
+ * s_ij = scale * q_i . k_j over the unmasked j, which the page's section 7 says
+ * training must keep.
+ *
+ * Layout (all tensors contiguous, row-major, last index fastest):
+ *   q, k, v, o : [B, H, N, D] 16-bit elements (fp16 for attn_fwd, bf16 for
+ *                attn_fwd_bf16); one N serves queries and keys.
+ *   lse        : [B, H, N] fp32, or NULL to skip it.
+ * The causal mask is the top-left square one (key j visible to query i iff
+ * j <= i).  Arithmetic: fp16/bf16 products accumulated in fp32 on the tensor
+ * cores, running max m, sum l and unnormalised output o kept in fp32 (the page's
+ * section 2), probabilities rounded to the input type before the P V product,
+ * O rounded to nearest even.
+ *
+ * Ownership: every pointer is device memory owned by the caller; the library
+ * allocates nothing per call and keeps no reference after the call returns.
+ * Asynchrony: the call only enqueues work on `stream` (NULL = legacy default
+ * stream) and never synchronises; a fault during execution surfaces at the
+ * caller's next synchronisation.  Calls may come from several host threads.
+ *
+ * Errors: arguments are checked before anything touches the GPU; an invalid
+ * call returns a negative status and launches nothing (section 9 of the page:
+ * unsupported shapes are rejected, never answered wrongly).
+ */
+#ifndef EXACT_CAUSAL_ATTENTION_GB300_ATTN_H_
+#define EXACT_CAUSAL_ATTENTION_GB300_ATTN_H_
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* A cudaStream_t, declared without the CUDA headers. */
+typedef struct CUstream_st* attn_stream_t;
+
+enum attn_status {
+  ATTN_OK = 0,
+  ATTN_ERR_INVALID_ARG = -1,    /* NULL tensor pointer, B/H/N < 1, scale not finite and > 0,
+                                   or sizes whose offsets overflow 64 bits / TMA limits */
+  ATTN_ERR_UNALIGNED = -2,      /* a tensor pointer is not 16-byte aligned */
+  ATTN_ERR_UNSUPPORTED_D = -3,  /* D is not 64 or 128 */
+  ATTN_ERR_ARCH = -4,           /* the current device is not an sm_103 part */
+  ATTN_ERR_LAUNCH = -5,         /* the CUDA runtime refused the launch (cudaGetLastError) */
+  ATTN_ERR_TIMEOUT = -6,        /* a kernel's bounded wait expired (reported by attn_device_status) */
+  ATTN_ERR_CUDA = -7            /* another CUDA runtime/driver call failed */
+};
+
+/*
+ * attn_fwd -- fp16 attention forward.
+ *   q, k, v : device, [B, H, N, D] fp16, 16-byte aligned, read only.
+ *   o       : device, [B, H, N, D] fp16, 16-byte aligned, written in full.
+ *   lse     : device, [B, H, N] fp32, 4-byte aligned, written in full; or NULL.
+ *   B, H, N : >= 1.   D : 64 or 128.   causal : 0 or nonzero.
+ *   scale   : finite and > 0 (1/sqrt(D) for the usual attention).
+ *   stream  : the caller's CUDA stream.
+ * o must not overlap q, k or v.  Returns ATTN_OK or a negative attn_status.
+ */
+int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N,
+             int D, int causal, float scale, attn_stream_t stream);
+
+/* attn_fwd_bf16 -- the same operation and contract with bf16 q, k, v and o. */
+int attn_fwd_bf16(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+                  int N, int D, int causal, float scale, attn_stream_t stream);
+
+/*
+ * attn_device_status -- synchronises `stream`, then reads and clears the
+ * library's device status word for the current device.  Returns ATTN_OK, or
+ * ATTN_ERR_TIMEOUT if a kernel enqueued since the last call gave up on a
+ * bounded wait (its outputs are then incomplete), or ATTN_ERR_CUDA if the
+ * synchronisation itself failed.
+ */
+int attn_device_status(attn_stream_t stream);
+
+/*
+ * attn_watchdog_selftest -- launches one block whose thread waits on a
+ * shared-memory barrier that nothing ever completes, with a limit of
+ * `timeout_us` microseconds (1 .. 10,000,000).  The wait gives up, the kernel
+ * records ATTN_ERR_TIMEOUT in the device status word and returns normally; a
+ * following attn_device_status(stream) reports it.  Exists so that the
+ * bounded-wait path can be tested without faulting or hanging a GPU.
+ */
+int attn_watchdog_selftest(unsigned int timeout_us, attn_stream_t stream);
+
+/* Text for a status code (static storage, never NULL). */
+const char* attn_status_string(int status);
+
+/* Library version, major * 10000 + minor * 100 + patch. */
+int attn_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* EXACT_CAUSAL_ATTENTION_GB300_ATTN_H_ */

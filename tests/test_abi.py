@@ -1,0 +1,89 @@
+"""The C ABI without a GPU: the library loads, exports every function that
+include/attn.h declares, and rejects bad arguments before any CUDA call."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import exact_causal_attention_gb300 as eca
+from exact_causal_attention_gb300 import build
+
+HEADER = os.path.join(build.INCLUDE, "attn.h")
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?\w+\s*\*?\s*(attn_\w+)\s*\(", text, flags=re.M)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return eca.load_library()
+
+
+def test_header_declares_the_expected_entry_points():
+    names = declared_functions()
+    assert "attn_fwd" in names and "attn_fwd_bf16" in names
+    assert set(names) == set(eca.SIGNATURES), names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+
+
+def test_version_and_status_strings(lib):
+    assert lib.attn_version() >= 100
+    for code, name in eca.STATUS.items():
+        text = lib.attn_status_string(code).decode()
+        assert text and text != "unknown status", name
+    assert lib.attn_status_string(12345).decode() == "unknown status"
+
+
+# Fake, never-dereferenced addresses: every case below must be refused by the
+# host-side checks, which run before the library touches CUDA.
+A = 0x10000000
+SZ = 1 << 24
+
+
+def call(lib, fn="attn_fwd", q=A, k=A + SZ, v=A + 2 * SZ, o=A + 3 * SZ, lse=None, B=1, H=1, N=16, D=64,
+         causal=1, scale=0.125):
+    return getattr(lib, fn)(q, k, v, o, lse, B, H, N, D, causal, scale, None)
+
+
+@pytest.mark.parametrize("fn", ["attn_fwd", "attn_fwd_bf16"])
+def test_argument_errors_without_gpu(lib, fn):
+    assert call(lib, fn, q=None) == -1
+    assert call(lib, fn, o=None) == -1
+    assert call(lib, fn, B=0) == -1
+    assert call(lib, fn, H=-3) == -1
+    assert call(lib, fn, N=0) == -1
+    assert call(lib, fn, D=96) == -3
+    assert call(lib, fn, D=256) == -3
+    assert call(lib, fn, scale=0.0) == -1
+    assert call(lib, fn, scale=-0.5) == -1
+    assert call(lib, fn, scale=float("inf")) == -1
+    assert call(lib, fn, scale=float("nan")) == -1
+    assert call(lib, fn, q=A + 2) == -2
+    assert call(lib, fn, o=A + 3 * SZ + 8) == -2
+    assert call(lib, fn, lse=A + 4 * SZ + 2) == -2
+    # o overlapping an input
+    assert call(lib, fn, o=A + 16) == -1
+    # grid / tensor-map limits
+    assert call(lib, fn, B=1 << 16, H=1 << 16) == -1
+
+
+def test_selftest_rejects_bad_timeouts(lib):
+    assert lib.attn_watchdog_selftest(0, None) == -1
+    assert lib.attn_watchdog_selftest(10_000_001, None) == -1
+
+
+def test_binding_rejects_cpu_tensors():
+    import torch
+
+    x = torch.zeros(1, 1, 4, 64, dtype=torch.float16)
+    with pytest.raises(TypeError):
+        eca.attn_fwd(x, x, x)

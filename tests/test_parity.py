@@ -1,0 +1,150 @@
+"""GPU parity: the CUDA path through the C ABI against the FP64 oracle.
+
+Same seeded inputs on both sides (exact fp16/bf16 bytes); outputs NaN-filled
+before every call (the coverage trap of section 3.4 of the lpnh.cn "Softmax
+kernels V1-V9" page); tolerances in tests/helpers.py.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+from exact_causal_attention_gb300 import inputs
+
+from helpers import compare, oracle_full, oracle_rows, run_gpu, sample_rows
+
+pytestmark = pytest.mark.gpu
+
+FULL = [n for n in inputs.WORKLOADS if n != "causal_b1_h32_n8192_d128_fp16"]
+
+
+@pytest.mark.parametrize("name", FULL)
+def test_workload_all_rows(cuda_lib, name):
+    w = inputs.WORKLOADS[name]
+    q, k, v = inputs.workload_qkv(w)
+    o, lse = run_gpu(q, k, v, w.causal, w.scale)
+    ro, rl = oracle_full(q, k, v, w.dtype, w.causal, w.scale)
+    stats = compare(o, lse, ro, rl, w.dtype)
+    print(name, stats)
+
+
+def test_n8192_sampled_rows(cuda_lib):
+    w = inputs.WORKLOADS["causal_b1_h32_n8192_d128_fp16"]
+    q, k, v = inputs.workload_qkv(w)
+    o, lse = run_gpu(q, k, v, w.causal, w.scale)
+    rows = sample_rows(w.B, w.H, w.N, 320, seed=3)
+    ro, rl = oracle_rows(q, k, v, w.dtype, w.causal, w.scale, rows)
+    bh = np.array([r[0] for r in rows])
+    i = np.array([r[1] for r in rows])
+    og = o.reshape(w.B * w.H, w.N, w.D)[bh, i]
+    lg = lse.reshape(w.B * w.H, w.N)[bh, i]
+    stats = compare(og, lg, ro, rl, w.dtype)
+    assert np.isfinite(o).all() and np.isfinite(lse).all()
+    print(w.name, stats)
+
+
+EDGE_N = [1, 2, 127, 128, 129, 255, 256, 257, 383, 513, 1000]
+
+
+@pytest.mark.parametrize("dtype", ["fp16", "bf16"])
+@pytest.mark.parametrize("D", [64, 128])
+@pytest.mark.parametrize("causal", [True, False])
+@pytest.mark.parametrize("N", EDGE_N)
+def test_edge_lengths(cuda_lib, N, causal, D, dtype):
+    B, H = (2, 3) if N < 300 else (1, 2)
+    q, k, v = inputs.make_qkv(B, H, N, D, dtype, seed=1000 + N + D, qk_std=1.5)
+    scale = 1.0 / math.sqrt(D)
+    o, lse = run_gpu(q, k, v, causal, scale)
+    ro, rl = oracle_full(q, k, v, dtype, causal, scale)
+    compare(o, lse, ro, rl, dtype)
+
+
+@pytest.mark.parametrize("causal", [True, False])
+def test_zero_queries_give_prefix_mean_at_full_size(cuda_lib, causal):
+    # Q = 0: every visible score is 0, so O_i is the mean of the visible v_j and
+    # lse_i = ln(count): a closed form that needs no oracle at any size.
+    B, H, N, D = 1, 4, 8192, 128
+    _, _, v = inputs.make_qkv(B, H, N, D, "fp16", seed=77)
+    q = torch.zeros_like(v)
+    k = torch.randn(v.shape, generator=torch.Generator().manual_seed(78)).to(torch.float16)
+    o, lse = run_gpu(q, k, v, causal, 1.0 / math.sqrt(D))
+    vd = v.double().numpy()
+    if causal:
+        ref = np.cumsum(vd, axis=2) / np.arange(1, N + 1)[None, None, :, None]
+        ref_l = np.log(np.arange(1, N + 1, dtype=np.float64))[None, None, :]
+    else:
+        ref = np.broadcast_to(vd.mean(axis=2, keepdims=True), vd.shape)
+        ref_l = np.full((1, 1, N), math.log(N))
+    assert np.abs(o - ref).max() <= 2e-3
+    assert np.abs(lse - ref_l).max() <= 1e-4
+
+
+@pytest.mark.parametrize("dtype", ["fp16", "bf16"])
+def test_values_all_ones_give_ones(cuda_lib, dtype):
+    # rows of softmax sum to one: V = 1 gives O = 1 up to rounding of P.
+    B, H, N, D = 2, 4, 2000, 64
+    q, k, _ = inputs.make_qkv(B, H, N, D, dtype, seed=5, qk_std=3.0)
+    v = torch.ones_like(q)
+    o, _ = run_gpu(q, k, v, True, 0.125)
+    tol = 4e-3 if dtype == "fp16" else 1.6e-2
+    assert np.abs(o - 1.0).max() <= tol
+
+
+def test_key_shift_invariance_through_the_abi(cuda_lib):
+    # Integer-valued inputs so k + u is exact in fp16: O unchanged, lse shifted by scale*q.u.
+    B, H, N, D = 1, 2, 1000, 64
+    g = torch.Generator().manual_seed(11)
+    q = torch.randint(-2, 3, (B, H, N, D), generator=g).to(torch.float16)
+    k = torch.randint(-2, 3, (B, H, N, D), generator=g).to(torch.float16)
+    v = torch.randn((B, H, N, D), generator=g).to(torch.float16)
+    u = torch.randint(-3, 4, (D,), generator=g).to(torch.float16)
+    scale = 0.125
+    o1, l1 = run_gpu(q, k, v, True, scale)
+    o2, l2 = run_gpu(q, k + u, v, True, scale)
+    shift = scale * (q.double() @ u.double()).numpy()
+    assert np.abs(o2 - o1).max() <= 2e-3
+    assert np.abs((l2 - l1) - shift).max() <= 1e-4
+
+
+def test_heads_independent_and_deterministic(cuda_lib):
+    B, H, N, D = 2, 3, 700, 128
+    q, k, v = inputs.make_qkv(B, H, N, D, "fp16", seed=21)
+    o, lse = run_gpu(q, k, v, True, 0.09)
+    o2, lse2 = run_gpu(q, k, v, True, 0.09)
+    assert np.array_equal(o, o2) and np.array_equal(lse, lse2)
+    for b, h in [(0, 0), (1, 2), (0, 1)]:
+        sl = (slice(b, b + 1), slice(h, h + 1))
+        os_, ls_ = run_gpu(q[sl].contiguous(), k[sl].contiguous(), v[sl].contiguous(), True, 0.09)
+        assert np.array_equal(os_[0, 0], o[b, h]) and np.array_equal(ls_[0, 0], lse[b, h])
+
+
+def test_lse_null_and_side_stream(cuda_lib):
+    import exact_causal_attention_gb300 as eca
+
+    q, k, v = (x.cuda() for x in inputs.make_qkv(1, 2, 300, 64, "bf16", seed=31))
+    o_ref, _ = eca.attn_fwd(q, k, v, causal=True)
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        o = torch.full_like(q, float("nan"))
+        eca.attn_fwd_into(q, k, v, o, None, causal=True, stream=s)
+    s.synchronize()
+    assert torch.equal(o, o_ref)
+
+
+def test_rejections_on_device(cuda_lib):
+    import exact_causal_attention_gb300 as eca
+
+    x = torch.zeros(1, 1, 64, 64 + 8, dtype=torch.float16, device="cuda")
+    q = x[..., 1:65]  # not contiguous
+    with pytest.raises(ValueError):
+        eca.attn_fwd(q, q, q)
+    flat = torch.zeros(1 + 64 * 64, dtype=torch.float16, device="cuda")
+    mis = flat[1:].view(1, 1, 64, 64)  # 2-byte offset
+    with pytest.raises(eca.AttnError) as e:
+        eca.attn_fwd(mis, mis, mis)
+    assert e.value.status == -2
+    d96 = torch.zeros(1, 1, 64, 96, dtype=torch.float16, device="cuda")
+    with pytest.raises(eca.AttnError) as e:
+        eca.attn_fwd(d96, d96, d96)
+    assert e.value.status == -3
