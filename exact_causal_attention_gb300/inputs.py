@@ -5,10 +5,13 @@ stands in for the workloads of "CUDA FlashAttentionï¼šä»Žåœ¨çº¿ Softmax åˆ°é•¿åº
 (section 1 and the section 8 benchmark: B=1, H=32, D=128, N from 512 to 8192):
 
 * one CPU ``torch.Generator`` seeded with the workload's seed;
-* ``torch.randn(B, H, N, D)`` in float32 three times, in the order q, k, v;
+* ``torch.randn(B, H, N, D)`` in float64 three times, in the order q, k, v
+  (float64 so the draw is the same on x86 and Arm hosts: torch's float32 path
+  is vectorised differently per CPU, while an ulp-level difference in a float64
+  draw survives the rounding to 16 bits with negligible probability);
 * q and k multiplied by ``qk_std`` (3 for the stress case so that scores reach
   tens and the max subtraction matters), v left at N(0, 1);
-* one round-to-nearest-even cast to fp16 or bf16.
+* round-to-nearest-even to float32, then to fp16 or bf16.
 
 The tensors stay on the CPU; callers move them to the device.
 """
@@ -75,14 +78,14 @@ def sweep_workload(n: int, seed: int = 1) -> Workload:
 def make_qkv(B: int, H: int, N: int, D: int, dtype: str, seed: int, qk_std: float = 1.0):
     """Return CPU tensors (q, k, v) of shape [B, H, N, D] in fp16 or bf16."""
     g = torch.Generator(device="cpu").manual_seed(int(seed))
-    q = torch.randn(B, H, N, D, generator=g, dtype=torch.float32)
-    k = torch.randn(B, H, N, D, generator=g, dtype=torch.float32)
-    v = torch.randn(B, H, N, D, generator=g, dtype=torch.float32)
+    q = torch.randn(B, H, N, D, generator=g, dtype=torch.float64)
+    k = torch.randn(B, H, N, D, generator=g, dtype=torch.float64)
+    v = torch.randn(B, H, N, D, generator=g, dtype=torch.float64)
     if qk_std != 1.0:
         q.mul_(qk_std)
         k.mul_(qk_std)
     t = TORCH_DTYPES[dtype]
-    return q.to(t), k.to(t), v.to(t)
+    return tuple(x.to(torch.float32).to(t) for x in (q, k, v))
 
 
 def workload_qkv(w: Workload):

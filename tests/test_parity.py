@@ -12,7 +12,7 @@ import torch
 
 from exact_causal_attention_gb300 import inputs
 
-from helpers import compare, oracle_full, oracle_rows, run_gpu, sample_rows
+from helpers import compare, oracle_full, oracle_rows, p_rounding_term, run_gpu, sample_rows
 
 pytestmark = pytest.mark.gpu
 
@@ -25,7 +25,7 @@ def test_workload_all_rows(cuda_lib, name):
     q, k, v = inputs.workload_qkv(w)
     o, lse = run_gpu(q, k, v, w.causal, w.scale)
     ro, rl = oracle_full(q, k, v, w.dtype, w.causal, w.scale)
-    stats = compare(o, lse, ro, rl, w.dtype)
+    stats = compare(o, lse, ro, rl, w.dtype, p_rounding_term(q, k, v, w.dtype, w.causal, w.scale))
     print(name, stats)
 
 
@@ -57,7 +57,7 @@ def test_edge_lengths(cuda_lib, N, causal, D, dtype):
     scale = 1.0 / math.sqrt(D)
     o, lse = run_gpu(q, k, v, causal, scale)
     ro, rl = oracle_full(q, k, v, dtype, causal, scale)
-    compare(o, lse, ro, rl, dtype)
+    compare(o, lse, ro, rl, dtype, p_rounding_term(q, k, v, dtype, causal, scale))
 
 
 @pytest.mark.parametrize("causal", [True, False])
