@@ -70,14 +70,18 @@ def kernel_source_hash():
 
 def recorded_traffic():
     """DRAM bytes per launch from the committed ncu summary, if it matches the current kernel."""
-    path = os.path.join(PROFILES, "attn_fwd_n8192_traffic.json")
+    path = os.path.join(PROFILES, "attn_fwd_n8192_traffic.txt")
     if not os.path.exists(path):
         return None
+    rec = {}
     with open(path) as f:
-        rec = json.load(f)
+        for line in f:
+            if ":" in line:
+                key, val = line.split(":", 1)
+                rec[key.strip()] = val.strip()
     if rec.get("kernel_source_sha256_16") != kernel_source_hash() or rec.get("workload") != WORKLOAD:
         return None
-    return rec.get("dram_bytes_per_launch")
+    return int(rec["dram_bytes_per_launch"])
 
 
 class ClockSampler:
@@ -139,31 +143,41 @@ class ClockSampler:
                 "samples": len(sm)}
 
 
-def oracle_rows_tflops(q, k, v, w, seconds_target, seed):
-    """Time the FP64 oracle on random query rows of the workload; returns (TFLOP/s, rows, seconds)."""
-    import numpy as np
+class OracleSampler:
+    """The FP64 oracle timed on random query rows of a workload (inputs decoded once)."""
 
-    import oracle
-    from exact_causal_attention_gb300 import inputs
+    def __init__(self, q, k, v, w):
+        import oracle
+        from exact_causal_attention_gb300 import inputs
 
-    qd, kd, vd = (oracle.decode(inputs.bits(x), w.dtype) for x in (q, k, v))
-    rng = np.random.default_rng(seed)
+        self.w = w
+        self.qd, self.kd, self.vd = (oracle.decode(inputs.bits(x), w.dtype) for x in (q, k, v))
+        self.rows_per_s = None
 
-    def flops(rows):
+    def flops(self, rows):
+        w = self.w
         return float(sum(4.0 * w.D * ((i + 1) if w.causal else w.N) for _, i in rows))
 
-    def run(count):
+    def run(self, count, seed):
+        """Returns (TFLOP/s, rows, seconds) for `count` seeded random rows."""
+        import numpy as np
+
+        import oracle
+
+        w = self.w
+        rng = np.random.default_rng(seed)
         rows = [(int(rng.integers(0, w.B * w.H)), int(rng.integers(0, w.N))) for _ in range(count)]
         t0 = time.perf_counter()
-        oracle.attention_rows(qd, kd, vd, w.causal, w.scale, rows)
-        return rows, time.perf_counter() - t0
+        oracle.attention_rows(self.qd, self.kd, self.vd, w.causal, w.scale, rows)
+        dt = time.perf_counter() - t0
+        return self.flops(rows) / dt / 1e12, len(rows), dt
 
-    rows, dt = run(4 * host_cores())
-    rate = flops(rows) / max(dt, 1e-9)
-    per_row = flops(rows) / len(rows)
-    count = max(host_cores(), int(seconds_target * rate / per_row))
-    rows, dt = run(count)
-    return flops(rows) / dt / 1e12, len(rows), dt
+    def timed(self, seconds, seed):
+        """A sample sized to take about `seconds` on this host."""
+        if self.rows_per_s is None:
+            _, n, dt = self.run(4 * host_cores(), seed + 99991)
+            self.rows_per_s = n / max(dt, 1e-9)
+        return self.run(max(host_cores(), int(seconds * self.rows_per_s)), seed)
 
 
 def bench_reference(args, w):
@@ -173,16 +187,17 @@ def bench_reference(args, w):
     from exact_causal_attention_gb300 import inputs
 
     q, k, v = inputs.workload_qkv(w)
-    per_step = max(1.0, 60.0 / max(1, args.steps + args.warmup))
+    sampler = OracleSampler(q, k, v, w)
+    per_step = max(0.02, 60.0 / max(1, args.steps + args.warmup))
     for s in range(args.warmup):
-        oracle_rows_tflops(q, k, v, w, min(per_step, 2.0), seed=100 + s)
-    vals, secs, nrows = [], 0.0, 0
+        sampler.timed(per_step, seed=100 + s)
+    flops, secs, nrows = 0.0, 0.0, 0
     for s in range(args.steps):
-        tf, n, dt = oracle_rows_tflops(q, k, v, w, per_step, seed=200 + s)
-        vals.append(tf)
+        tf, n, dt = sampler.timed(per_step, seed=200 + s)
+        flops += tf * 1e12 * dt
         secs += dt
         nrows += n
-    value = sum(vals) / len(vals)
+    value = flops / secs / 1e12
     cores = host_cores()
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus,
@@ -330,7 +345,7 @@ def bench_ours(args, w):
 
     cpu = None
     if rank == 0 and not args.no_cpu:
-        tf, nrows, secs = oracle_rows_tflops(q, k, v, w, args.cpu_seconds, seed=7)
+        tf, nrows, secs = OracleSampler(q, k, v, w).timed(args.cpu_seconds, seed=7)
         cpu = {"value": tf, "unit": "TFLOP/s", "cores": host_cores(), "kind": "oracle",
                "sample": f"{nrows} random query rows of the workload ({secs:.1f} s, two-pass FP64 oracle, "
                          f"{host_cores()} threads)"}
@@ -372,7 +387,7 @@ def bench_ours(args, w):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=300)
+    ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-sweep", action="store_true")
