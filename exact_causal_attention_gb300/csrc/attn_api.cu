@@ -27,6 +27,7 @@ using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t
 struct DeviceState {
   bool probed = false;
   bool sm103 = false;
+  int sm_count = 0;
   int* status = nullptr;    // address of g_device_status on this device
   unsigned configured = 0;  // bitmask of kernel instantiations with smem attribute set
 };
@@ -62,6 +63,10 @@ int device_state(DeviceState** out) {
       return ATTN_ERR_CUDA;
     }
     st.sm103 = (major == 10 && minor == 3);
+    if (cudaDeviceGetAttribute(&st.sm_count, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+        st.sm_count < 1) {
+      return ATTN_ERR_CUDA;
+    }
     if (st.sm103) {
       void* addr = nullptr;
       if (cudaGetSymbolAddress(&addr, g_device_status) != cudaSuccess) return ATTN_ERR_CUDA;
@@ -146,11 +151,13 @@ int launch(const void* q, const void* k, const void* v, void* o, float* lse, int
   p.n_tiles = (N + eca::kBlockM - 1) / eca::kBlockM;
   p.n_pairs = (p.n_tiles + 1) / 2;
   p.BH = BH;
+  p.n_units = p.n_pairs * BH;
   p.causal = causal ? 1 : 0;
   p.scale_log2e = scale * 1.4426950408889634f;
   p.wait_limit_ns = kWaitLimitNs;
   p.timeout_code = ATTN_ERR_TIMEOUT;
-  const unsigned grid = static_cast<unsigned>(p.n_pairs) * static_cast<unsigned>(BH);
+  // Persistent: one CTA per SM (the shared-memory footprint admits only one), never more than the units.
+  const unsigned grid = static_cast<unsigned>(p.n_units < st->sm_count ? p.n_units : st->sm_count);
   kernel<<<grid, eca::kThreads, L::kDynamicBytes, stream>>>(tq, tk, tv, p);
   return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_LAUNCH;
 }

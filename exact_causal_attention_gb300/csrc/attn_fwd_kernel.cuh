@@ -11,7 +11,12 @@
 // the diagonal, mask element-wise only on the diagonal tile; keep the LSE).
 //
 // GB300 mapping (differs from the page's mma.sync / cp.async design):
-//   * one CTA = two 128-row query tiles of one (batch, head); 320 threads:
+//   * persistent CTAs, one per SM; a work unit is two consecutive 128-row query
+//     tiles of one (batch, head).  Units are ordered heaviest first (causal work
+//     grows with the tile index) and dealt to the CTAs in zig-zag waves.  The
+//     next unit's Q load starts as soon as the current unit's last Q K^T MMA is
+//     done, and its first P V only waits until that tile's epilogue has read O,
+//     so unit boundaries overlap.  320 threads:
 //       warps 0-3  softmax for query tile 0     warps 4-7  softmax for query tile 1
 //       warp 8     TMA producer (Q once, then K_j, V_j into a ring of smem slots)
 //       warp 9     TMEM owner and single-thread tcgen05.mma issuer
@@ -49,6 +54,7 @@ struct FwdParams {
   int n_tiles;    // ceil(N / 128), for queries and keys alike
   int n_pairs;    // ceil(n_tiles / 2)
   int BH;
+  int n_units;    // n_pairs * BH
   int causal;
   float scale_log2e;  // scale * log2(e)
   unsigned long long wait_limit_ns;
@@ -64,18 +70,46 @@ struct FwdSmem {
   static constexpr int kKVOff = 2 * kTileBytes;
   static constexpr int kBarOff = kKVOff + kStages * kTileBytes;
   // barrier indices
-  static constexpr int kBarQ = 0;
-  static constexpr int kBarFull = 1;
+  static constexpr int kBarQFull = 0;
+  static constexpr int kBarQFree = 1;
+  static constexpr int kBarFull = 2;
   static constexpr int kBarEmpty = kBarFull + kStages;
-  static constexpr int kBarS = kBarEmpty + kStages;  // + t
-  static constexpr int kBarP = kBarS + 2;            // + t
-  static constexpr int kBarO = kBarP + 2;            // + t
-  static constexpr int kBarDrain = kBarO + 2;
+  static constexpr int kBarS = kBarEmpty + kStages;  // + t: S_t computed
+  static constexpr int kBarP = kBarS + 2;            // + t: P_t written (and O_t rescaled)
+  static constexpr int kBarO = kBarP + 2;            // + t: last P V of the unit done
+  static constexpr int kBarOFree = kBarO + 2;        // + t: epilogue has read O_t
+  static constexpr int kBarDrain = kBarOFree + 2;
   static constexpr int kNumBars = kBarDrain + 1;
   static constexpr int kMiscOff = kBarOff + kNumBars * 8;  // TMEM base, abort flag
   static constexpr int kBytes = kMiscOff + 16;
   static constexpr int kDynamicBytes = kBytes + 1024;  // slack for 1024-B alignment
 };
+
+// One work unit: query tiles 2*pair and 2*pair + 1 of slice bh.
+struct Unit {
+  int bh;
+  int tile0;
+  int n_kv[2];  // key tiles each query tile needs (0 = tile absent)
+  int n_max;
+};
+
+// The k-th unit of this CTA (zig-zag over waves of gridDim.x units, heaviest
+// first).  False once the CTA has no more work.
+__device__ __forceinline__ bool unit_at(int k, const FwdParams& p, Unit& u) {
+  const int G = static_cast<int>(gridDim.x);
+  const int c = static_cast<int>(blockIdx.x);
+  const long long L = static_cast<long long>(k) * G + ((k & 1) ? (G - 1 - c) : c);
+  if (L >= p.n_units) return false;
+  const int l = static_cast<int>(L);
+  u.bh = l % p.BH;
+  const int pair = p.n_pairs - 1 - l / p.BH;
+  u.tile0 = 2 * pair;
+  const bool has1 = u.tile0 + 1 < p.n_tiles;
+  u.n_kv[0] = p.causal ? u.tile0 + 1 : p.n_tiles;
+  u.n_kv[1] = has1 ? (p.causal ? u.tile0 + 2 : p.n_tiles) : 0;
+  u.n_max = u.n_kv[0] > u.n_kv[1] ? u.n_kv[0] : u.n_kv[1];
+  return true;
+}
 
 template <int D, bool BF16>
 __device__ __forceinline__ void issue_qk(uint32_t s_tmem, uint32_t q_smem, uint32_t k_smem) {
@@ -100,6 +134,8 @@ __device__ __forceinline__ void issue_pv(uint32_t o_tmem, uint32_t p_tmem, uint3
   }
 }
 
+__device__ __forceinline__ uint32_t parity(int count) { return static_cast<uint32_t>(count) & 1u; }
+
 template <int D, bool BF16>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
@@ -116,18 +152,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int warp = threadIdx.x / 32;
   const int lane = threadIdx.x % 32;
 
-  // Work unit: heaviest query-tile pairs first across all heads.
-  const int bh = blockIdx.x % p.BH;
-  const int pair = p.n_pairs - 1 - static_cast<int>(blockIdx.x / p.BH);
-  const int tile0 = 2 * pair;
-  const bool has1 = tile0 + 1 < p.n_tiles;
-  int n_kv[2];
-  n_kv[0] = p.causal ? tile0 + 1 : p.n_tiles;
-  n_kv[1] = has1 ? (p.causal ? tile0 + 2 : p.n_tiles) : 0;
-  const int n_max = n_kv[0] > n_kv[1] ? n_kv[0] : n_kv[1];
-
   if (threadIdx.x == 0) {
-    mbar_init(bar(L::kBarQ), 1);
+    mbar_init(bar(L::kBarQFull), 1);
+    mbar_init(bar(L::kBarQFree), 1);
     for (int s = 0; s < L::kStages; ++s) {
       mbar_init(bar(L::kBarFull + s), 1);
       mbar_init(bar(L::kBarEmpty + s), 1);
@@ -136,6 +163,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(bar(L::kBarS + t), 1);
       mbar_init(bar(L::kBarP + t), 4);
       mbar_init(bar(L::kBarO + t), 1);
+      mbar_init(bar(L::kBarOFree + t), 4);
     }
     mbar_init(bar(L::kBarDrain), 1);
     *abort_flag = 0;
@@ -159,92 +187,117 @@ __global__ void __launch_bounds__(kThreads, 1)
       tma_prefetch_map(&tm_v);
       const uint64_t pol_q = policy_evict_first();
       const uint64_t pol_kv = policy_evict_last();
-      mbar_arrive_expect_tx(bar(L::kBarQ), (has1 ? 2 : 1) * L::kTileBytes);
-      for (int t = 0; t < (has1 ? 2 : 1); ++t) {
-        for (int s = 0; s < L::kSub; ++s) {
-          tma_load_3d(sbase + L::kQOff + t * L::kTileBytes + s * kSubTileBytes, &tm_q, bar(L::kBarQ),
-                      64 * s, (tile0 + t) * kBlockM, bh, pol_q);
-        }
-      }
-      int u = 0;  // ring uses issued: K_j is use 2j, V_j is use 2j + 1
+      int u = 0;       // ring uses issued: K_j of a unit is use base + 2j, V_j is base + 2j + 1
+      int units = 0;   // Q loads issued
       bool ok = true;
-      for (int j = 0; j < n_max && ok; ++j) {
-        for (int which = 0; which < 2; ++which) {
-          const int slot = u % L::kStages;
-          const uint32_t phase = static_cast<uint32_t>(u / L::kStages) & 1u;
-          if (!wd.wait(bar(L::kBarEmpty + slot), phase ^ 1u)) {
-            ok = false;
-            break;
-          }
-          mbar_arrive_expect_tx(bar(L::kBarFull + slot), L::kTileBytes);
-          const CUtensorMap* map = which ? &tm_v : &tm_k;
+      Unit w;
+      for (int k = 0; ok && unit_at(k, p, w); ++k) {
+        // The Q buffer is reused: wait until every Q K^T of the previous unit is done.
+        if (k > 0 && !wd.wait(bar(L::kBarQFree), parity(k - 1))) break;
+        const int nq = w.n_kv[1] > 0 ? 2 : 1;
+        mbar_arrive_expect_tx(bar(L::kBarQFull), nq * L::kTileBytes);
+        for (int t = 0; t < nq; ++t) {
           for (int s = 0; s < L::kSub; ++s) {
-            tma_load_3d(sbase + L::kKVOff + slot * L::kTileBytes + s * kSubTileBytes, map,
-                        bar(L::kBarFull + slot), 64 * s, j * kBlockN, bh, pol_kv);
+            tma_load_3d(sbase + L::kQOff + t * L::kTileBytes + s * kSubTileBytes, &tm_q,
+                        bar(L::kBarQFull), 64 * s, (w.tile0 + t) * kBlockM, w.bh, pol_q);
           }
-          ++u;
+        }
+        ++units;
+        for (int j = 0; j < w.n_max && ok; ++j) {
+          for (int which = 0; which < 2; ++which) {
+            const int slot = u % L::kStages;
+            if (!wd.wait(bar(L::kBarEmpty + slot), parity(u / L::kStages) ^ 1u)) {
+              ok = false;
+              break;
+            }
+            mbar_arrive_expect_tx(bar(L::kBarFull + slot), L::kTileBytes);
+            const CUtensorMap* map = which ? &tm_v : &tm_k;
+            for (int s = 0; s < L::kSub; ++s) {
+              tma_load_3d(sbase + L::kKVOff + slot * L::kTileBytes + s * kSubTileBytes, map,
+                          bar(L::kBarFull + slot), 64 * s, j * kBlockN, w.bh, pol_kv);
+            }
+            ++u;
+          }
         }
       }
       // Let every copy this thread started land before the block can exit.
-      wd.drain(bar(L::kBarQ), 0);
-      for (int k = (u > L::kStages ? u - L::kStages : 0); k < u; ++k) {
-        wd.drain(bar(L::kBarFull + k % L::kStages), static_cast<uint32_t>(k / L::kStages) & 1u);
+      if (units > 0) wd.drain(bar(L::kBarQFull), parity(units - 1));
+      for (int x = (u > L::kStages ? u - L::kStages : 0); x < u; ++x) {
+        wd.drain(bar(L::kBarFull + x % L::kStages), parity(x / L::kStages));
       }
     }
   } else if (warp == 9) {
     // ------------------------------------------------------------- MMA issuer
     if (lane == 0) {
-      const uint32_t q_smem[2] = {sbase + L::kQOff, sbase + L::kQOff + L::kTileBytes};
-      const uint32_t s_tmem[2] = {tmem + 0, tmem + 128};
-      const uint32_t o_tmem[2] = {tmem + 256, tmem + 256 + D};
+      const uint32_t q_smem0 = sbase + L::kQOff;
       auto slot_smem = [&](int u) { return sbase + L::kKVOff + (u % L::kStages) * L::kTileBytes; };
-      auto full_parity = [&](int u) { return static_cast<uint32_t>(u / L::kStages) & 1u; };
-      do {
-        if (!wd.wait(bar(L::kBarQ), 0)) break;
-        if (!wd.wait(bar(L::kBarFull + 0), 0)) break;
+      auto wait_full = [&](int u) { return wd.wait(bar(L::kBarFull + u % L::kStages), parity(u / L::kStages)); };
+      int base = 0;              // ring position of the current unit's K_0
+      int p_waits[2] = {0, 0};   // P_t handshakes consumed
+      int used[2] = {0, 0};      // earlier units in which tile t existed (its O_t is read by an epilogue)
+      bool ok = true;
+      Unit w;
+      for (int k = 0; ok && unit_at(k, p, w); ++k) {
+        if (!wd.wait(bar(L::kBarQFull), parity(k)) || !wait_full(base)) break;
         tc_fence_after_sync();
+#pragma unroll
         for (int t = 0; t < 2; ++t) {
-          if (n_kv[t] > 0) {
-            issue_qk<D, BF16>(s_tmem[t], q_smem[t], slot_smem(0));
+          if (w.n_kv[t] > 0) {
+            issue_qk<D, BF16>(tmem + 128u * t, q_smem0 + t * L::kTileBytes, slot_smem(base));
             tc_commit(bar(L::kBarS + t));
           }
         }
-        tc_commit(bar(L::kBarEmpty + 0));
-        bool ok = true;
-        for (int j = 0; j < n_max && ok; ++j) {
-          const int uv = 2 * j + 1, uk = 2 * j + 2;
-          if (!wd.wait(bar(L::kBarFull + uv % L::kStages), full_parity(uv))) break;
+        tc_commit(bar(L::kBarEmpty + base % L::kStages));
+        if (w.n_max == 1) tc_commit(bar(L::kBarQFree));
+        for (int j = 0; j < w.n_max && ok; ++j) {
+          const int uv = base + 2 * j + 1, uk = base + 2 * j + 2;
+          if (!wait_full(uv)) {
+            ok = false;
+            break;
+          }
           tc_fence_after_sync();
           bool k_ready = false;
-          for (int t = 0; t < 2 && ok; ++t) {
-            if (j >= n_kv[t]) continue;
-            if (!wd.wait(bar(L::kBarP + t), static_cast<uint32_t>(j) & 1u)) {
+#pragma unroll
+          for (int t = 0; t < 2; ++t) {
+            if (j >= w.n_kv[t] || !ok) continue;
+            // O_t is overwritten by the first P V of a unit: the previous epilogue must have read it.
+            if (j == 0 && used[t] > 0 && !wd.wait(bar(L::kBarOFree + t), parity(used[t] - 1))) {
               ok = false;
-              break;
+              continue;
             }
+            if (!wd.wait(bar(L::kBarP + t), parity(p_waits[t]))) {
+              ok = false;
+              continue;
+            }
+            ++p_waits[t];
             tc_fence_after_sync();
-            issue_pv<D, BF16>(o_tmem[t], s_tmem[t], slot_smem(uv), j > 0);
-            if (j + 1 < n_kv[t]) {
+            issue_pv<D, BF16>(tmem + 256u + static_cast<uint32_t>(D) * t, tmem + 128u * t, slot_smem(uv), j > 0);
+            if (j + 1 < w.n_kv[t]) {
               if (!k_ready) {
-                if (!wd.wait(bar(L::kBarFull + uk % L::kStages), full_parity(uk))) {
+                if (!wait_full(uk)) {
                   ok = false;
-                  break;
+                  continue;
                 }
                 tc_fence_after_sync();
                 k_ready = true;
               }
-              issue_qk<D, BF16>(s_tmem[t], q_smem[t], slot_smem(uk));
+              issue_qk<D, BF16>(tmem + 128u * t, q_smem0 + t * L::kTileBytes, slot_smem(uk));
               tc_commit(bar(L::kBarS + t));
             }
           }
           if (!ok) break;
           tc_commit(bar(L::kBarEmpty + uv % L::kStages));
           if (k_ready) tc_commit(bar(L::kBarEmpty + uk % L::kStages));
+          if (j + 2 == w.n_max) tc_commit(bar(L::kBarQFree));  // the unit's last Q K^T was just issued
+#pragma unroll
           for (int t = 0; t < 2; ++t) {
-            if (j + 1 == n_kv[t]) tc_commit(bar(L::kBarO + t));
+            if (j + 1 == w.n_kv[t]) tc_commit(bar(L::kBarO + t));
           }
         }
-      } while (false);
+        base += 2 * w.n_max;
+#pragma unroll
+        for (int t = 0; t < 2; ++t) used[t] += w.n_kv[t] > 0 ? 1 : 0;
+      }
       // Every MMA issued above must finish before TMEM is released.
       tc_commit(bar(L::kBarDrain));
       wd.drain(bar(L::kBarDrain), 0);
@@ -254,107 +307,127 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int t = warp / 4;
     const int wq = warp % 4;
     const int r_local = wq * 32 + lane;
-    const int row = (tile0 + t) * kBlockM + r_local;
     const uint32_t lane_base = static_cast<uint32_t>(wq * 32) << 16;
     const uint32_t t_s = tmem + lane_base + 128u * t;
     const uint32_t t_o = tmem + lane_base + 256u + static_cast<uint32_t>(D) * t;
     const float c = p.scale_log2e;
-    float m_ref = -INFINITY;  // reference max, base-2 domain (already multiplied by c)
-    float l = 0.f;
-    bool ok = n_kv[t] > 0;
     const bool ragged_keys = !p.causal && (p.N % kBlockN) != 0;
     // Waits stay warp-uniform: the tcgen05.ld/st below are warp-collective.
-    auto warp_wait = [&](uint32_t b, uint32_t parity) -> bool {
-      const bool got = wd.wait(b, parity);
+    auto warp_wait = [&](uint32_t b, uint32_t ph) -> bool {
+      const bool got = wd.wait(b, ph);
       return __all_sync(0xffffffffu, got) != 0;
     };
-    for (int j = 0; j < n_kv[t] && ok; ++j) {
-      if (!warp_wait(bar(L::kBarS + t), static_cast<uint32_t>(j) & 1u)) {
+    int s_waits = 0, o_waits = 0;
+    bool ok = true;
+    Unit w;
+    for (int k = 0; ok && unit_at(k, p, w); ++k) {
+      const int n_kv = w.n_kv[t];
+      if (n_kv == 0) continue;
+      const int tile = w.tile0 + t;
+      const int row = tile * kBlockM + r_local;
+      float m_ref = -INFINITY;  // reference max, base-2 domain (already multiplied by c)
+      float l = 0.f;
+      for (int j = 0; j < n_kv; ++j) {
+        if (!warp_wait(bar(L::kBarS + t), parity(s_waits))) {
+          ok = false;
+          break;
+        }
+        ++s_waits;
+        tc_fence_after_sync();
+        uint32_t s[4][32];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) tmem_ld_x32(t_s + 32u * q, s[q]);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) tmem_wait_ld_x32(s[q]);
+
+        // Mask before the max: the diagonal tile (causal) or the ragged last tile (non-causal).
+        if (p.causal && j == tile) {
+#pragma unroll
+          for (int q = 0; q < 4; ++q)
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+              if (32 * q + i > r_local) s[q][i] = __float_as_uint(-INFINITY);
+        } else if (ragged_keys && j == p.n_tiles - 1) {
+          const int valid = p.N - j * kBlockN;
+#pragma unroll
+          for (int q = 0; q < 4; ++q)
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+              if (32 * q + i >= valid) s[q][i] = __float_as_uint(-INFINITY);
+        }
+
+        float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+        for (int i = 0; i < 32; i += 2) {
+#pragma unroll
+          for (int q = 0; q < 4; ++q)
+            mx[q] = fmax3(mx[q], __uint_as_float(s[q][i]), __uint_as_float(s[q][i + 1]));
+        }
+        const float m_tile = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * c;
+        float alpha = 1.f;
+        if (m_tile > m_ref + kRescaleThreshold) {
+          alpha = ex2(m_ref - m_tile);  // 0 on the first tile (m_ref = -inf)
+          m_ref = m_tile;
+        }
+        const float neg_m = m_ref == -INFINITY ? 0.f : -m_ref;
+        const float2 c2 = make_float2(c, c);
+        const float2 nm2 = make_float2(neg_m, neg_m);
+
+        float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
+                         make_float2(0.f, 0.f)};
+        uint32_t pk[2][32];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+#pragma unroll
+          for (int i = 0; i < 32; i += 2) {
+            const float2 x = __ffma2_rn(make_float2(__uint_as_float(s[q][i]), __uint_as_float(s[q][i + 1])), c2, nm2);
+            const float2 e = make_float2(ex2(x.x), ex2(x.y));
+            acc[q] = __fadd2_rn(acc[q], e);
+            pk[q / 2][(q % 2) * 16 + i / 2] = pack2<BF16>(e.x, e.y);
+          }
+        }
+        const float2 a01 = __fadd2_rn(acc[0], acc[1]);
+        const float2 a23 = __fadd2_rn(acc[2], acc[3]);
+        const float2 a = __fadd2_rn(a01, a23);
+        l = l * alpha + (a.x + a.y);
+        tmem_st_x32(t_s, pk[0]);
+        tmem_st_x32(t_s + 32u, pk[1]);
+
+        // Rescale the running O before this tile's P V is added (P V of tile j-1 is
+        // complete: S of tile j was committed after it by the same issuer).
+        if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+          const float2 al2 = make_float2(alpha, alpha);
+#pragma unroll
+          for (int c0 = 0; c0 < D; c0 += 32) {
+            uint32_t o[32];
+            tmem_ld_x32(t_o + c0, o);
+            tmem_wait_ld_x32(o);
+#pragma unroll
+            for (int i = 0; i < 32; i += 2) {
+              const float2 v = __fmul2_rn(make_float2(__uint_as_float(o[i]), __uint_as_float(o[i + 1])), al2);
+              o[i] = __float_as_uint(v.x);
+              o[i + 1] = __float_as_uint(v.y);
+            }
+            tmem_st_x32(t_o + c0, o);
+          }
+        }
+        tmem_wait_st();
+        tc_fence_before_sync();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(L::kBarP + t));
+      }
+      if (!ok || !warp_wait(bar(L::kBarO + t), parity(o_waits))) {
         ok = false;
         break;
       }
+      ++o_waits;
       tc_fence_after_sync();
-      uint32_t s[4][32];
-#pragma unroll
-      for (int q = 0; q < 4; ++q) tmem_ld_x32(t_s + 32u * q, s[q]);
-#pragma unroll
-      for (int q = 0; q < 4; ++q) tmem_wait_ld_x32(s[q]);
 
-      // Mask before the max: the diagonal tile (causal) or the ragged last tile (non-causal).
-      if (p.causal && j == tile0 + t) {
-#pragma unroll
-        for (int q = 0; q < 4; ++q)
-#pragma unroll
-          for (int i = 0; i < 32; ++i)
-            if (32 * q + i > r_local) s[q][i] = __float_as_uint(-INFINITY);
-      } else if (ragged_keys && j == p.n_tiles - 1) {
-        const int valid = p.N - j * kBlockN;
-#pragma unroll
-        for (int q = 0; q < 4; ++q)
-#pragma unroll
-          for (int i = 0; i < 32; ++i)
-            if (32 * q + i >= valid) s[q][i] = __float_as_uint(-INFINITY);
-      }
-
-      float mx0 = -INFINITY, mx1 = -INFINITY, mx2 = -INFINITY, mx3 = -INFINITY;
-#pragma unroll
-      for (int i = 0; i < 32; i += 2) {
-        mx0 = fmax3(mx0, __uint_as_float(s[0][i]), __uint_as_float(s[0][i + 1]));
-        mx1 = fmax3(mx1, __uint_as_float(s[1][i]), __uint_as_float(s[1][i + 1]));
-        mx2 = fmax3(mx2, __uint_as_float(s[2][i]), __uint_as_float(s[2][i + 1]));
-        mx3 = fmax3(mx3, __uint_as_float(s[3][i]), __uint_as_float(s[3][i + 1]));
-      }
-      const float m_tile = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * c;
-      float alpha = 1.f;
-      if (m_tile > m_ref + kRescaleThreshold) {
-        alpha = ex2(m_ref - m_tile);  // 0 on the first tile (m_ref = -inf)
-        m_ref = m_tile;
-      }
-      const float neg_m = m_ref == -INFINITY ? 0.f : -m_ref;
-
-      float sum0 = 0.f, sum1 = 0.f, sum2 = 0.f, sum3 = 0.f;
-      uint32_t pk[2][32];
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-#pragma unroll
-        for (int i = 0; i < 32; i += 2) {
-          const float a = ex2(fmaf(__uint_as_float(s[q][i]), c, neg_m));
-          const float b = ex2(fmaf(__uint_as_float(s[q][i + 1]), c, neg_m));
-          if (q == 0) sum0 += a + b;
-          if (q == 1) sum1 += a + b;
-          if (q == 2) sum2 += a + b;
-          if (q == 3) sum3 += a + b;
-          pk[q / 2][(q % 2) * 16 + i / 2] = pack2<BF16>(a, b);
-        }
-      }
-      l = l * alpha + ((sum0 + sum1) + (sum2 + sum3));
-      tmem_st_x32(t_s, pk[0]);
-      tmem_st_x32(t_s + 32u, pk[1]);
-
-      // Rescale the running O before this tile's P V is added (PV of tile j-1 is
-      // complete: S of tile j was committed after it).
-      if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
-#pragma unroll
-        for (int c0 = 0; c0 < D; c0 += 32) {
-          uint32_t o[32];
-          tmem_ld_x32(t_o + c0, o);
-          tmem_wait_ld_x32(o);
-#pragma unroll
-          for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
-          tmem_st_x32(t_o + c0, o);
-        }
-      }
-      tmem_wait_st();
-      tc_fence_before_sync();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar(L::kBarP + t));
-    }
-
-    if (ok && warp_wait(bar(L::kBarO + t), 0)) {
-      tc_fence_after_sync();
+      // Epilogue: O = o / l rounded to the output type, lse = (m + log2 l) ln 2.
       const float inv_l = 1.f / l;
+      const float2 il2 = make_float2(inv_l, inv_l);
       uint16_t* orow = static_cast<uint16_t*>(p.o) +
-                       (static_cast<size_t>(bh) * p.N + static_cast<size_t>(row)) * D;
+                       (static_cast<size_t>(w.bh) * p.N + static_cast<size_t>(row)) * D;
 #pragma unroll
       for (int c0 = 0; c0 < D; c0 += 32) {
         uint32_t o[32];
@@ -362,8 +435,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_wait_ld_x32(o);
         uint32_t h[16];
 #pragma unroll
-        for (int i = 0; i < 16; ++i)
-          h[i] = pack2<BF16>(__uint_as_float(o[2 * i]) * inv_l, __uint_as_float(o[2 * i + 1]) * inv_l);
+        for (int i = 0; i < 16; ++i) {
+          const float2 v = __fmul2_rn(make_float2(__uint_as_float(o[2 * i]), __uint_as_float(o[2 * i + 1])), il2);
+          h[i] = pack2<BF16>(v.x, v.y);
+        }
         if (row < p.N) {
           uint4* dst = reinterpret_cast<uint4*>(orow + c0);
 #pragma unroll
@@ -371,8 +446,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             dst[v4] = make_uint4(h[4 * v4], h[4 * v4 + 1], h[4 * v4 + 2], h[4 * v4 + 3]);
         }
       }
+      // O_t has been read: the next unit's first P V may overwrite it.
+      tc_fence_before_sync();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(L::kBarOFree + t));
       if (p.lse != nullptr && row < p.N) {
-        p.lse[static_cast<size_t>(bh) * p.N + row] = (m_ref + log2f(l)) * 0.69314718055994530942f;
+        p.lse[static_cast<size_t>(w.bh) * p.N + row] = (m_ref + log2f(l)) * 0.69314718055994530942f;
       }
     }
   }
