@@ -16,10 +16,16 @@
 //     grows with the tile index) and dealt to the CTAs in zig-zag waves.  The
 //     next unit's Q load starts as soon as the current unit's last Q K^T MMA is
 //     done, and its first P V only waits until that tile's epilogue has read O,
-//     so unit boundaries overlap.  320 threads:
+//     so unit boundaries overlap.  352 threads:
 //       warps 0-3  softmax for query tile 0     warps 4-7  softmax for query tile 1
-//       warp 8     TMA producer (Q once, then K_j, V_j into a ring of smem slots)
-//       warp 9     TMEM owner and single-thread tcgen05.mma issuer
+//       warp 8     TMA producer (Q once per unit, then ring items {V_j, K_j+1})
+//       warp 9     TMEM owner; tcgen05.mma issuer for query tile 0
+//       warp 10    tcgen05.mma issuer for query tile 1
+//     One issuing thread per query tile: an MMA costs its issuing thread about
+//     as long to issue as a 128x128x16 MMA takes to run, so a single issuer
+//     that also waits and commits leaves the tensor pipe idle; two issuers
+//     overlap each other's waits.  Each tile's P V -> Q K^T order stays within
+//     one thread, where tcgen05.mma executes in issue order.
 //   * TMEM (512 columns x 128 lanes): S_t at column 128 t (128 fp32 columns),
 //     O_t at column 256 + D t.  P_t (16-bit, two per column) is written over the
 //     first 64 columns of S_t and read by the P V MMA straight from TMEM.
@@ -42,7 +48,7 @@ namespace eca {
 constexpr int kBlockM = 128;            // query rows per tile (one per TMEM lane)
 constexpr int kBlockN = 128;            // keys per K/V tile
 constexpr int kSubTileBytes = 128 * 128;  // 128 rows x 64 16-bit elements (one 128-B swizzle span)
-constexpr int kThreads = 320;
+constexpr int kThreads = 352;
 constexpr int kTmemCols = 512;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 
@@ -61,25 +67,30 @@ struct FwdParams {
   int timeout_code;
 };
 
+// Shared memory: Q of the unit's two query tiles, then a ring of stages.  A ring
+// item is {V_j-1, K_j}: the V tile of step j-1 and the K tile of step j, which
+// one step of each issuer consumes together (the first item of a unit holds K_0
+// alone, the last V_last alone).
 template <int D>
 struct FwdSmem {
   static constexpr int kSub = D / 64;                      // 64-element column blocks per row
   static constexpr int kTileBytes = kSub * kSubTileBytes;  // one 128 x D tile
-  static constexpr int kStages = D == 128 ? 4 : 8;         // K/V ring slots
+  static constexpr int kStageBytes = 2 * kTileBytes;       // V part, then K part
+  static constexpr int kStages = D == 128 ? 2 : 4;
   static constexpr int kQOff = 0;
-  static constexpr int kKVOff = 2 * kTileBytes;
-  static constexpr int kBarOff = kKVOff + kStages * kTileBytes;
+  static constexpr int kRingOff = 2 * kTileBytes;
+  static constexpr int kBarOff = kRingOff + kStages * kStageBytes;
   // barrier indices
   static constexpr int kBarQFull = 0;
-  static constexpr int kBarQFree = 1;
+  static constexpr int kBarQFree = 1;                // two arrivals: both issuers
   static constexpr int kBarFull = 2;
-  static constexpr int kBarEmpty = kBarFull + kStages;
+  static constexpr int kBarEmpty = kBarFull + kStages;  // two arrivals: both issuers
   static constexpr int kBarS = kBarEmpty + kStages;  // + t: S_t computed
   static constexpr int kBarP = kBarS + 2;            // + t: P_t written (and O_t rescaled)
   static constexpr int kBarO = kBarP + 2;            // + t: last P V of the unit done
   static constexpr int kBarOFree = kBarO + 2;        // + t: epilogue has read O_t
-  static constexpr int kBarDrain = kBarOFree + 2;
-  static constexpr int kNumBars = kBarDrain + 1;
+  static constexpr int kBarDrain = kBarOFree + 2;    // + t: issuer t's MMAs all done
+  static constexpr int kNumBars = kBarDrain + 2;
   static constexpr int kMiscOff = kBarOff + kNumBars * 8;  // TMEM base, abort flag
   static constexpr int kBytes = kMiscOff + 16;
   static constexpr int kDynamicBytes = kBytes + 1024;  // slack for 1024-B alignment
@@ -89,7 +100,7 @@ struct FwdSmem {
 struct Unit {
   int bh;
   int tile0;
-  int n_kv[2];  // key tiles each query tile needs (0 = tile absent)
+  int n_kv0, n_kv1;  // key tiles each query tile needs (0 = tile absent)
   int n_max;
 };
 
@@ -105,32 +116,34 @@ __device__ __forceinline__ bool unit_at(int k, const FwdParams& p, Unit& u) {
   const int pair = p.n_pairs - 1 - l / p.BH;
   u.tile0 = 2 * pair;
   const bool has1 = u.tile0 + 1 < p.n_tiles;
-  u.n_kv[0] = p.causal ? u.tile0 + 1 : p.n_tiles;
-  u.n_kv[1] = has1 ? (p.causal ? u.tile0 + 2 : p.n_tiles) : 0;
-  u.n_max = u.n_kv[0] > u.n_kv[1] ? u.n_kv[0] : u.n_kv[1];
+  u.n_kv0 = p.causal ? u.tile0 + 1 : p.n_tiles;
+  u.n_kv1 = has1 ? (p.causal ? u.tile0 + 2 : p.n_tiles) : 0;
+  u.n_max = u.n_kv0 > u.n_kv1 ? u.n_kv0 : u.n_kv1;
   return true;
 }
 
+// S = Q K^T: A = Q (K-major, 128-B swizzle), B = K (K-major).  Descriptors are
+// built once; stepping K by 16 elements adds 32 B (2 in the >>4 address field)
+// inside a 128-B span and 16 KB (1024) across the 64-column blocks.
 template <int D, bool BF16>
-__device__ __forceinline__ void issue_qk(uint32_t s_tmem, uint32_t q_smem, uint32_t k_smem) {
+__device__ __forceinline__ void issue_qk(uint32_t s_tmem, uint64_t q_desc, uint64_t k_desc) {
   constexpr uint32_t idesc = idesc_f16_f32acc(kBlockM, kBlockN, BF16, false);
 #pragma unroll
   for (int kk = 0; kk < D / 16; ++kk) {
-    const uint32_t off = (kk / 4) * kSubTileBytes + (kk % 4) * 32;
-    mma_ss(s_tmem, smem_desc_sw128(q_smem + off, 16, 1024), smem_desc_sw128(k_smem + off, 16, 1024),
-           idesc, kk > 0 ? 1u : 0u);
+    const uint64_t off = static_cast<uint64_t>((kk / 4) * (kSubTileBytes >> 4) + (kk % 4) * 2);
+    mma_ss(s_tmem, q_desc + off, k_desc + off, idesc, kk > 0 ? 1u : 0u);
   }
 }
 
+// O (+)= P V: A = P from TMEM (16 keys = 8 columns per step), B = V (MN-major,
+// 16 keys = 16 rows of 128 B = 2048 B per step, 64-column blocks 16 KB apart).
 template <int D, bool BF16>
-__device__ __forceinline__ void issue_pv(uint32_t o_tmem, uint32_t p_tmem, uint32_t v_smem,
-                                         bool accumulate) {
+__device__ __forceinline__ void issue_pv(uint32_t o_tmem, uint32_t p_tmem, uint64_t v_desc, bool accumulate) {
   constexpr uint32_t idesc = idesc_f16_f32acc(kBlockM, D, BF16, true);
 #pragma unroll
   for (int kk = 0; kk < kBlockN / 16; ++kk) {
-    // P: 16 keys = 8 TMEM columns.  V: 16 keys = 16 rows of 128 B.
-    mma_ts(o_tmem, p_tmem + kk * 8, smem_desc_sw128(v_smem + kk * 16 * 128, kSubTileBytes, 1024),
-           idesc, (accumulate || kk > 0) ? 1u : 0u);
+    mma_ts(o_tmem, p_tmem + kk * 8, v_desc + static_cast<uint64_t>(kk * (2048 >> 4)), idesc,
+           (accumulate || kk > 0) ? 1u : 0u);
   }
 }
 
@@ -154,18 +167,18 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (threadIdx.x == 0) {
     mbar_init(bar(L::kBarQFull), 1);
-    mbar_init(bar(L::kBarQFree), 1);
+    mbar_init(bar(L::kBarQFree), 2);
     for (int s = 0; s < L::kStages; ++s) {
       mbar_init(bar(L::kBarFull + s), 1);
-      mbar_init(bar(L::kBarEmpty + s), 1);
+      mbar_init(bar(L::kBarEmpty + s), 2);
     }
     for (int t = 0; t < 2; ++t) {
       mbar_init(bar(L::kBarS + t), 1);
       mbar_init(bar(L::kBarP + t), 4);
       mbar_init(bar(L::kBarO + t), 1);
       mbar_init(bar(L::kBarOFree + t), 4);
+      mbar_init(bar(L::kBarDrain + t), 1);
     }
-    mbar_init(bar(L::kBarDrain), 1);
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -187,14 +200,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       tma_prefetch_map(&tm_v);
       const uint64_t pol_q = policy_evict_first();
       const uint64_t pol_kv = policy_evict_last();
-      int u = 0;       // ring uses issued: K_j of a unit is use base + 2j, V_j is base + 2j + 1
+      int it = 0;      // ring items issued
       int units = 0;   // Q loads issued
       bool ok = true;
       Unit w;
       for (int k = 0; ok && unit_at(k, p, w); ++k) {
-        // The Q buffer is reused: wait until every Q K^T of the previous unit is done.
+        // The Q buffer is reused: wait until both issuers' last Q K^T of the previous unit is done.
         if (k > 0 && !wd.wait(bar(L::kBarQFree), parity(k - 1))) break;
-        const int nq = w.n_kv[1] > 0 ? 2 : 1;
+        const int nq = w.n_kv1 > 0 ? 2 : 1;
         mbar_arrive_expect_tx(bar(L::kBarQFull), nq * L::kTileBytes);
         for (int t = 0; t < nq; ++t) {
           for (int s = 0; s < L::kSub; ++s) {
@@ -203,104 +216,101 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
         ++units;
-        for (int j = 0; j < w.n_max && ok; ++j) {
-          for (int which = 0; which < 2; ++which) {
-            const int slot = u % L::kStages;
-            if (!wd.wait(bar(L::kBarEmpty + slot), parity(u / L::kStages) ^ 1u)) {
-              ok = false;
-              break;
-            }
-            mbar_arrive_expect_tx(bar(L::kBarFull + slot), L::kTileBytes);
-            const CUtensorMap* map = which ? &tm_v : &tm_k;
-            for (int s = 0; s < L::kSub; ++s) {
-              tma_load_3d(sbase + L::kKVOff + slot * L::kTileBytes + s * kSubTileBytes, map,
-                          bar(L::kBarFull + slot), 64 * s, j * kBlockN, w.bh, pol_kv);
-            }
-            ++u;
+        // Items i = 0 .. n_max: {V_(i-1) if i > 0, K_i if i < n_max}.
+        for (int i = 0; i <= w.n_max; ++i) {
+          const int slot = it % L::kStages;
+          if (!wd.wait(bar(L::kBarEmpty + slot), parity(it / L::kStages) ^ 1u)) {
+            ok = false;
+            break;
           }
+          const uint32_t stage = sbase + L::kRingOff + slot * L::kStageBytes;
+          const uint32_t full = bar(L::kBarFull + slot);
+          mbar_arrive_expect_tx(full, ((i > 0) + (i < w.n_max)) * L::kTileBytes);
+          if (i > 0) {
+            for (int s = 0; s < L::kSub; ++s)
+              tma_load_3d(stage + s * kSubTileBytes, &tm_v, full, 64 * s, (i - 1) * kBlockN, w.bh, pol_kv);
+          }
+          if (i < w.n_max) {
+            for (int s = 0; s < L::kSub; ++s)
+              tma_load_3d(stage + L::kTileBytes + s * kSubTileBytes, &tm_k, full, 64 * s, i * kBlockN, w.bh,
+                          pol_kv);
+          }
+          ++it;
         }
       }
       // Let every copy this thread started land before the block can exit.
       if (units > 0) wd.drain(bar(L::kBarQFull), parity(units - 1));
-      for (int x = (u > L::kStages ? u - L::kStages : 0); x < u; ++x) {
+      for (int x = (it > L::kStages ? it - L::kStages : 0); x < it; ++x) {
         wd.drain(bar(L::kBarFull + x % L::kStages), parity(x / L::kStages));
       }
     }
-  } else if (warp == 9) {
-    // ------------------------------------------------------------- MMA issuer
+  } else if (warp >= 9) {
+    // ------------------------------------------------- MMA issuer of query tile t
     if (lane == 0) {
-      const uint32_t q_smem0 = sbase + L::kQOff;
-      auto slot_smem = [&](int u) { return sbase + L::kKVOff + (u % L::kStages) * L::kTileBytes; };
-      auto wait_full = [&](int u) { return wd.wait(bar(L::kBarFull + u % L::kStages), parity(u / L::kStages)); };
-      int base = 0;              // ring position of the current unit's K_0
-      int p_waits[2] = {0, 0};   // P_t handshakes consumed
-      int used[2] = {0, 0};      // earlier units in which tile t existed (its O_t is read by an epilogue)
+      const int t = warp - 9;
+      const uint32_t s_tmem = tmem + 128u * t;                           // S_t, and P_t over it
+      const uint32_t o_tmem = tmem + 256u + static_cast<uint32_t>(D) * t;  // O_t
+      const uint64_t q_desc = smem_desc_sw128(sbase + L::kQOff + t * L::kTileBytes, 16, 1024);
+      const uint64_t ring_v_desc = smem_desc_sw128(sbase + L::kRingOff, kSubTileBytes, 1024);
+      const uint64_t ring_k_desc = smem_desc_sw128(sbase + L::kRingOff + L::kTileBytes, 16, 1024);
+      auto stage_off = [&](int item) {  // stage offset in the descriptors' >>4 address field
+        return static_cast<uint64_t>((item % L::kStages) * (L::kStageBytes >> 4));
+      };
+      int it = 0;       // ring items consumed
+      int p_waits = 0;  // P_t handshakes consumed
+      int used = 0;     // earlier units in which tile t existed (its O_t is read by an epilogue)
       bool ok = true;
       Unit w;
       for (int k = 0; ok && unit_at(k, p, w); ++k) {
-        if (!wd.wait(bar(L::kBarQFull), parity(k)) || !wait_full(base)) break;
-        tc_fence_after_sync();
-#pragma unroll
-        for (int t = 0; t < 2; ++t) {
-          if (w.n_kv[t] > 0) {
-            issue_qk<D, BF16>(tmem + 128u * t, q_smem0 + t * L::kTileBytes, slot_smem(base));
-            tc_commit(bar(L::kBarS + t));
-          }
+        const int n_kv = t ? w.n_kv1 : w.n_kv0;
+        // Item 0 (K_0).  Every item is waited for and released by both issuers,
+        // whether or not this tile uses it, so the ring's two-arrival phases stay aligned.
+        if (!wd.wait(bar(L::kBarQFull), parity(k)) ||
+            !wd.wait(bar(L::kBarFull + it % L::kStages), parity(it / L::kStages))) {
+          ok = false;
+          break;
         }
-        tc_commit(bar(L::kBarEmpty + base % L::kStages));
-        if (w.n_max == 1) tc_commit(bar(L::kBarQFree));
-        for (int j = 0; j < w.n_max && ok; ++j) {
-          const int uv = base + 2 * j + 1, uk = base + 2 * j + 2;
-          if (!wait_full(uv)) {
+        tc_fence_after_sync();
+        if (n_kv > 0) {
+          issue_qk<D, BF16>(s_tmem, q_desc, ring_k_desc + stage_off(it));
+          tc_commit(bar(L::kBarS + t));
+        }
+        if (n_kv <= 1) tc_commit(bar(L::kBarQFree));  // this tile's Q K^T are all issued
+        tc_commit(bar(L::kBarEmpty + it % L::kStages));
+        ++it;
+        for (int j = 0; j < w.n_max; ++j, ++it) {
+          if (!wd.wait(bar(L::kBarFull + it % L::kStages), parity(it / L::kStages))) {
             ok = false;
             break;
           }
-          tc_fence_after_sync();
-          bool k_ready = false;
-#pragma unroll
-          for (int t = 0; t < 2; ++t) {
-            if (j >= w.n_kv[t] || !ok) continue;
+          if (j < n_kv) {
             // O_t is overwritten by the first P V of a unit: the previous epilogue must have read it.
-            if (j == 0 && used[t] > 0 && !wd.wait(bar(L::kBarOFree + t), parity(used[t] - 1))) {
+            if (j == 0 && used > 0 && !wd.wait(bar(L::kBarOFree + t), parity(used - 1))) {
               ok = false;
-              continue;
+              break;
             }
-            if (!wd.wait(bar(L::kBarP + t), parity(p_waits[t]))) {
+            if (!wd.wait(bar(L::kBarP + t), parity(p_waits))) {
               ok = false;
-              continue;
+              break;
             }
-            ++p_waits[t];
+            ++p_waits;
             tc_fence_after_sync();
-            issue_pv<D, BF16>(tmem + 256u + static_cast<uint32_t>(D) * t, tmem + 128u * t, slot_smem(uv), j > 0);
-            if (j + 1 < w.n_kv[t]) {
-              if (!k_ready) {
-                if (!wait_full(uk)) {
-                  ok = false;
-                  continue;
-                }
-                tc_fence_after_sync();
-                k_ready = true;
-              }
-              issue_qk<D, BF16>(tmem + 128u * t, q_smem0 + t * L::kTileBytes, slot_smem(uk));
+            issue_pv<D, BF16>(o_tmem, s_tmem, ring_v_desc + stage_off(it), j > 0);
+            if (j + 1 < n_kv) {
+              issue_qk<D, BF16>(s_tmem, q_desc, ring_k_desc + stage_off(it));
               tc_commit(bar(L::kBarS + t));
+              if (j + 2 == n_kv) tc_commit(bar(L::kBarQFree));
+            } else {
+              tc_commit(bar(L::kBarO + t));
             }
           }
-          if (!ok) break;
-          tc_commit(bar(L::kBarEmpty + uv % L::kStages));
-          if (k_ready) tc_commit(bar(L::kBarEmpty + uk % L::kStages));
-          if (j + 2 == w.n_max) tc_commit(bar(L::kBarQFree));  // the unit's last Q K^T was just issued
-#pragma unroll
-          for (int t = 0; t < 2; ++t) {
-            if (j + 1 == w.n_kv[t]) tc_commit(bar(L::kBarO + t));
-          }
+          tc_commit(bar(L::kBarEmpty + it % L::kStages));
         }
-        base += 2 * w.n_max;
-#pragma unroll
-        for (int t = 0; t < 2; ++t) used[t] += w.n_kv[t] > 0 ? 1 : 0;
+        used += n_kv > 0 ? 1 : 0;
       }
       // Every MMA issued above must finish before TMEM is released.
-      tc_commit(bar(L::kBarDrain));
-      wd.drain(bar(L::kBarDrain), 0);
+      tc_commit(bar(L::kBarDrain + t));
+      wd.drain(bar(L::kBarDrain + t), 0);
     }
   } else {
     // ------------------------------------------------------------------ softmax
@@ -321,7 +331,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool ok = true;
     Unit w;
     for (int k = 0; ok && unit_at(k, p, w); ++k) {
-      const int n_kv = w.n_kv[t];
+      const int n_kv = t ? w.n_kv1 : w.n_kv0;
       if (n_kv == 0) continue;
       const int tile = w.tile0 + t;
       const int row = tile * kBlockM + r_local;
