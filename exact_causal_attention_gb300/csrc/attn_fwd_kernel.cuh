@@ -24,8 +24,11 @@
 //     One issuing thread per query tile: an MMA costs its issuing thread about
 //     as long to issue as a 128x128x16 MMA takes to run, so a single issuer
 //     that also waits and commits leaves the tensor pipe idle; two issuers
-//     overlap each other's waits.  Each tile's P V -> Q K^T order stays within
-//     one thread, where tcgen05.mma executes in issue order.
+//     overlap each other's waits and commits.  Each tile's P V -> Q K^T order
+//     stays within one thread, where tcgen05.mma executes in issue order, and a
+//     shared-memory lock keeps each turn's MMAs contiguous in the pipe so the
+//     two tiles alternate (one tile's softmax overlaps the other's MMAs) instead
+//     of advancing together.
 //   * TMEM (512 columns x 128 lanes): S_t at column 128 t (128 fp32 columns),
 //     O_t at column 256 + D t.  P_t (16-bit, two per column) is written over the
 //     first 64 columns of S_t and read by the P V MMA straight from TMEM.
@@ -91,7 +94,7 @@ struct FwdSmem {
   static constexpr int kBarOFree = kBarO + 2;        // + t: epilogue has read O_t
   static constexpr int kBarDrain = kBarOFree + 2;    // + t: issuer t's MMAs all done
   static constexpr int kNumBars = kBarDrain + 2;
-  static constexpr int kMiscOff = kBarOff + kNumBars * 8;  // TMEM base, abort flag
+  static constexpr int kMiscOff = kBarOff + kNumBars * 8;  // TMEM base, abort flag, issue lock
   static constexpr int kBytes = kMiscOff + 16;
   static constexpr int kDynamicBytes = kBytes + 1024;  // slack for 1024-B alignment
 };
@@ -161,6 +164,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto bar = [&](int i) -> uint32_t { return sbase + L::kBarOff + 8u * static_cast<uint32_t>(i); };
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kMiscOff);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kMiscOff + 4);
+  int* issue_lock = reinterpret_cast<int*>(smem + L::kMiscOff + 8);
 
   const int warp = threadIdx.x / 32;
   const int lane = threadIdx.x % 32;
@@ -180,6 +184,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(bar(L::kBarDrain + t), 1);
     }
     *abort_flag = 0;
+    *issue_lock = 0;
     fence_barrier_init();
   }
   if (warp == 9) {
@@ -256,6 +261,20 @@ __global__ void __launch_bounds__(kThreads, 1)
       auto stage_off = [&](int item) {  // stage offset in the descriptors' >>4 address field
         return static_cast<uint64_t>((item % L::kStages) * (L::kStageBytes >> 4));
       };
+      // One issuer at a time puts its turn's MMAs into the pipe.
+      auto lock = [&]() -> bool {
+        if (atomicCAS_block(issue_lock, 0, 1) == 0) return true;
+        const uint64_t t0 = global_timer_ns();
+        while (atomicCAS_block(issue_lock, 0, 1) != 0) {
+          if (wd.aborted()) return false;
+          if (global_timer_ns() - t0 > wd.limit_ns) {
+            wd.fire();
+            return false;
+          }
+        }
+        return true;
+      };
+      auto unlock = [&]() { atomicExch_block(issue_lock, 0); };
       int it = 0;       // ring items consumed
       int p_waits = 0;  // P_t handshakes consumed
       int used = 0;     // earlier units in which tile t existed (its O_t is read by an epilogue)
@@ -272,7 +291,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         tc_fence_after_sync();
         if (n_kv > 0) {
+          if (!lock()) {
+            ok = false;
+            break;
+          }
           issue_qk<D, BF16>(s_tmem, q_desc, ring_k_desc + stage_off(it));
+          unlock();
           tc_commit(bar(L::kBarS + t));
         }
         if (n_kv <= 1) tc_commit(bar(L::kBarQFree));  // this tile's Q K^T are all issued
@@ -295,9 +319,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             ++p_waits;
             tc_fence_after_sync();
+            if (!lock()) {
+              ok = false;
+              break;
+            }
             issue_pv<D, BF16>(o_tmem, s_tmem, ring_v_desc + stage_off(it), j > 0);
+            if (j + 1 < n_kv) issue_qk<D, BF16>(s_tmem, q_desc, ring_k_desc + stage_off(it));
+            unlock();
             if (j + 1 < n_kv) {
-              issue_qk<D, BF16>(s_tmem, q_desc, ring_k_desc + stage_off(it));
               tc_commit(bar(L::kBarS + t));
               if (j + 2 == n_kv) tc_commit(bar(L::kBarQFree));
             } else {
