@@ -35,11 +35,13 @@
 //   * a query row is a TMEM lane, so each softmax thread owns one full score row:
 //     the row max and row sum need no shuffles.
 //   * exp is computed as 2^(s * scale * log2 e - m) with the MUFU ex2.
-//   * conditional rescaling: the reference max m is only moved (and O, l
-//     rescaled) when the new row max exceeds it by more than 2^8 in the base-2
-//     domain; otherwise probabilities are formed against the stale, smaller
-//     reference, which is exact algebra (o and l share that reference) and keeps
-//     every p below 256.
+//   * stale reference max: o and l share one reference m, and any reference
+//     gives the same O and lse (exact algebra), so p is formed against the
+//     current reference without first taking the new tile's row max.  The row
+//     sum bounds every p of the row, so a sum of at most 2^15 proves that no p
+//     overflows the 16-bit P; only the first key tile of a unit and the rare
+//     rows whose sum exceeds the bound take the row max, move the reference
+//     (rescaling O and l) and redo the tile from S, still intact in TMEM.
 #pragma once
 #include <cuda.h>
 #include <cstdint>
@@ -53,7 +55,7 @@ constexpr int kBlockN = 128;            // keys per K/V tile
 constexpr int kSubTileBytes = 128 * 128;  // 128 rows x 64 16-bit elements (one 128-B swizzle span)
 constexpr int kThreads = 352;
 constexpr int kTmemCols = 512;
-constexpr float kRescaleThreshold = 8.0f;  // log2 units
+constexpr float kMaxRowSum = 32768.0f;  // bound on sum_j p_ij that keeps every p in fp16 range
 
 struct FwdParams {
   void* o;        // [BH, N, D] 16-bit
@@ -374,61 +376,75 @@ __global__ void __launch_bounds__(kThreads, 1)
         ++s_waits;
         tc_fence_after_sync();
         uint32_t s[4][32];
+        // S of this key tile, masked: the diagonal tile (causal) or the ragged
+        // last tile (non-causal).
+        auto load_scores = [&]() {
 #pragma unroll
-        for (int q = 0; q < 4; ++q) tmem_ld_x32(t_s + 32u * q, s[q]);
+          for (int q = 0; q < 4; ++q) tmem_ld_x32(t_s + 32u * q, s[q]);
 #pragma unroll
-        for (int q = 0; q < 4; ++q) tmem_wait_ld_x32(s[q]);
-
-        // Mask before the max: the diagonal tile (causal) or the ragged last tile (non-causal).
-        if (p.causal && j == tile) {
+          for (int q = 0; q < 4; ++q) tmem_wait_ld_x32(s[q]);
+          if (p.causal && j == tile) {
 #pragma unroll
-          for (int q = 0; q < 4; ++q)
+            for (int q = 0; q < 4; ++q)
 #pragma unroll
-            for (int i = 0; i < 32; ++i)
-              if (32 * q + i > r_local) s[q][i] = __float_as_uint(-INFINITY);
-        } else if (ragged_keys && j == p.n_tiles - 1) {
-          const int valid = p.N - j * kBlockN;
+              for (int i = 0; i < 32; ++i)
+                if (32 * q + i > r_local) s[q][i] = __float_as_uint(-INFINITY);
+          } else if (ragged_keys && j == p.n_tiles - 1) {
+            const int valid = p.N - j * kBlockN;
 #pragma unroll
-          for (int q = 0; q < 4; ++q)
+            for (int q = 0; q < 4; ++q)
 #pragma unroll
-            for (int i = 0; i < 32; ++i)
-              if (32 * q + i >= valid) s[q][i] = __float_as_uint(-INFINITY);
-        }
-
-        float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-#pragma unroll
-        for (int i = 0; i < 32; i += 2) {
-#pragma unroll
-          for (int q = 0; q < 4; ++q)
-            mx[q] = fmax3(mx[q], __uint_as_float(s[q][i]), __uint_as_float(s[q][i + 1]));
-        }
-        const float m_tile = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * c;
-        float alpha = 1.f;
-        if (m_tile > m_ref + kRescaleThreshold) {
-          alpha = ex2(m_ref - m_tile);  // 0 on the first tile (m_ref = -inf)
-          m_ref = m_tile;
-        }
-        const float neg_m = m_ref == -INFINITY ? 0.f : -m_ref;
-        const float2 c2 = make_float2(c, c);
-        const float2 nm2 = make_float2(neg_m, neg_m);
-
-        float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
-                         make_float2(0.f, 0.f)};
-        uint32_t pk[2][32];
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-#pragma unroll
-          for (int i = 0; i < 32; i += 2) {
-            const float2 x = __ffma2_rn(make_float2(__uint_as_float(s[q][i]), __uint_as_float(s[q][i + 1])), c2, nm2);
-            const float2 e = make_float2(ex2(x.x), ex2(x.y));
-            acc[q] = __fadd2_rn(acc[q], e);
-            pk[q / 2][(q % 2) * 16 + i / 2] = pack2<BF16>(e.x, e.y);
+              for (int i = 0; i < 32; ++i)
+                if (32 * q + i >= valid) s[q][i] = __float_as_uint(-INFINITY);
           }
+        };
+        // p = 2^(s c - m_ref) for the row, packed for the P V MMA; returns sum p.
+        uint32_t pk[2][32];
+        auto exponentiate = [&](float neg_m) -> float {
+          const float2 c2 = make_float2(c, c);
+          const float2 nm2 = make_float2(neg_m, neg_m);
+          float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
+                           make_float2(0.f, 0.f)};
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+#pragma unroll
+            for (int i = 0; i < 32; i += 2) {
+              const float2 x = __ffma2_rn(make_float2(__uint_as_float(s[q][i]), __uint_as_float(s[q][i + 1])), c2, nm2);
+              const float2 e = make_float2(ex2(x.x), ex2(x.y));
+              acc[q] = __fadd2_rn(acc[q], e);
+              pk[q / 2][(q % 2) * 16 + i / 2] = pack2<BF16>(e.x, e.y);
+            }
+          }
+          const float2 a = __fadd2_rn(__fadd2_rn(acc[0], acc[1]), __fadd2_rn(acc[2], acc[3]));
+          return a.x + a.y;
+        };
+
+        float alpha = 1.f;
+        float row_sum = 0.f;
+        bool move = true;  // the first key tile of a unit has no reference yet
+        if (j > 0) {
+          load_scores();
+          row_sum = exponentiate(-m_ref);
+          move = !(row_sum <= kMaxRowSum);  // also true for an overflowed (inf) sum
         }
-        const float2 a01 = __fadd2_rn(acc[0], acc[1]);
-        const float2 a23 = __fadd2_rn(acc[2], acc[3]);
-        const float2 a = __fadd2_rn(a01, a23);
-        l = l * alpha + (a.x + a.y);
+        if (__any_sync(0xffffffffu, move)) {
+          load_scores();  // S is still intact in TMEM: P has not been stored yet
+          if (move) {
+            float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+            for (int i = 0; i < 32; i += 2) {
+#pragma unroll
+              for (int q = 0; q < 4; ++q)
+                mx[q] = fmax3(mx[q], __uint_as_float(s[q][i]), __uint_as_float(s[q][i + 1]));
+            }
+            const float m_tile = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * c;
+            const float m_new = fmaxf(m_ref, m_tile);
+            alpha = m_ref == -INFINITY ? 0.f : ex2(m_ref - m_new);
+            m_ref = m_new;
+          }
+          row_sum = exponentiate(m_ref == -INFINITY ? 0.f : -m_ref);
+        }
+        l = l * alpha + row_sum;
         tmem_st_x32(t_s, pk[0]);
         tmem_st_x32(t_s + 32u, pk[1]);
 
