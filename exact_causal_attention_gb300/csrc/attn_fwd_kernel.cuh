@@ -403,19 +403,21 @@ __global__ void __launch_bounds__(kThreads, 1)
         auto exponentiate = [&](float neg_m) -> float {
           const float2 c2 = make_float2(c, c);
           const float2 nm2 = make_float2(neg_m, neg_m);
-          float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
-                           make_float2(0.f, 0.f)};
+          float2 acc[8];
+#pragma unroll
+          for (int a = 0; a < 8; ++a) acc[a] = make_float2(0.f, 0.f);
 #pragma unroll
           for (int q = 0; q < 4; ++q) {
 #pragma unroll
             for (int i = 0; i < 32; i += 2) {
               const float2 x = __ffma2_rn(make_float2(__uint_as_float(s[q][i]), __uint_as_float(s[q][i + 1])), c2, nm2);
               const float2 e = make_float2(ex2(x.x), ex2(x.y));
-              acc[q] = __fadd2_rn(acc[q], e);
+              acc[(i / 2) % 8] = __fadd2_rn(acc[(i / 2) % 8], e);  // eight short add chains
               pk[q / 2][(q % 2) * 16 + i / 2] = pack2<BF16>(e.x, e.y);
             }
           }
-          const float2 a = __fadd2_rn(__fadd2_rn(acc[0], acc[1]), __fadd2_rn(acc[2], acc[3]));
+          const float2 a = __fadd2_rn(__fadd2_rn(__fadd2_rn(acc[0], acc[1]), __fadd2_rn(acc[2], acc[3])),
+                                      __fadd2_rn(__fadd2_rn(acc[4], acc[5]), __fadd2_rn(acc[6], acc[7])));
           return a.x + a.y;
         };
 
