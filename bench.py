@@ -326,6 +326,41 @@ def bench_ours(args, w):
             sweep[str(n)] = {"ms": round(med, 4), "tflops": round(sw.flops / (med * 1e-3) / 1e12, 1)}
             del sq, sk, sv, so, sl
 
+    # Key split on a workload too small in B x H to fill the GPU (causal, B=1, H=4, N=8192, D=128).
+    splitkv = {}
+    if not args.no_sweep and rank == 0:
+        sw = inputs.Workload("causal_b1_h4_n8192_d128_fp16", 1, 4, 8192, 128, "fp16", True, 5)
+        sq, sk, sv = (x.to(dev) for x in inputs.workload_qkv(sw))
+        so = torch.empty_like(sq)
+        sl = torch.empty((sw.B, sw.H, sw.N), dtype=torch.float32, device=dev)
+        splits = eca.splitkv_default_splits(sw.B, sw.H, sw.N, sw.D)
+        need = eca.splitkv_workspace_bytes(sw.B, sw.H, sw.N, sw.D, splits)
+        ws = torch.empty(need + 256, dtype=torch.uint8, device=dev)
+        off = (-ws.data_ptr()) % 256
+        ws = ws[off:off + need]
+
+        def timed(fn):
+            times = []
+            for i in range(13):
+                flush.zero_()
+                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a.record(stream)
+                fn()
+                b.record(stream)
+                times.append((a, b))
+            torch.cuda.synchronize(dev)
+            ms = sorted(a.elapsed_time(b) for a, b in times[3:])
+            return ms[len(ms) // 2]
+
+        t_plain = timed(lambda: eca.attn_fwd_into(sq, sk, sv, so, sl, causal=True, scale=sw.scale, stream=stream))
+        t_split = timed(lambda: eca.attn_fwd_splitkv(sq, sk, sv, so, sl, kv_splits=splits, workspace=ws,
+                                                     causal=True, scale=sw.scale, stream=stream))
+        splitkv = {"workload": sw.name, "kv_splits": splits, "workspace_bytes": need,
+                   "unsplit_ms": round(t_plain, 4), "unsplit_tflops": round(sw.flops / (t_plain * 1e-3) / 1e12, 1),
+                   "split_ms": round(t_split, 4), "split_tflops": round(sw.flops / (t_split * 1e-3) / 1e12, 1),
+                   "launches_per_call": 2}
+        del sq, sk, sv, so, sl, ws
+
     fp16_peak = None
     if not args.no_peak and rank == 0:
         a = torch.randn(8192, 8192, device=dev, dtype=torch.float16)
@@ -376,6 +411,7 @@ def bench_ours(args, w):
         "gpu_launches": args.steps,
         "clocks": clocks,
         "sweep": sweep,
+        "splitkv": splitkv,
         "fp16_matmul_peak_tflops": fp16_peak,
         "frac_of_measured_fp16_matmul": (achieved / fp16_peak) if fp16_peak else None,
         "frac_of_datasheet_dense_fp16": achieved / 2250.0,

@@ -12,8 +12,9 @@ import math
 import os
 import threading
 
-__all__ = ["attn_fwd", "attn_fwd_into", "load_library", "device_status", "watchdog_selftest",
-           "AttnError", "STATUS"]
+__all__ = ["attn_fwd", "attn_fwd_into", "attn_fwd_splitkv", "splitkv_workspace_bytes",
+           "splitkv_default_splits", "load_library", "device_status", "watchdog_selftest", "AttnError",
+           "STATUS"]
 
 _LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "_build", "libeca_attn.so")
 _lock = threading.Lock()
@@ -31,10 +32,14 @@ STATUS = {
 }
 
 # Every exported symbol of include/attn.h with its ctypes signature.
-_VP, _I, _F, _U = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_uint
+_VP, _I, _F, _U, _SZ = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_uint, ctypes.c_size_t
 SIGNATURES = {
     "attn_fwd": (_I, [_VP, _VP, _VP, _VP, _VP, _I, _I, _I, _I, _I, _F, _VP]),
     "attn_fwd_bf16": (_I, [_VP, _VP, _VP, _VP, _VP, _I, _I, _I, _I, _I, _F, _VP]),
+    "attn_fwd_splitkv": (_I, [_VP, _VP, _VP, _VP, _VP, _I, _I, _I, _I, _I, _F, _I, _VP, _SZ, _VP]),
+    "attn_fwd_splitkv_bf16": (_I, [_VP, _VP, _VP, _VP, _VP, _I, _I, _I, _I, _I, _F, _I, _VP, _SZ, _VP]),
+    "attn_splitkv_workspace_bytes": (_SZ, [_I, _I, _I, _I, _I]),
+    "attn_splitkv_default_splits": (_I, [_I, _I, _I, _I]),
     "attn_device_status": (_I, [_VP]),
     "attn_watchdog_selftest": (_I, [_U, _VP]),
     "attn_status_string": (ctypes.c_char_p, [_I]),
@@ -137,6 +142,53 @@ def attn_fwd(q, k, v, causal: bool = True, scale: float | None = None, return_ls
     lse = torch.empty(q.shape[:3], dtype=torch.float32, device=q.device) if return_lse else None
     attn_fwd_into(q, k, v, o, lse, causal=causal, scale=scale, stream=stream)
     return (o, lse) if return_lse else o
+
+
+def splitkv_workspace_bytes(B: int, H: int, N: int, D: int, kv_splits: int) -> int:
+    """Workspace bytes attn_fwd_splitkv needs (0 for invalid sizes)."""
+    return int(load_library().attn_splitkv_workspace_bytes(B, H, N, D, kv_splits))
+
+
+def splitkv_default_splits(B: int, H: int, N: int, D: int) -> int:
+    rc = load_library().attn_splitkv_default_splits(B, H, N, D)
+    if rc < 0:
+        raise AttnError(rc, "attn_splitkv_default_splits")
+    return rc
+
+
+def attn_fwd_splitkv(q, k, v, o=None, lse=None, kv_splits: int | None = None, workspace=None,
+                     causal: bool = True, scale: float | None = None, stream=None):
+    """attn_fwd with the key tiles split into kv_splits segments merged by a second
+    kernel.  The fp32 workspace comes from the caller (a uint8 CUDA tensor) or is
+    allocated here with torch.  Returns (o, lse)."""
+    import torch
+
+    _check_qkv(q, k, v)
+    B, H, N, D = q.shape
+    if kv_splits is None:
+        with torch.cuda.device(q.device):
+            kv_splits = splitkv_default_splits(B, H, N, D)
+    if o is None:
+        o = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
+    need = splitkv_workspace_bytes(B, H, N, D, kv_splits)
+    if workspace is None:
+        workspace = torch.empty(max(need, 1) + 256, dtype=torch.uint8, device=q.device)
+        off = (-workspace.data_ptr()) % 256
+        workspace = workspace[off:off + max(need, 1)]
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    lib = load_library()
+    fn = lib.attn_fwd_splitkv_bf16 if q.dtype == torch.bfloat16 else lib.attn_fwd_splitkv
+    with torch.cuda.device(q.device):
+        rc = fn(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                lse.data_ptr() if lse is not None else None, B, H, N, D, int(bool(causal)), float(scale),
+                int(kv_splits), workspace.data_ptr(), workspace.numel() * workspace.element_size(),
+                _stream_handle(stream))
+    if rc != 0:
+        raise AttnError(rc, "attn_fwd_splitkv")
+    return o, lse
 
 
 def device_status(stream=None) -> int:

@@ -10,10 +10,12 @@
 
 #include "attn.h"
 #include "attn_fwd_kernel.cuh"
+#include "splitkv_combine.cuh"
 
 namespace {
 
 constexpr int kMaxDevices = 64;
+constexpr int kMaxSplits = 64;
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;  // 2 s per single wait
 
 // Device status word: 0, or the code of the last bounded wait that gave up.
@@ -124,9 +126,34 @@ int check_args(const void* q, const void* k, const void* v, const void* o, const
   return ATTN_OK;
 }
 
+// Split of the key tiles into segments: tiles per segment and the number of
+// non-empty segments for a requested split count.
+struct KeySplit {
+  int seg_tiles;
+  int splits;
+};
+
+KeySplit key_split(int N, int requested) {
+  const int n_tiles = (N + eca::kBlockN - 1) / eca::kBlockN;
+  const int r = requested < 1 ? 1 : (requested > n_tiles ? n_tiles : requested);
+  const int seg = (n_tiles + r - 1) / r;
+  return KeySplit{seg, (n_tiles + seg - 1) / seg};
+}
+
+uint64_t align256(uint64_t x) { return (x + 255) & ~static_cast<uint64_t>(255); }
+
+// Workspace of a key split: fp32 partial outputs [splits, BH, N, D], then fp32
+// partial log-sum-exp [splits, BH, N] at the next 256-byte boundary.
+uint64_t splitkv_bytes(uint64_t bh, uint64_t N, uint64_t D, uint64_t splits, uint64_t* lse_offset) {
+  const uint64_t o_bytes = splits * bh * N * D * 4;
+  if (lse_offset) *lse_offset = align256(o_bytes);
+  return align256(o_bytes) + align256(splits * bh * N * 4);
+}
+
 template <int D, bool BF16>
 int launch(const void* q, const void* k, const void* v, void* o, float* lse, int BH, int N, int causal,
-           float scale, cudaStream_t stream, DeviceState* st, EncodeTiledFn encode) {
+           float scale, cudaStream_t stream, DeviceState* st, EncodeTiledFn encode, const KeySplit& ks,
+           float* part_o, float* part_lse) {
   using L = eca::FwdSmem<D>;
   auto kernel = eca::attn_fwd_kernel<D, BF16>;
   const unsigned bit = 1u << ((D == 128 ? 2 : 0) + (BF16 ? 1 : 0));
@@ -146,12 +173,16 @@ int launch(const void* q, const void* k, const void* v, void* o, float* lse, int
   eca::FwdParams p;
   p.o = o;
   p.lse = lse;
+  p.part_o = part_o;
+  p.part_lse = part_lse;
   p.status = st->status;
   p.N = N;
   p.n_tiles = (N + eca::kBlockM - 1) / eca::kBlockM;
   p.n_pairs = (p.n_tiles + 1) / 2;
   p.BH = BH;
-  p.n_units = p.n_pairs * BH;
+  p.splits = ks.splits;
+  p.seg_tiles = ks.seg_tiles;
+  p.n_units = p.n_pairs * BH * ks.splits;
   p.causal = causal ? 1 : 0;
   p.scale_log2e = scale * 1.4426950408889634f;
   p.wait_limit_ns = kWaitLimitNs;
@@ -159,13 +190,53 @@ int launch(const void* q, const void* k, const void* v, void* o, float* lse, int
   // Persistent: one CTA per SM (the shared-memory footprint admits only one), never more than the units.
   const unsigned grid = static_cast<unsigned>(p.n_units < st->sm_count ? p.n_units : st->sm_count);
   kernel<<<grid, eca::kThreads, L::kDynamicBytes, stream>>>(tq, tk, tv, p);
+  if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_LAUNCH;
+  if (part_o == nullptr) return ATTN_OK;
+
+  eca::CombineParams c;
+  c.part_o = part_o;
+  c.part_lse = part_lse;
+  c.o = o;
+  c.lse = lse;
+  c.BH = BH;
+  c.N = N;
+  c.n_tiles = p.n_tiles;
+  c.seg_tiles = ks.seg_tiles;
+  c.splits = ks.splits;
+  c.causal = p.causal;
+  const long long rows = static_cast<long long>(BH) * N;
+  const long long want = (rows + 7) / 8;  // 8 rows (warps) per 256-thread block
+  const long long cap = static_cast<long long>(st->sm_count) * 8;
+  eca::splitkv_combine_kernel<D, BF16><<<static_cast<unsigned>(want < cap ? want : cap), 256, 0, stream>>>(c);
   return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_LAUNCH;
 }
 
 int attn_fwd_impl(bool bf16, const void* q, const void* k, const void* v, void* o, float* lse, int B,
-                  int H, int N, int D, int causal, float scale, attn_stream_t stream) {
-  const int rc = check_args(q, k, v, o, lse, B, H, N, D, scale);
+                  int H, int N, int D, int causal, float scale, attn_stream_t stream, int kv_splits = 0,
+                  void* workspace = nullptr, size_t workspace_bytes = 0) {
+  int rc = check_args(q, k, v, o, lse, B, H, N, D, scale);
   if (rc != ATTN_OK) return rc;
+  KeySplit ks{(N + eca::kBlockN - 1) / eca::kBlockN, 1};
+  float* part_o = nullptr;
+  float* part_lse = nullptr;
+  if (kv_splits > 0) {
+    if (kv_splits > kMaxSplits || workspace == nullptr) return ATTN_ERR_INVALID_ARG;
+    if (!aligned(workspace, 256)) return ATTN_ERR_UNALIGNED;
+    ks = key_split(N, kv_splits);
+    const uint64_t bh = static_cast<uint64_t>(B) * static_cast<uint64_t>(H);
+    uint64_t lse_off = 0;
+    const uint64_t need = splitkv_bytes(bh, N, D, ks.splits, &lse_off);
+    if (static_cast<uint64_t>(workspace_bytes) < need) return ATTN_ERR_INVALID_ARG;
+    const uint64_t io_bytes = bh * static_cast<uint64_t>(N) * static_cast<uint64_t>(D) * 2;
+    if (overlaps(workspace, q, io_bytes) || overlaps(workspace, k, io_bytes) || overlaps(workspace, v, io_bytes) ||
+        overlaps(workspace, o, io_bytes) || overlaps(o, workspace, need)) {
+      return ATTN_ERR_INVALID_ARG;
+    }
+    const uint64_t n_pairs = ((static_cast<uint64_t>(N) + 127) / 128 + 1) / 2;
+    if (n_pairs * bh * static_cast<uint64_t>(ks.splits) > 0x7fffffffull) return ATTN_ERR_INVALID_ARG;
+    part_o = static_cast<float*>(workspace);
+    part_lse = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + lse_off);
+  }
   std::lock_guard<std::mutex> lock(g_mutex);
   DeviceState* st = nullptr;
   int r = device_state(&st);
@@ -176,11 +247,11 @@ int attn_fwd_impl(bool bf16, const void* q, const void* k, const void* v, void* 
   const int BH = B * H;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   if (D == 128) {
-    return bf16 ? launch<128, true>(q, k, v, o, lse, BH, N, causal, scale, s, st, encode)
-                : launch<128, false>(q, k, v, o, lse, BH, N, causal, scale, s, st, encode);
+    return bf16 ? launch<128, true>(q, k, v, o, lse, BH, N, causal, scale, s, st, encode, ks, part_o, part_lse)
+                : launch<128, false>(q, k, v, o, lse, BH, N, causal, scale, s, st, encode, ks, part_o, part_lse);
   }
-  return bf16 ? launch<64, true>(q, k, v, o, lse, BH, N, causal, scale, s, st, encode)
-              : launch<64, false>(q, k, v, o, lse, BH, N, causal, scale, s, st, encode);
+  return bf16 ? launch<64, true>(q, k, v, o, lse, BH, N, causal, scale, s, st, encode, ks, part_o, part_lse)
+              : launch<64, false>(q, k, v, o, lse, BH, N, causal, scale, s, st, encode, ks, part_o, part_lse);
 }
 
 // One thread waits on a barrier that nothing ever arrives on, with a bounded wait.
@@ -211,6 +282,44 @@ int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, i
 int attn_fwd_bf16(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N,
                   int D, int causal, float scale, attn_stream_t stream) {
   return attn_fwd_impl(true, q, k, v, o, lse, B, H, N, D, causal, scale, stream);
+}
+
+int attn_fwd_splitkv(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N,
+                     int D, int causal, float scale, int kv_splits, void* workspace, size_t workspace_bytes,
+                     attn_stream_t stream) {
+  if (kv_splits < 1) return ATTN_ERR_INVALID_ARG;
+  return attn_fwd_impl(false, q, k, v, o, lse, B, H, N, D, causal, scale, stream, kv_splits, workspace,
+                       workspace_bytes);
+}
+
+int attn_fwd_splitkv_bf16(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N,
+                          int D, int causal, float scale, int kv_splits, void* workspace, size_t workspace_bytes,
+                          attn_stream_t stream) {
+  if (kv_splits < 1) return ATTN_ERR_INVALID_ARG;
+  return attn_fwd_impl(true, q, k, v, o, lse, B, H, N, D, causal, scale, stream, kv_splits, workspace,
+                       workspace_bytes);
+}
+
+size_t attn_splitkv_workspace_bytes(int B, int H, int N, int D, int kv_splits) {
+  if (B < 1 || H < 1 || N < 1 || (D != 64 && D != 128) || kv_splits < 1 || kv_splits > kMaxSplits) return 0;
+  const KeySplit ks = key_split(N, kv_splits);
+  return static_cast<size_t>(
+      splitkv_bytes(static_cast<uint64_t>(B) * static_cast<uint64_t>(H), N, D, ks.splits, nullptr));
+}
+
+int attn_splitkv_default_splits(int B, int H, int N, int D) {
+  if (B < 1 || H < 1 || N < 1 || (D != 64 && D != 128)) return ATTN_ERR_INVALID_ARG;
+  std::lock_guard<std::mutex> lock(g_mutex);
+  DeviceState* st = nullptr;
+  const int r = device_state(&st);
+  if (r != ATTN_OK) return r;
+  const long long n_tiles = (static_cast<long long>(N) + 127) / 128;
+  const long long units = (n_tiles + 1) / 2 * static_cast<long long>(B) * H;
+  // Enough segments for about two units per SM; never more than the key tiles.
+  long long s = (2LL * st->sm_count + units - 1) / units;
+  if (s > n_tiles) s = n_tiles;
+  if (s > kMaxSplits) s = kMaxSplits;
+  return s < 1 ? 1 : static_cast<int>(s);
 }
 
 int attn_device_status(attn_stream_t stream) {

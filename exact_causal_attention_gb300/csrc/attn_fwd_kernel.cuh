@@ -16,7 +16,11 @@
 //     grows with the tile index) and dealt to the CTAs in zig-zag waves.  The
 //     next unit's Q load starts as soon as the current unit's last Q K^T MMA is
 //     done, and its first P V only waits until that tile's epilogue has read O,
-//     so unit boundaries overlap.  352 threads:
+//     so unit boundaries overlap.  With a key split (long sequences, few
+//     heads), a unit also names a segment of key tiles and its epilogue writes
+//     the segment's normalised partial output and log-sum-exp in fp32 for a
+//     separate merge ("CUDA KV Cache：分页存储与长上下文 Decode 极致优化",
+//     section 6.4).  352 threads:
 //       warps 0-3  softmax for query tile 0     warps 4-7  softmax for query tile 1
 //       warp 8     TMA producer (Q once per unit, then ring items {V_j, K_j+1})
 //       warp 9     TMEM owner; tcgen05.mma issuer for query tile 0
@@ -58,14 +62,18 @@ constexpr int kTmemCols = 512;
 constexpr float kMaxRowSum = 32768.0f;  // bound on sum_j p_ij that keeps every p in fp16 range
 
 struct FwdParams {
-  void* o;        // [BH, N, D] 16-bit
-  float* lse;     // [BH, N] or null
+  void* o;        // [BH, N, D] 16-bit (unused when part_o is set)
+  float* lse;     // [BH, N] or null (unused when part_o is set)
+  float* part_o;  // key split: [splits, BH, N, D] fp32 partial outputs, else null
+  float* part_lse;  // key split: [splits, BH, N] fp32 partial log-sum-exp
   int* status;    // device status word
   int N;
   int n_tiles;    // ceil(N / 128), for queries and keys alike
   int n_pairs;    // ceil(n_tiles / 2)
   int BH;
-  int n_units;    // n_pairs * BH
+  int splits;     // key segments (1 = no split)
+  int seg_tiles;  // key tiles per segment
+  int n_units;    // n_pairs * BH * splits
   int causal;
   float scale_log2e;  // scale * log2(e)
   unsigned long long wait_limit_ns;
@@ -101,11 +109,14 @@ struct FwdSmem {
   static constexpr int kDynamicBytes = kBytes + 1024;  // slack for 1024-B alignment
 };
 
-// One work unit: query tiles 2*pair and 2*pair + 1 of slice bh.
+// One work unit: query tiles 2*pair and 2*pair + 1 of slice bh, against the
+// key tiles kv0 .. kv0 + n_kv - 1 of key segment seg.
 struct Unit {
   int bh;
   int tile0;
-  int n_kv0, n_kv1;  // key tiles each query tile needs (0 = tile absent)
+  int seg;
+  int kv0;           // first key tile of the segment
+  int n_kv0, n_kv1;  // key tiles each query tile takes from the segment (0 = nothing to do)
   int n_max;
 };
 
@@ -117,12 +128,21 @@ __device__ __forceinline__ bool unit_at(int k, const FwdParams& p, Unit& u) {
   const long long L = static_cast<long long>(k) * G + ((k & 1) ? (G - 1 - c) : c);
   if (L >= p.n_units) return false;
   const int l = static_cast<int>(L);
-  u.bh = l % p.BH;
-  const int pair = p.n_pairs - 1 - l / p.BH;
+  u.seg = l % p.splits;
+  const int r = l / p.splits;
+  u.bh = r % p.BH;
+  const int pair = p.n_pairs - 1 - r / p.BH;
   u.tile0 = 2 * pair;
+  u.kv0 = u.seg * p.seg_tiles;
+  const int kv_end = u.kv0 + p.seg_tiles < p.n_tiles ? u.kv0 + p.seg_tiles : p.n_tiles;
   const bool has1 = u.tile0 + 1 < p.n_tiles;
-  u.n_kv0 = p.causal ? u.tile0 + 1 : p.n_tiles;
-  u.n_kv1 = has1 ? (p.causal ? u.tile0 + 2 : p.n_tiles) : 0;
+  // key tiles each query tile needs in total, then the part inside this segment
+  const int need0 = p.causal ? u.tile0 + 1 : p.n_tiles;
+  const int need1 = has1 ? (p.causal ? u.tile0 + 2 : p.n_tiles) : 0;
+  const int e0 = need0 < kv_end ? need0 : kv_end;
+  const int e1 = need1 < kv_end ? need1 : kv_end;
+  u.n_kv0 = e0 > u.kv0 ? e0 - u.kv0 : 0;
+  u.n_kv1 = e1 > u.kv0 ? e1 - u.kv0 : 0;
   u.n_max = u.n_kv0 > u.n_kv1 ? u.n_kv0 : u.n_kv1;
   return true;
 }
@@ -212,8 +232,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = true;
       Unit w;
       for (int k = 0; ok && unit_at(k, p, w); ++k) {
+        if (w.n_max == 0) continue;  // a key segment past this pair's last key tile
         // The Q buffer is reused: wait until both issuers' last Q K^T of the previous unit is done.
-        if (k > 0 && !wd.wait(bar(L::kBarQFree), parity(k - 1))) break;
+        if (units > 0 && !wd.wait(bar(L::kBarQFree), parity(units - 1))) break;
         const int nq = w.n_kv1 > 0 ? 2 : 1;
         mbar_arrive_expect_tx(bar(L::kBarQFull), nq * L::kTileBytes);
         for (int t = 0; t < nq; ++t) {
@@ -235,12 +256,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           mbar_arrive_expect_tx(full, ((i > 0) + (i < w.n_max)) * L::kTileBytes);
           if (i > 0) {
             for (int s = 0; s < L::kSub; ++s)
-              tma_load_3d(stage + s * kSubTileBytes, &tm_v, full, 64 * s, (i - 1) * kBlockN, w.bh, pol_kv);
+              tma_load_3d(stage + s * kSubTileBytes, &tm_v, full, 64 * s, (w.kv0 + i - 1) * kBlockN, w.bh, pol_kv);
           }
           if (i < w.n_max) {
             for (int s = 0; s < L::kSub; ++s)
-              tma_load_3d(stage + L::kTileBytes + s * kSubTileBytes, &tm_k, full, 64 * s, i * kBlockN, w.bh,
-                          pol_kv);
+              tma_load_3d(stage + L::kTileBytes + s * kSubTileBytes, &tm_k, full, 64 * s, (w.kv0 + i) * kBlockN,
+                          w.bh, pol_kv);
           }
           ++it;
         }
@@ -280,13 +301,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       int it = 0;       // ring items consumed
       int p_waits = 0;  // P_t handshakes consumed
       int used = 0;     // earlier units in which tile t existed (its O_t is read by an epilogue)
+      int units = 0;    // units with work, in the producer's Q-load order
       bool ok = true;
       Unit w;
       for (int k = 0; ok && unit_at(k, p, w); ++k) {
+        if (w.n_max == 0) continue;
         const int n_kv = t ? w.n_kv1 : w.n_kv0;
         // Item 0 (K_0).  Every item is waited for and released by both issuers,
         // whether or not this tile uses it, so the ring's two-arrival phases stay aligned.
-        if (!wd.wait(bar(L::kBarQFull), parity(k)) ||
+        if (!wd.wait(bar(L::kBarQFull), parity(units++)) ||
             !wd.wait(bar(L::kBarFull + it % L::kStages), parity(it / L::kStages))) {
           ok = false;
           break;
@@ -383,14 +406,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int q = 0; q < 4; ++q) tmem_ld_x32(t_s + 32u * q, s[q]);
 #pragma unroll
           for (int q = 0; q < 4; ++q) tmem_wait_ld_x32(s[q]);
-          if (p.causal && j == tile) {
+          if (p.causal && w.kv0 + j == tile) {
 #pragma unroll
             for (int q = 0; q < 4; ++q)
 #pragma unroll
               for (int i = 0; i < 32; ++i)
                 if (32 * q + i > r_local) s[q][i] = __float_as_uint(-INFINITY);
-          } else if (ragged_keys && j == p.n_tiles - 1) {
-            const int valid = p.N - j * kBlockN;
+          } else if (ragged_keys && w.kv0 + j == p.n_tiles - 1) {
+            const int valid = p.N - (w.kv0 + j) * kBlockN;
 #pragma unroll
             for (int q = 0; q < 4; ++q)
 #pragma unroll
@@ -480,9 +503,35 @@ __global__ void __launch_bounds__(kThreads, 1)
       ++o_waits;
       tc_fence_after_sync();
 
-      // Epilogue: O = o / l rounded to the output type, lse = (m + log2 l) ln 2.
+      // Epilogue: O = o / l rounded to the output type, lse = (m + log2 l) ln 2;
+      // with a key split, the segment's O in fp32 and its lse go to the workspace.
       const float inv_l = 1.f / l;
       const float2 il2 = make_float2(inv_l, inv_l);
+      const float row_lse = (m_ref + log2f(l)) * 0.69314718055994530942f;
+      if (p.part_o != nullptr) {
+        const size_t prow = (static_cast<size_t>(w.seg) * p.BH + w.bh) * p.N + static_cast<size_t>(row);
+        float* dst = p.part_o + prow * D;
+#pragma unroll
+        for (int c0 = 0; c0 < D; c0 += 32) {
+          uint32_t o[32];
+          tmem_ld_x32(t_o + c0, o);
+          tmem_wait_ld_x32(o);
+          if (row < p.N) {
+            float4* d4 = reinterpret_cast<float4*>(dst + c0);
+#pragma unroll
+            for (int v4 = 0; v4 < 8; ++v4) {
+              const float2 a = __fmul2_rn(make_float2(__uint_as_float(o[4 * v4]), __uint_as_float(o[4 * v4 + 1])), il2);
+              const float2 b = __fmul2_rn(make_float2(__uint_as_float(o[4 * v4 + 2]), __uint_as_float(o[4 * v4 + 3])), il2);
+              d4[v4] = make_float4(a.x, a.y, b.x, b.y);
+            }
+          }
+        }
+        tc_fence_before_sync();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(L::kBarOFree + t));
+        if (row < p.N) p.part_lse[prow] = row_lse;
+        continue;
+      }
       uint16_t* orow = static_cast<uint16_t*>(p.o) +
                        (static_cast<size_t>(w.bh) * p.N + static_cast<size_t>(row)) * D;
 #pragma unroll
@@ -508,7 +557,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(L::kBarOFree + t));
       if (p.lse != nullptr && row < p.N) {
-        p.lse[static_cast<size_t>(w.bh) * p.N + row] = (m_ref + log2f(l)) * 0.69314718055994530942f;
+        p.lse[static_cast<size_t>(w.bh) * p.N + row] = row_lse;
       }
     }
   }

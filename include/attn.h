@@ -35,6 +35,8 @@
 #ifndef EXACT_CAUSAL_ATTENTION_GB300_ATTN_H_
 #define EXACT_CAUSAL_ATTENTION_GB300_ATTN_H_
 
+#include <stddef.h>
+
 #ifdef __cplusplus
 extern "C" {
 #endif
@@ -70,6 +72,43 @@ int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, i
 /* attn_fwd_bf16 -- the same operation and contract with bf16 q, k, v and o. */
 int attn_fwd_bf16(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
                   int N, int D, int causal, float scale, attn_stream_t stream);
+
+/*
+ * attn_fwd_splitkv -- the same operation with the key tiles split into
+ * segments that run as separate work units (page "CUDA KV Cache：分页存储与长上下
+ * 文 Decode 极致优化", section 6.4: when B x heads is too small to fill the GPU
+ * and the sequence is long, each segment produces its own (m, l, o) and a second
+ * kernel merges them with the online-softmax law).  Same arguments and result as
+ * attn_fwd, plus:
+ *   kv_splits       : requested segments, 1 .. 64 (fewer are used when N has
+ *                     fewer 128-key tiles); see attn_splitkv_default_splits.
+ *   workspace       : device memory owned by the caller, 256-byte aligned, at
+ *                     least attn_splitkv_workspace_bytes(B, H, N, D, kv_splits)
+ *                     bytes, not overlapping q, k, v or o.  It holds the fp32
+ *                     partial outputs and log-sum-exps; its contents on entry do
+ *                     not matter and are overwritten.  Two calls must not share
+ *                     one workspace while both may be running.
+ *   workspace_bytes : its size.
+ * Returns ATTN_ERR_INVALID_ARG for kv_splits outside 1 .. 64, a NULL or too
+ * small workspace, or overlap; ATTN_ERR_UNALIGNED for a misaligned workspace.
+ */
+int attn_fwd_splitkv(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+                     int N, int D, int causal, float scale, int kv_splits, void* workspace,
+                     size_t workspace_bytes, attn_stream_t stream);
+
+/* attn_fwd_splitkv_bf16 -- the same with bf16 q, k, v and o. */
+int attn_fwd_splitkv_bf16(const void* q, const void* k, const void* v, void* o, float* lse, int B,
+                          int H, int N, int D, int causal, float scale, int kv_splits,
+                          void* workspace, size_t workspace_bytes, attn_stream_t stream);
+
+/* Bytes of workspace attn_fwd_splitkv needs for these sizes; 0 for invalid sizes.
+ * Needs no GPU. */
+size_t attn_splitkv_workspace_bytes(int B, int H, int N, int D, int kv_splits);
+
+/* A split count for the current device: about two work units per SM, capped by
+ * the number of 128-key tiles and by 64.  Negative attn_status on bad sizes or a
+ * non-sm_103 device. */
+int attn_splitkv_default_splits(int B, int H, int N, int D);
 
 /*
  * attn_device_status -- synchronises `stream`, then reads and clears the

@@ -87,3 +87,34 @@ def test_binding_rejects_cpu_tensors():
     x = torch.zeros(1, 1, 4, 64, dtype=torch.float16)
     with pytest.raises(TypeError):
         eca.attn_fwd(x, x, x)
+
+
+def test_splitkv_workspace_size_without_gpu(lib):
+    ws = lib.attn_splitkv_workspace_bytes
+    # [splits, BH, N, D] fp32 outputs + [splits, BH, N] fp32 lse, each rounded up to 256 bytes
+    assert ws(1, 2, 256, 64, 2) == 2 * 2 * 256 * 64 * 4 + 2 * 2 * 256 * 4
+    assert ws(1, 1, 1, 128, 4) == 512 + 256  # one key tile: one segment; 512 B of o, 4 B of lse -> 256
+    assert ws(1, 1, 1000, 64, 64) == 8 * 1000 * 64 * 4 + ((8 * 1000 * 4 + 255) // 256) * 256  # 8 key tiles
+    assert ws(0, 1, 256, 64, 2) == 0 and ws(1, 1, 256, 96, 2) == 0 and ws(1, 1, 256, 64, 0) == 0
+    assert ws(1, 1, 256, 64, 65) == 0
+
+
+@pytest.mark.parametrize("fn", ["attn_fwd_splitkv", "attn_fwd_splitkv_bf16"])
+def test_splitkv_argument_errors_without_gpu(lib, fn):
+    f = getattr(lib, fn)
+    W = A + 8 * SZ
+
+    def c(splits=2, ws=W, wsb=1 << 30, **kw):
+        a = dict(q=A, k=A + SZ, v=A + 2 * SZ, o=A + 3 * SZ, lse=None, B=1, H=1, N=512, D=64, causal=1,
+                 scale=0.125)
+        a.update(kw)
+        return f(a["q"], a["k"], a["v"], a["o"], a["lse"], a["B"], a["H"], a["N"], a["D"], a["causal"],
+                 a["scale"], splits, ws, wsb, None)
+
+    assert c(splits=0) == -1
+    assert c(splits=65) == -1
+    assert c(ws=None) == -1
+    assert c(ws=W + 16) == -2
+    assert c(wsb=100) == -1
+    assert c(ws=A) == -1  # workspace overlapping q
+    assert c(D=96) == -3

@@ -1,0 +1,81 @@
+"""GPU parity of the key-split path (segments merged by the second kernel) against
+the FP64 oracle; the merge law is section 6.4 of "CUDA KV Cache：分页存储与长上下文
+Decode 极致优化".  The workspace is filled with NaN bytes before each call: its
+contents on entry must not matter."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+from exact_causal_attention_gb300 import inputs
+
+from helpers import compare, oracle_full, oracle_rows, p_rounding_term, sample_rows
+
+pytestmark = pytest.mark.gpu
+
+
+def run_split(q, k, v, causal, scale, splits):
+    import exact_causal_attention_gb300 as eca
+
+    dq, dk, dv = (x.cuda() for x in (q, k, v))
+    B, H, N, D = q.shape
+    o = torch.full_like(dq, float("nan"))
+    lse = torch.full((B, H, N), float("nan"), dtype=torch.float32, device="cuda")
+    need = eca.splitkv_workspace_bytes(B, H, N, D, splits)
+    assert need > 0
+    ws = torch.full((need + 256,), 0xFF, dtype=torch.uint8, device="cuda")
+    off = (-ws.data_ptr()) % 256
+    eca.attn_fwd_splitkv(dq, dk, dv, o, lse, kv_splits=splits, workspace=ws[off:off + need], causal=causal,
+                         scale=scale)
+    torch.cuda.synchronize()
+    assert eca.device_status() == 0
+    return o.double().cpu().numpy(), lse.double().cpu().numpy()
+
+
+CASES = [
+    # B, H, N, D, dtype, causal, splits
+    (1, 2, 256, 64, "fp16", True, 2),
+    (1, 2, 1000, 128, "bf16", True, 3),
+    (1, 4, 2048, 128, "fp16", False, 4),
+    (2, 1, 129, 64, "fp16", True, 2),
+    (1, 1, 1, 64, "fp16", True, 4),
+    (1, 2, 3000, 64, "bf16", False, 64),
+    (1, 3, 1536, 128, "fp16", True, 5),
+]
+
+
+@pytest.mark.parametrize("B,H,N,D,dtype,causal,splits", CASES)
+def test_splitkv_matches_oracle(cuda_lib, B, H, N, D, dtype, causal, splits):
+    q, k, v = inputs.make_qkv(B, H, N, D, dtype, seed=2000 + N + splits, qk_std=1.5)
+    scale = 1.0 / math.sqrt(D)
+    o, lse = run_split(q, k, v, causal, scale, splits)
+    ro, rl = oracle_full(q, k, v, dtype, causal, scale)
+    compare(o, lse, ro, rl, dtype, p_rounding_term(q, k, v, dtype, causal, scale))
+
+
+def test_splitkv_agrees_with_unsplit_path(cuda_lib):
+    from helpers import run_gpu
+
+    q, k, v = inputs.make_qkv(1, 4, 1500, 128, "fp16", seed=77)
+    o1, l1 = run_gpu(q, k, v, True, 0.088)
+    for splits in (1, 2, 7):
+        o2, l2 = run_split(q, k, v, True, 0.088, splits)
+        assert np.abs(o2 - o1).max() <= 2e-3
+        assert np.abs(l2 - l1).max() <= 2e-5
+
+
+def test_splitkv_long_sequence_few_heads_sampled(cuda_lib):
+    import exact_causal_attention_gb300 as eca
+
+    B, H, N, D = 1, 2, 8192, 128
+    q, k, v = inputs.make_qkv(B, H, N, D, "fp16", seed=31)
+    splits = eca.splitkv_default_splits(B, H, N, D)
+    assert 1 < splits <= 64
+    o, lse = run_split(q, k, v, True, 1.0 / math.sqrt(D), splits)
+    rows = sample_rows(B, H, N, 200, seed=5)
+    ro, rl = oracle_rows(q, k, v, "fp16", True, 1.0 / math.sqrt(D), rows)
+    bh = np.array([r[0] for r in rows])
+    i = np.array([r[1] for r in rows])
+    compare(o.reshape(B * H, N, D)[bh, i], lse.reshape(B * H, N)[bh, i], ro, rl, "fp16")
+    assert np.isfinite(o).all() and np.isfinite(lse).all()
