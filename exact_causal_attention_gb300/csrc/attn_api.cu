@@ -101,9 +101,10 @@ int encode_qkv_map(EncodeTiledFn encode, CUtensorMap* map, const void* ptr, bool
 
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
-bool overlaps(const void* a, const void* b, uint64_t bytes) {
+// Do [a, a + na) and [b, b + nb) intersect?
+bool overlaps(const void* a, uint64_t na, const void* b, uint64_t nb) {
   const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
-  return x < y + bytes && y < x + bytes;
+  return x < y + nb && y < x + na;
 }
 
 // Checks that need no GPU.  Order: pointers, sizes, head dim, scale, alignment, overlap.
@@ -122,7 +123,9 @@ int check_args(const void* q, const void* k, const void* v, const void* o, const
   if (bh > 0x7fffffffull || n_pairs * bh > 0x7fffffffull) return ATTN_ERR_INVALID_ARG;
   const uint64_t bytes = bh * static_cast<uint64_t>(N) * static_cast<uint64_t>(D) * 2;
   if (static_cast<uint64_t>(N) * D * 2 >= (1ull << 40) || bytes >= (1ull << 62)) return ATTN_ERR_INVALID_ARG;
-  if (overlaps(o, q, bytes) || overlaps(o, k, bytes) || overlaps(o, v, bytes)) return ATTN_ERR_INVALID_ARG;
+  if (overlaps(o, bytes, q, bytes) || overlaps(o, bytes, k, bytes) || overlaps(o, bytes, v, bytes)) {
+    return ATTN_ERR_INVALID_ARG;
+  }
   return ATTN_OK;
 }
 
@@ -228,8 +231,8 @@ int attn_fwd_impl(bool bf16, const void* q, const void* k, const void* v, void* 
     const uint64_t need = splitkv_bytes(bh, N, D, ks.splits, &lse_off);
     if (static_cast<uint64_t>(workspace_bytes) < need) return ATTN_ERR_INVALID_ARG;
     const uint64_t io_bytes = bh * static_cast<uint64_t>(N) * static_cast<uint64_t>(D) * 2;
-    if (overlaps(workspace, q, io_bytes) || overlaps(workspace, k, io_bytes) || overlaps(workspace, v, io_bytes) ||
-        overlaps(workspace, o, io_bytes) || overlaps(o, workspace, need)) {
+    if (overlaps(workspace, need, q, io_bytes) || overlaps(workspace, need, k, io_bytes) ||
+        overlaps(workspace, need, v, io_bytes) || overlaps(workspace, need, o, io_bytes)) {
       return ATTN_ERR_INVALID_ARG;
     }
     const uint64_t n_pairs = ((static_cast<uint64_t>(N) + 127) / 128 + 1) / 2;

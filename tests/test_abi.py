@@ -118,3 +118,15 @@ def test_splitkv_argument_errors_without_gpu(lib, fn):
     assert c(wsb=100) == -1
     assert c(ws=A) == -1  # workspace overlapping q
     assert c(D=96) == -3
+
+
+def test_splitkv_adjacent_workspace_is_not_overlap(lib):
+    # q, k, v, o of 1*1*512*64*2 = 64 KiB each; a workspace starting right after o is legal.
+    io = 512 * 64 * 2
+    q, k, v, o = A, A + io, A + 2 * io, A + 3 * io
+    ws = A + 4 * io
+    need = lib.attn_splitkv_workspace_bytes(1, 1, 512, 64, 2)
+    rc = lib.attn_fwd_splitkv(q, k, v, o, None, 1, 1, 512, 64, 1, 0.125, 2, ws, need, None)
+    assert rc not in (-1, -2, -3)  # passes the argument checks (then needs a GPU)
+    rc = lib.attn_fwd_splitkv(q, k, v, o, None, 1, 1, 512, 64, 1, 0.125, 2, o, need, None)
+    assert rc == -1  # workspace on top of o
