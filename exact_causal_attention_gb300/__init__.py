@@ -29,6 +29,7 @@ STATUS = {
     -5: "ATTN_ERR_LAUNCH",
     -6: "ATTN_ERR_TIMEOUT",
     -7: "ATTN_ERR_CUDA",
+    -8: "ATTN_ERR_SCRATCH_LIMIT",
 }
 
 # Every exported symbol of include/attn.h with its ctypes signature.
@@ -38,6 +39,7 @@ SIGNATURES = {
     "attn_fwd_bf16": (_I, [_VP, _VP, _VP, _VP, _VP, _I, _I, _I, _I, _I, _F, _VP]),
     "attn_fwd_splitkv": (_I, [_VP, _VP, _VP, _VP, _VP, _I, _I, _I, _I, _I, _F, _I, _VP, _SZ, _VP]),
     "attn_fwd_splitkv_bf16": (_I, [_VP, _VP, _VP, _VP, _VP, _I, _I, _I, _I, _I, _F, _I, _VP, _SZ, _VP]),
+    "attn_fwd_splitkv_noalloc": (_I, [_VP, _VP, _VP, _VP, _VP, _I, _I, _I, _I, _I, _F, _I, _VP]),
     "attn_splitkv_workspace_bytes": (_SZ, [_I, _I, _I, _I, _I]),
     "attn_splitkv_default_splits": (_I, [_I, _I, _I, _I]),
     "attn_device_status": (_I, [_VP]),

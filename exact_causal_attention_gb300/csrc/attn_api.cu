@@ -12,6 +12,12 @@
 #include "attn_fwd_kernel.cuh"
 #include "splitkv_combine.cuh"
 
+// Scratch of attn_fwd_splitkv_noalloc: one fixed array per device that loads this
+// library, held until the process exits.  In host code this name only stands for
+// the device array; its device address comes from cudaGetSymbolAddress.
+constexpr unsigned long long kNoAllocScratchBytes = 64ull << 20;
+static __device__ __align__(256) unsigned char g_splitkv_scratch[kNoAllocScratchBytes];
+
 namespace {
 
 constexpr int kMaxDevices = 64;
@@ -31,6 +37,7 @@ struct DeviceState {
   bool sm103 = false;
   int sm_count = 0;
   int* status = nullptr;    // address of g_device_status on this device
+  void* scratch = nullptr;  // address of g_splitkv_scratch on this device, set by its first use
   unsigned configured = 0;  // bitmask of kernel instantiations with smem attribute set
 };
 
@@ -303,6 +310,32 @@ int attn_fwd_splitkv_bf16(const void* q, const void* k, const void* v, void* o, 
                        workspace_bytes);
 }
 
+int attn_fwd_splitkv_noalloc(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+                             int N, int D, int causal, float scale, int kv_splits, attn_stream_t stream) {
+  if (kv_splits < 1 || kv_splits > kMaxSplits) return ATTN_ERR_INVALID_ARG;
+  const int rc = check_args(q, k, v, o, lse, B, H, N, D, scale);
+  if (rc != ATTN_OK) return rc;
+  const KeySplit ks = key_split(N, kv_splits);
+  const uint64_t need =
+      splitkv_bytes(static_cast<uint64_t>(B) * static_cast<uint64_t>(H), N, D, ks.splits, nullptr);
+  if (need > kNoAllocScratchBytes) return ATTN_ERR_SCRATCH_LIMIT;
+  void* scratch = nullptr;
+  {
+    std::lock_guard<std::mutex> lock(g_mutex);
+    DeviceState* st = nullptr;
+    const int r = device_state(&st);
+    if (r != ATTN_OK) return r;
+    if (st->scratch == nullptr) {  // first use on this device: look the array's address up once
+      void* ptr = nullptr;
+      if (cudaGetSymbolAddress(&ptr, g_splitkv_scratch) != cudaSuccess || ptr == nullptr) return ATTN_ERR_CUDA;
+      st->scratch = ptr;
+    }
+    scratch = st->scratch;
+  }
+  return attn_fwd_impl(false, q, k, v, o, lse, B, H, N, D, causal, scale, stream, kv_splits, scratch,
+                       static_cast<size_t>(kNoAllocScratchBytes));
+}
+
 size_t attn_splitkv_workspace_bytes(int B, int H, int N, int D, int kv_splits) {
   if (B < 1 || H < 1 || N < 1 || (D != 64 && D != 128) || kv_splits < 1 || kv_splits > kMaxSplits) return 0;
   const KeySplit ks = key_split(N, kv_splits);
@@ -359,6 +392,7 @@ const char* attn_status_string(int status) {
     case ATTN_ERR_LAUNCH: return "kernel launch failed";
     case ATTN_ERR_TIMEOUT: return "a bounded device wait timed out";
     case ATTN_ERR_CUDA: return "CUDA runtime/driver call failed";
+    case ATTN_ERR_SCRATCH_LIMIT: return "the split needs more than the library's fixed 64 MiB scratch";
     default: return "unknown status";
   }
 }

@@ -53,7 +53,8 @@ enum attn_status {
   ATTN_ERR_ARCH = -4,           /* the current device is not an sm_103 part */
   ATTN_ERR_LAUNCH = -5,         /* the CUDA runtime refused the launch (cudaGetLastError) */
   ATTN_ERR_TIMEOUT = -6,        /* a kernel's bounded wait expired (reported by attn_device_status) */
-  ATTN_ERR_CUDA = -7            /* another CUDA runtime/driver call failed */
+  ATTN_ERR_CUDA = -7,           /* another CUDA runtime/driver call failed */
+  ATTN_ERR_SCRATCH_LIMIT = -8   /* attn_fwd_splitkv_noalloc: the split needs more than its fixed scratch */
 };
 
 /*
@@ -100,6 +101,30 @@ int attn_fwd_splitkv(const void* q, const void* k, const void* v, void* o, float
 int attn_fwd_splitkv_bf16(const void* q, const void* k, const void* v, void* o, float* lse, int B,
                           int H, int N, int D, int causal, float scale, int kv_splits,
                           void* workspace, size_t workspace_bytes, attn_stream_t stream);
+
+/*
+ * attn_fwd_splitkv_noalloc -- attn_fwd_splitkv (fp16) for callers that cannot
+ * allocate device memory: code whose device memory is all owned by a host
+ * framework's own pool or budget, plugins that are handed only their input and
+ * output buffers, and latency-bound callers that must not pay for an allocation
+ * call on the hot path.  The pages have no counterpart of this entry point.
+ *
+ * The partial results live in one scratch array that the library declares at
+ * file scope: 64 MiB per device, reserved on every GPU that loads the library
+ * and held until the process exits.  The caller passes q, k, v, o and lse as
+ * for attn_fwd_splitkv, but no workspace; nothing is allocated.  A call whose
+ * split needs more than 64 MiB (see attn_splitkv_workspace_bytes) returns
+ * ATTN_ERR_SCRATCH_LIMIT and launches nothing.
+ * The first call on a device looks up the scratch array's device address (once
+ * per device, with that device current); make that first call before any stream
+ * capture.  Every call uses the same array, which keeps whatever the last call
+ * left there; no part of it needs to start at zero, since each call writes every
+ * value it later reads.  Calls whose kernels may overlap on the GPU (other
+ * streams, other host threads) race on the array: order them.
+ */
+int attn_fwd_splitkv_noalloc(const void* q, const void* k, const void* v, void* o, float* lse, int B,
+                             int H, int N, int D, int causal, float scale, int kv_splits,
+                             attn_stream_t stream);
 
 /* Bytes of workspace attn_fwd_splitkv needs for these sizes; 0 for invalid sizes.
  * Needs no GPU. */
