@@ -51,12 +51,12 @@ def _load():
             dp = ctypes.POINTER(ctypes.c_double)
             lib.oracle_decode.argtypes = [ctypes.c_void_p, dp, ctypes.c_long, ctypes.c_int, ctypes.c_int]
             lib.oracle_decode.restype = ctypes.c_int
-            lib.oracle_attn_fwd.argtypes = [dp, dp, dp, dp, dp, ctypes.c_long, ctypes.c_long,
+            lib.oracle_attn_fwd.argtypes = [dp, dp, dp, dp, dp, ctypes.c_long, ctypes.c_long, ctypes.c_long,
                                             ctypes.c_long, ctypes.c_long, ctypes.c_int,
                                             ctypes.c_double, ctypes.c_int, ctypes.c_long, ctypes.c_int]
             lib.oracle_attn_fwd.restype = ctypes.c_int
             lib.oracle_attn_rows.argtypes = [dp, dp, dp, ctypes.c_long, ctypes.c_long, ctypes.c_long,
-                                             ctypes.c_long, ctypes.c_int, ctypes.c_double,
+                                             ctypes.c_long, ctypes.c_long, ctypes.c_int, ctypes.c_double,
                                              ctypes.POINTER(ctypes.c_long), ctypes.c_long, dp, dp,
                                              ctypes.c_int]
             lib.oracle_attn_rows.restype = ctypes.c_int
@@ -83,17 +83,25 @@ def decode(bits: np.ndarray, dtype: str, nthreads: int = 0) -> np.ndarray:
     return out
 
 
+def _shapes(q, k, v):
+    if q.ndim != 4 or k.ndim != 4 or k.shape != v.shape:
+        raise ValueError("q is [B, H, N, D]; k and v share one [B, Hkv, N, D] shape")
+    B, H, N, D = q.shape
+    if k.shape[0] != B or k.shape[2:] != (N, D) or k.shape[1] < 1 or H % k.shape[1] != 0:
+        raise ValueError("k, v must be [B, Hkv, N, D] with Hkv dividing H")
+    return B, H, k.shape[1], N, D
+
+
 def attention(q, k, v, causal: bool, scale: float, mode: str = "two_pass", tile: int = 128,
               nthreads: int = 0):
-    """O [B,H,N,D] and lse [B,H,N] in float64 for float64-convertible inputs of shape [B,H,N,D]."""
+    """O [B,H,N,D] and lse [B,H,N] in float64.  q is [B,H,N,D]; k, v are [B,Hkv,N,D] with Hkv
+    dividing H (query head h reads key/value head h // (H // Hkv))."""
     q, k, v = _f64(q), _f64(k), _f64(v)
-    if q.ndim != 4 or q.shape != k.shape or q.shape != v.shape:
-        raise ValueError("q, k, v must share one [B, H, N, D] shape")
-    B, H, N, D = q.shape
+    B, H, Hkv, N, D = _shapes(q, k, v)
     o = np.empty_like(q)
     lse = np.empty((B, H, N), dtype=np.float64)
     m = {"two_pass": MODE_TWO_PASS, "online": MODE_ONLINE}[mode]
-    rc = _load().oracle_attn_fwd(_dptr(q), _dptr(k), _dptr(v), _dptr(o), _dptr(lse), B, H, N, D,
+    rc = _load().oracle_attn_fwd(_dptr(q), _dptr(k), _dptr(v), _dptr(o), _dptr(lse), B, H, Hkv, N, D,
                                  int(bool(causal)), float(scale), m, int(tile), nthreads)
     if rc != 0:
         raise ValueError("oracle_attn_fwd rejected its arguments")
@@ -103,11 +111,11 @@ def attention(q, k, v, causal: bool, scale: float, mode: str = "two_pass", tile:
 def attention_rows(q, k, v, causal: bool, scale: float, rows, nthreads: int = 0):
     """O and lse of selected rows only; rows is a sequence of (b*H + h, i) pairs."""
     q, k, v = _f64(q), _f64(k), _f64(v)
-    B, H, N, D = q.shape
+    B, H, Hkv, N, D = _shapes(q, k, v)
     r = np.ascontiguousarray(np.asarray(rows, dtype=np.int64).reshape(-1, 2))
     o = np.empty((r.shape[0], D), dtype=np.float64)
     lse = np.empty((r.shape[0],), dtype=np.float64)
-    rc = _load().oracle_attn_rows(_dptr(q), _dptr(k), _dptr(v), B, H, N, D, int(bool(causal)),
+    rc = _load().oracle_attn_rows(_dptr(q), _dptr(k), _dptr(v), B, H, Hkv, N, D, int(bool(causal)),
                                   float(scale), r.ctypes.data_as(ctypes.POINTER(ctypes.c_long)),
                                   r.shape[0], _dptr(o), _dptr(lse), nthreads)
     if rc != 0:

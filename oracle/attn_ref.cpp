@@ -35,6 +35,11 @@
 //   * inputs arrive as fp16 / bf16 bit patterns and are decoded exactly to
 //     double here, with a decoder written from the IEEE-754 binary16 and the
 //     bfloat16 (truncated binary32) formats.
+//
+// Grouped heads (page "CUDA KV Cache：分页存储与长上下文 Decode 极致优化", section
+// 3.3): with H query heads and Hkv key/value heads, g = H / Hkv, query head h
+// reads key/value head floor(h / g) of the same batch entry.  Hkv = H is the
+// ordinary one-to-one case.
 #include <cmath>
 #include <cstdint>
 #include <cstring>
@@ -83,12 +88,19 @@ struct Problem {
   long B, H, N, D;
   int causal;
   double scale;
+  long Hkv;  // key/value heads; H is a multiple of it
 };
+
+// Key/value slice read by query slice bh = b * H + h.
+long kv_slice(const Problem& p, long bh) {
+  const long b = bh / p.H, h = bh % p.H;
+  return b * p.Hkv + h / (p.H / p.Hkv);
+}
 
 // Scores of query row i of slice bh against keys 0..last, written to s.
 void score_row(const Problem& p, long bh, long i, long last, std::vector<double>& s) {
   const double* qi = p.q + (bh * p.N + i) * p.D;
-  const double* kb = p.k + bh * p.N * p.D;
+  const double* kb = p.k + kv_slice(p, bh) * p.N * p.D;
   s.resize(last + 1);
   for (long j = 0; j <= last; ++j) {
     const double* kj = kb + j * p.D;
@@ -112,7 +124,7 @@ void row_two_pass(const Problem& p, long bh, long i, double* o, double* lse,
   }
   double l = 0.0;
   for (long j = 0; j <= last; ++j) l += std::exp(s[j] - m);
-  const double* vb = p.v + bh * p.N * p.D;
+  const double* vb = p.v + kv_slice(p, bh) * p.N * p.D;
   for (long j = 0; j <= last; ++j) {
     const double w = std::exp(s[j] - m) / l;
     const double* vj = vb + j * p.D;
@@ -127,7 +139,7 @@ void row_online(const Problem& p, long bh, long i, long tile, double* o, double*
   const double neg_inf = -std::numeric_limits<double>::infinity();
   const long last = p.causal ? i : p.N - 1;
   score_row(p, bh, i, last, s);
-  const double* vb = p.v + bh * p.N * p.D;
+  const double* vb = p.v + kv_slice(p, bh) * p.N * p.D;
   acc.assign(p.D, 0.0);
   double m = neg_inf;  // running max
   double l = 0.0;      // running sum of exp(s - m)
@@ -188,6 +200,7 @@ void parallel_rows(long count, int nthreads, F f) {
 bool valid(const Problem& p, int mode, long tile) {
   if (!p.q || !p.k || !p.v) return false;
   if (p.B < 1 || p.H < 1 || p.N < 1 || p.D < 1) return false;
+  if (p.Hkv < 1 || p.H % p.Hkv != 0) return false;
   if (mode != 0 && mode != 1) return false;
   if (mode == 1 && tile < 1) return false;
   return true;
@@ -206,12 +219,12 @@ int oracle_decode(const uint16_t* bits, double* out, long n, int dtype, int nthr
   return 0;
 }
 
-// Full forward: o is [B, H, N, D], lse is [B, H, N] (may be null).
+// Full forward: q, o are [B, H, N, D], k, v are [B, Hkv, N, D], lse is [B, H, N] (may be null).
 // mode 0 = two-pass definition, mode 1 = online recurrence with key tiles of `tile`.
 int oracle_attn_fwd(const double* q, const double* k, const double* v, double* o, double* lse,
-                    long B, long H, long N, long D, int causal, double scale, int mode, long tile,
-                    int nthreads) {
-  Problem p{q, k, v, B, H, N, D, causal, scale};
+                    long B, long H, long Hkv, long N, long D, int causal, double scale, int mode,
+                    long tile, int nthreads) {
+  Problem p{q, k, v, B, H, N, D, causal, scale, Hkv};
   if (!valid(p, mode, tile) || !o) return -1;
   parallel_rows(B * H * N, nthreads, [&](long lo, long hi) {
     std::vector<double> s, acc;
@@ -230,10 +243,10 @@ int oracle_attn_fwd(const double* q, const double* k, const double* v, double* o
 }
 
 // Selected rows only: rows holds nrows pairs (bh, i); o_rows is [nrows, D], lse_rows [nrows].
-int oracle_attn_rows(const double* q, const double* k, const double* v, long B, long H, long N,
-                     long D, int causal, double scale, const long* rows, long nrows,
+int oracle_attn_rows(const double* q, const double* k, const double* v, long B, long H, long Hkv,
+                     long N, long D, int causal, double scale, const long* rows, long nrows,
                      double* o_rows, double* lse_rows, int nthreads) {
-  Problem p{q, k, v, B, H, N, D, causal, scale};
+  Problem p{q, k, v, B, H, N, D, causal, scale, Hkv};
   if (!valid(p, 0, 1) || !rows || !o_rows || !lse_rows || nrows < 0) return -1;
   for (long r = 0; r < nrows; ++r) {
     if (rows[2 * r] < 0 || rows[2 * r] >= B * H || rows[2 * r + 1] < 0 || rows[2 * r + 1] >= N)

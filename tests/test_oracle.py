@@ -241,3 +241,34 @@ def test_oracle_rejects_bad_arguments():
     with pytest.raises(ValueError):
         oracle.attention_rows(np.zeros((1, 1, 2, 2)), np.zeros((1, 1, 2, 2)), np.zeros((1, 1, 2, 2)), True,
                               1.0, [(0, 2)])
+
+
+# ---------------------------------------------------------------- grouped heads
+
+@pytest.mark.parametrize("H,Hkv", [(4, 1), (4, 2), (6, 3), (8, 8)])
+@pytest.mark.parametrize("mode", ["two_pass", "online"])
+def test_grouped_heads_equal_expanded_heads(H, Hkv, mode):
+    # The decode page's section 3.3: copying each key/value head g = H / Hkv times
+    # (repeat_interleave) turns grouped attention into ordinary attention; the
+    # oracle's head map h -> h // g must give exactly that result.
+    B, N, D = 2, 21, 8
+    q = rnd((B, H, N, D), 50 + H)
+    k, v = rnd((B, Hkv, N, D), 60 + Hkv), rnd((B, Hkv, N, D), 70 + Hkv)
+    g = H // Hkv
+    ke, ve = np.repeat(k, g, axis=1), np.repeat(v, g, axis=1)
+    for causal in (True, False):
+        o, lse = oracle.attention(q, k, v, causal, 0.3, mode=mode, tile=4)
+        oe, lsee = oracle.attention(q, ke, ve, causal, 0.3, mode=mode, tile=4)
+        assert np.array_equal(o, oe) and np.array_equal(lse, lsee)
+
+
+def test_grouped_heads_rows_entry_and_errors():
+    B, H, Hkv, N, D = 1, 4, 2, 30, 8
+    q, k, v = rnd((B, H, N, D), 80), rnd((B, Hkv, N, D), 81), rnd((B, Hkv, N, D), 82)
+    o, lse = oracle.attention(q, k, v, True, 0.3)
+    rows = [(0, 0), (3, 29), (1, 7), (2, 15)]
+    ro, rl = oracle.attention_rows(q, k, v, True, 0.3, rows)
+    for r, (bh, i) in enumerate(rows):
+        assert np.array_equal(ro[r], o.reshape(B * H, N, D)[bh, i])
+    with pytest.raises(ValueError):
+        oracle.attention(q, rnd((B, 3, N, D), 1), rnd((B, 3, N, D), 2), True, 0.3)  # 3 does not divide 4

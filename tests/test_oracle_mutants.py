@@ -34,6 +34,8 @@ MUTANTS = {
     "online_beta_dropped": ("l = alpha * l + beta * l_tile;", "l = alpha * l + l_tile;"),
     "fp16_exponent_bias": ("exponent - 25);", "exponent - 24);"),
     "bf16_hidden_bit": ("static_cast<double>(128 + mantissa)", "static_cast<double>(mantissa)"),
+    "head_map_modulo": ("return b * p.Hkv + h / (p.H / p.Hkv);", "return b * p.Hkv + h % p.Hkv;"),
+    "head_map_batch": ("return b * p.Hkv + h / (p.H / p.Hkv);", "return b * p.H + h / (p.H / p.Hkv);"),
 }
 
 
