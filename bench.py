@@ -361,6 +361,29 @@ def bench_ours(args, w):
                    "launches_per_call": 2}
         del sq, sk, sv, so, sl, ws
 
+    # Grouped key/value heads (GQA, 4 query heads per key/value head), causal B=1 H=32 Hkv=8 N=8192 D=128.
+    gqa = {}
+    if not args.no_sweep and rank == 0:
+        gq, _, _ = inputs.make_qkv(1, 32, 8192, 128, "fp16", seed=6)
+        _, gk, gv = inputs.make_qkv(1, 8, 8192, 128, "fp16", seed=7)
+        gq, gk, gv = gq.to(dev), gk.to(dev), gv.to(dev)
+        go = torch.empty_like(gq)
+        gl = torch.empty((1, 32, 8192), dtype=torch.float32, device=dev)
+        times = []
+        for i in range(13):
+            flush.zero_()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            eca.attn_fwd_gqa(gq, gk, gv, causal=True, o=go, lse=gl, stream=stream)
+            b.record(stream)
+            times.append((a, b))
+        torch.cuda.synchronize(dev)
+        ms = sorted(a.elapsed_time(b) for a, b in times[3:])
+        med = ms[len(ms) // 2]
+        gqa = {"workload": "causal_b1_h32_hkv8_n8192_d128_fp16", "ms": round(med, 4),
+               "tflops": round(flops / (med * 1e-3) / 1e12, 1)}
+        del gq, gk, gv, go, gl
+
     fp16_peak = None
     if not args.no_peak and rank == 0:
         a = torch.randn(8192, 8192, device=dev, dtype=torch.float16)
@@ -412,6 +435,7 @@ def bench_ours(args, w):
         "clocks": clocks,
         "sweep": sweep,
         "splitkv": splitkv,
+        "gqa": gqa,
         "fp16_matmul_peak_tflops": fp16_peak,
         "frac_of_measured_fp16_matmul": (achieved / fp16_peak) if fp16_peak else None,
         "frac_of_datasheet_dense_fp16": achieved / 2250.0,

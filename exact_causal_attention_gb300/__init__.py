@@ -12,7 +12,7 @@ import math
 import os
 import threading
 
-__all__ = ["attn_fwd", "attn_fwd_into", "attn_fwd_splitkv", "splitkv_workspace_bytes",
+__all__ = ["attn_fwd", "attn_fwd_into", "attn_fwd_gqa", "attn_fwd_splitkv", "splitkv_workspace_bytes",
            "splitkv_default_splits", "load_library", "device_status", "watchdog_selftest", "AttnError",
            "STATUS"]
 
@@ -37,6 +37,8 @@ _VP, _I, _F, _U, _SZ = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_u
 SIGNATURES = {
     "attn_fwd": (_I, [_VP, _VP, _VP, _VP, _VP, _I, _I, _I, _I, _I, _F, _VP]),
     "attn_fwd_bf16": (_I, [_VP, _VP, _VP, _VP, _VP, _I, _I, _I, _I, _I, _F, _VP]),
+    "attn_fwd_gqa": (_I, [_VP, _VP, _VP, _VP, _VP, _I, _I, _I, _I, _I, _I, _F, _VP]),
+    "attn_fwd_gqa_bf16": (_I, [_VP, _VP, _VP, _VP, _VP, _I, _I, _I, _I, _I, _I, _F, _VP]),
     "attn_fwd_splitkv": (_I, [_VP, _VP, _VP, _VP, _VP, _I, _I, _I, _I, _I, _F, _I, _VP, _SZ, _VP]),
     "attn_fwd_splitkv_bf16": (_I, [_VP, _VP, _VP, _VP, _VP, _I, _I, _I, _I, _I, _F, _I, _VP, _SZ, _VP]),
     "attn_fwd_splitkv_noalloc": (_I, [_VP, _VP, _VP, _VP, _VP, _I, _I, _I, _I, _I, _F, _I, _VP]),
@@ -144,6 +146,36 @@ def attn_fwd(q, k, v, causal: bool = True, scale: float | None = None, return_ls
     lse = torch.empty(q.shape[:3], dtype=torch.float32, device=q.device) if return_lse else None
     attn_fwd_into(q, k, v, o, lse, causal=causal, scale=scale, stream=stream)
     return (o, lse) if return_lse else o
+
+
+def attn_fwd_gqa(q, k, v, causal: bool = True, scale: float | None = None, o=None, lse=None, stream=None):
+    """Grouped-head attention: q [B,H,N,D], k and v [B,Hkv,N,D] with Hkv dividing H; query head h
+    reads key/value head h // (H // Hkv).  Returns (o, lse)."""
+    import torch
+
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        if not isinstance(t, torch.Tensor) or not t.is_cuda or t.dim() != 4 or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous 4-D CUDA tensor")
+    B, H, N, D = q.shape
+    if k.shape != v.shape or k.shape[0] != B or tuple(k.shape[2:]) != (N, D):
+        raise ValueError("k, v must be [B, Hkv, N, D] matching q's B, N, D")
+    if not (q.dtype == k.dtype == v.dtype) or q.dtype not in (torch.float16, torch.bfloat16):
+        raise TypeError("q, k, v must all be float16 or all bfloat16")
+    Hkv = k.shape[1]
+    if o is None:
+        o = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    lib = load_library()
+    fn = lib.attn_fwd_gqa_bf16 if q.dtype == torch.bfloat16 else lib.attn_fwd_gqa
+    with torch.cuda.device(q.device):
+        rc = fn(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(), B, H, Hkv, N, D,
+                int(bool(causal)), float(scale), _stream_handle(stream))
+    if rc != 0:
+        raise AttnError(rc, "attn_fwd_gqa")
+    return o, lse
 
 
 def splitkv_workspace_bytes(B: int, H: int, N: int, D: int, kv_splits: int) -> int:

@@ -116,9 +116,10 @@ bool overlaps(const void* a, uint64_t na, const void* b, uint64_t nb) {
 
 // Checks that need no GPU.  Order: pointers, sizes, head dim, scale, alignment, overlap.
 int check_args(const void* q, const void* k, const void* v, const void* o, const float* lse, int B,
-               int H, int N, int D, float scale) {
+               int H, int N, int D, float scale, int Hkv = 0) {
+  if (Hkv == 0) Hkv = H;
   if (!q || !k || !v || !o) return ATTN_ERR_INVALID_ARG;
-  if (B < 1 || H < 1 || N < 1) return ATTN_ERR_INVALID_ARG;
+  if (B < 1 || H < 1 || N < 1 || Hkv < 1 || H % Hkv != 0) return ATTN_ERR_INVALID_ARG;
   if (D != 64 && D != 128) return ATTN_ERR_UNSUPPORTED_D;
   if (!std::isfinite(scale) || !(scale > 0.f)) return ATTN_ERR_INVALID_ARG;
   if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16)) return ATTN_ERR_UNALIGNED;
@@ -129,8 +130,9 @@ int check_args(const void* q, const void* k, const void* v, const void* o, const
   // Grid (pairs x heads) and tensor-map extents must fit; byte sizes stay far below 2^63.
   if (bh > 0x7fffffffull || n_pairs * bh > 0x7fffffffull) return ATTN_ERR_INVALID_ARG;
   const uint64_t bytes = bh * static_cast<uint64_t>(N) * static_cast<uint64_t>(D) * 2;
+  const uint64_t kv_bytes = bytes / static_cast<uint64_t>(H / Hkv);
   if (static_cast<uint64_t>(N) * D * 2 >= (1ull << 40) || bytes >= (1ull << 62)) return ATTN_ERR_INVALID_ARG;
-  if (overlaps(o, bytes, q, bytes) || overlaps(o, bytes, k, bytes) || overlaps(o, bytes, v, bytes)) {
+  if (overlaps(o, bytes, q, bytes) || overlaps(o, bytes, k, kv_bytes) || overlaps(o, bytes, v, kv_bytes)) {
     return ATTN_ERR_INVALID_ARG;
   }
   return ATTN_OK;
@@ -161,9 +163,10 @@ uint64_t splitkv_bytes(uint64_t bh, uint64_t N, uint64_t D, uint64_t splits, uin
 }
 
 template <int D, bool BF16>
-int launch(const void* q, const void* k, const void* v, void* o, float* lse, int BH, int N, int causal,
-           float scale, cudaStream_t stream, DeviceState* st, EncodeTiledFn encode, const KeySplit& ks,
+int launch(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int Hkv, int N,
+           int causal, float scale, cudaStream_t stream, DeviceState* st, EncodeTiledFn encode, const KeySplit& ks,
            float* part_o, float* part_lse) {
+  const int BH = B * H;
   using L = eca::FwdSmem<D>;
   auto kernel = eca::attn_fwd_kernel<D, BF16>;
   const unsigned bit = 1u << ((D == 128 ? 2 : 0) + (BF16 ? 1 : 0));
@@ -176,8 +179,8 @@ int launch(const void* q, const void* k, const void* v, void* o, float* lse, int
   }
   CUtensorMap tq, tk, tv;
   int rc = encode_qkv_map(encode, &tq, q, BF16, D, N, BH);
-  if (rc == ATTN_OK) rc = encode_qkv_map(encode, &tk, k, BF16, D, N, BH);
-  if (rc == ATTN_OK) rc = encode_qkv_map(encode, &tv, v, BF16, D, N, BH);
+  if (rc == ATTN_OK) rc = encode_qkv_map(encode, &tk, k, BF16, D, N, B * Hkv);
+  if (rc == ATTN_OK) rc = encode_qkv_map(encode, &tv, v, BF16, D, N, B * Hkv);
   if (rc != ATTN_OK) return rc;
 
   eca::FwdParams p;
@@ -190,6 +193,8 @@ int launch(const void* q, const void* k, const void* v, void* o, float* lse, int
   p.n_tiles = (N + eca::kBlockM - 1) / eca::kBlockM;
   p.n_pairs = (p.n_tiles + 1) / 2;
   p.BH = BH;
+  p.H = H;
+  p.Hkv = Hkv;
   p.splits = ks.splits;
   p.seg_tiles = ks.seg_tiles;
   p.n_units = p.n_pairs * BH * ks.splits;
@@ -223,8 +228,9 @@ int launch(const void* q, const void* k, const void* v, void* o, float* lse, int
 
 int attn_fwd_impl(bool bf16, const void* q, const void* k, const void* v, void* o, float* lse, int B,
                   int H, int N, int D, int causal, float scale, attn_stream_t stream, int kv_splits = 0,
-                  void* workspace = nullptr, size_t workspace_bytes = 0) {
-  int rc = check_args(q, k, v, o, lse, B, H, N, D, scale);
+                  void* workspace = nullptr, size_t workspace_bytes = 0, int Hkv = 0) {
+  if (Hkv == 0) Hkv = H;
+  int rc = check_args(q, k, v, o, lse, B, H, N, D, scale, Hkv);
   if (rc != ATTN_OK) return rc;
   KeySplit ks{(N + eca::kBlockN - 1) / eca::kBlockN, 1};
   float* part_o = nullptr;
@@ -238,8 +244,9 @@ int attn_fwd_impl(bool bf16, const void* q, const void* k, const void* v, void* 
     const uint64_t need = splitkv_bytes(bh, N, D, ks.splits, &lse_off);
     if (static_cast<uint64_t>(workspace_bytes) < need) return ATTN_ERR_INVALID_ARG;
     const uint64_t io_bytes = bh * static_cast<uint64_t>(N) * static_cast<uint64_t>(D) * 2;
-    if (overlaps(workspace, need, q, io_bytes) || overlaps(workspace, need, k, io_bytes) ||
-        overlaps(workspace, need, v, io_bytes) || overlaps(workspace, need, o, io_bytes)) {
+    const uint64_t kv_bytes = io_bytes / static_cast<uint64_t>(H / Hkv);
+    if (overlaps(workspace, need, q, io_bytes) || overlaps(workspace, need, k, kv_bytes) ||
+        overlaps(workspace, need, v, kv_bytes) || overlaps(workspace, need, o, io_bytes)) {
       return ATTN_ERR_INVALID_ARG;
     }
     const uint64_t n_pairs = ((static_cast<uint64_t>(N) + 127) / 128 + 1) / 2;
@@ -254,14 +261,16 @@ int attn_fwd_impl(bool bf16, const void* q, const void* k, const void* v, void* 
   EncodeTiledFn encode = nullptr;
   r = get_encode_fn(&encode);
   if (r != ATTN_OK) return r;
-  const int BH = B * H;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   if (D == 128) {
-    return bf16 ? launch<128, true>(q, k, v, o, lse, BH, N, causal, scale, s, st, encode, ks, part_o, part_lse)
-                : launch<128, false>(q, k, v, o, lse, BH, N, causal, scale, s, st, encode, ks, part_o, part_lse);
+    return bf16 ? launch<128, true>(q, k, v, o, lse, B, H, Hkv, N, causal, scale, s, st, encode, ks, part_o,
+                                    part_lse)
+                : launch<128, false>(q, k, v, o, lse, B, H, Hkv, N, causal, scale, s, st, encode, ks, part_o,
+                                     part_lse);
   }
-  return bf16 ? launch<64, true>(q, k, v, o, lse, BH, N, causal, scale, s, st, encode, ks, part_o, part_lse)
-              : launch<64, false>(q, k, v, o, lse, BH, N, causal, scale, s, st, encode, ks, part_o, part_lse);
+  return bf16 ? launch<64, true>(q, k, v, o, lse, B, H, Hkv, N, causal, scale, s, st, encode, ks, part_o, part_lse)
+              : launch<64, false>(q, k, v, o, lse, B, H, Hkv, N, causal, scale, s, st, encode, ks, part_o,
+                                  part_lse);
 }
 
 // One thread waits on a barrier that nothing ever arrives on, with a bounded wait.
@@ -292,6 +301,18 @@ int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, i
 int attn_fwd_bf16(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N,
                   int D, int causal, float scale, attn_stream_t stream) {
   return attn_fwd_impl(true, q, k, v, o, lse, B, H, N, D, causal, scale, stream);
+}
+
+int attn_fwd_gqa(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int Hkv,
+                 int N, int D, int causal, float scale, attn_stream_t stream) {
+  if (Hkv < 1) return ATTN_ERR_INVALID_ARG;
+  return attn_fwd_impl(false, q, k, v, o, lse, B, H, N, D, causal, scale, stream, 0, nullptr, 0, Hkv);
+}
+
+int attn_fwd_gqa_bf16(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int Hkv,
+                      int N, int D, int causal, float scale, attn_stream_t stream) {
+  if (Hkv < 1) return ATTN_ERR_INVALID_ARG;
+  return attn_fwd_impl(true, q, k, v, o, lse, B, H, N, D, causal, scale, stream, 0, nullptr, 0, Hkv);
 }
 
 int attn_fwd_splitkv(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N,

@@ -20,7 +20,10 @@
 //     heads), a unit also names a segment of key tiles and its epilogue writes
 //     the segment's normalised partial output and log-sum-exp in fp32 for a
 //     separate merge ("CUDA KV Cache：分页存储与长上下文 Decode 极致优化",
-//     section 6.4).  352 threads:
+//     section 6.4).  Grouped heads (same page, section 3.3): query head h
+//     reads key/value head h / (H / Hkv) directly, with no copy; the heads of
+//     one group are adjacent in the unit order so their K/V tiles come from L2.
+//     352 threads:
 //       warps 0-3  softmax for query tile 0     warps 4-7  softmax for query tile 1
 //       warp 8     TMA producer (Q once per unit, then ring items {V_j, K_j+1})
 //       warp 9     TMEM owner; tcgen05.mma issuer for query tile 0
@@ -71,6 +74,8 @@ struct FwdParams {
   int n_tiles;    // ceil(N / 128), for queries and keys alike
   int n_pairs;    // ceil(n_tiles / 2)
   int BH;
+  int H;          // query heads per batch entry
+  int Hkv;        // key/value heads per batch entry (H is a multiple)
   int splits;     // key segments (1 = no split)
   int seg_tiles;  // key tiles per segment
   int n_units;    // n_pairs * BH * splits
@@ -113,6 +118,7 @@ struct FwdSmem {
 // key tiles kv0 .. kv0 + n_kv - 1 of key segment seg.
 struct Unit {
   int bh;
+  int kvh;  // key/value slice: query head h of batch b reads head h / (H / Hkv) of batch b
   int tile0;
   int seg;
   int kv0;           // first key tile of the segment
@@ -131,6 +137,7 @@ __device__ __forceinline__ bool unit_at(int k, const FwdParams& p, Unit& u) {
   u.seg = l % p.splits;
   const int r = l / p.splits;
   u.bh = r % p.BH;
+  u.kvh = (u.bh / p.H) * p.Hkv + (u.bh % p.H) / (p.H / p.Hkv);
   const int pair = p.n_pairs - 1 - r / p.BH;
   u.tile0 = 2 * pair;
   u.kv0 = u.seg * p.seg_tiles;
@@ -256,12 +263,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           mbar_arrive_expect_tx(full, ((i > 0) + (i < w.n_max)) * L::kTileBytes);
           if (i > 0) {
             for (int s = 0; s < L::kSub; ++s)
-              tma_load_3d(stage + s * kSubTileBytes, &tm_v, full, 64 * s, (w.kv0 + i - 1) * kBlockN, w.bh, pol_kv);
+              tma_load_3d(stage + s * kSubTileBytes, &tm_v, full, 64 * s, (w.kv0 + i - 1) * kBlockN, w.kvh, pol_kv);
           }
           if (i < w.n_max) {
             for (int s = 0; s < L::kSub; ++s)
               tma_load_3d(stage + L::kTileBytes + s * kSubTileBytes, &tm_k, full, 64 * s, (w.kv0 + i) * kBlockN,
-                          w.bh, pol_kv);
+                          w.kvh, pol_kv);
           }
           ++it;
         }

@@ -75,6 +75,23 @@ int attn_fwd_bf16(const void* q, const void* k, const void* v, void* o, float* l
                   int N, int D, int causal, float scale, attn_stream_t stream);
 
 /*
+ * attn_fwd_gqa -- fp16 attention forward with grouped key/value heads (GQA; MQA
+ * when Hkv = 1), page "CUDA KV Cache：分页存储与长上下文 Decode 极致优化", section
+ * 3.3: with g = H / Hkv, query head h reads key/value head floor(h / g) of the
+ * same batch entry, and K/V are not copied per query head.
+ *   q, o : [B, H, N, D].    k, v : [B, Hkv, N, D].    lse : [B, H, N] or NULL.
+ *   Hkv  : >= 1 and divides H.  Hkv = H is attn_fwd.
+ * Everything else as attn_fwd.  Returns ATTN_ERR_INVALID_ARG when Hkv does not
+ * divide H.
+ */
+int attn_fwd_gqa(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+                 int Hkv, int N, int D, int causal, float scale, attn_stream_t stream);
+
+/* attn_fwd_gqa_bf16 -- the same with bf16 q, k, v and o. */
+int attn_fwd_gqa_bf16(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+                      int Hkv, int N, int D, int causal, float scale, attn_stream_t stream);
+
+/*
  * attn_fwd_splitkv -- the same operation with the key tiles split into
  * segments that run as separate work units (page "CUDA KV Cache：分页存储与长上下
  * 文 Decode 极致优化", section 6.4: when B x heads is too small to fill the GPU

@@ -130,3 +130,13 @@ def test_splitkv_adjacent_workspace_is_not_overlap(lib):
     assert rc not in (-1, -2, -3)  # passes the argument checks (then needs a GPU)
     rc = lib.attn_fwd_splitkv(q, k, v, o, None, 1, 1, 512, 64, 1, 0.125, 2, o, need, None)
     assert rc == -1  # workspace on top of o
+
+
+@pytest.mark.parametrize("fn", ["attn_fwd_gqa", "attn_fwd_gqa_bf16"])
+def test_gqa_argument_errors_without_gpu(lib, fn):
+    f = getattr(lib, fn)
+    args = lambda H, Hkv, D=64: (A, A + SZ, A + 2 * SZ, A + 3 * SZ, None, 1, H, Hkv, 256, D, 1, 0.125, None)
+    assert f(*args(8, 3)) == -1  # 3 does not divide 8
+    assert f(*args(8, 0)) == -1
+    assert f(*args(8, 16)) == -1
+    assert f(*args(8, 2, 96)) == -3
