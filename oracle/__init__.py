@@ -19,7 +19,7 @@ import threading
 import numpy as np
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
-_SRC = os.path.join(_HERE, "attn_ref.cpp")
+_SRCS = [os.path.join(_HERE, "attn_ref.cpp"), os.path.join(_HERE, "softmax_ref.cpp")]
 _LIB_PATH = os.path.join(_HERE, "_build", "liboracle.so")
 _lock = threading.Lock()
 _lib = None
@@ -32,10 +32,10 @@ DTYPE_CODES = {"fp16": 0, "bf16": 1}
 def build(force: bool = False) -> str:
     """Compile the oracle shared library with the host C++ compiler."""
     os.makedirs(os.path.dirname(_LIB_PATH), exist_ok=True)
-    stale = (not os.path.exists(_LIB_PATH)) or os.path.getmtime(_LIB_PATH) < os.path.getmtime(_SRC)
+    stale = (not os.path.exists(_LIB_PATH)) or os.path.getmtime(_LIB_PATH) < max(os.path.getmtime(f) for f in _SRCS)
     if force or stale:
         tmp = _LIB_PATH + f".tmp{os.getpid()}"
-        cmd = ["g++", "-O2", "-std=c++17", "-shared", "-fPIC", "-pthread", "-o", tmp, _SRC]
+        cmd = ["g++", "-O2", "-std=c++17", "-shared", "-fPIC", "-pthread", "-o", tmp, *_SRCS]
         subprocess.run(cmd, check=True)
         os.replace(tmp, _LIB_PATH)
     return _LIB_PATH
@@ -60,6 +60,9 @@ def _load():
                                              ctypes.POINTER(ctypes.c_long), ctypes.c_long, dp, dp,
                                              ctypes.c_int]
             lib.oracle_attn_rows.restype = ctypes.c_int
+            lib.oracle_softmax.argtypes = [dp, dp, ctypes.c_long, ctypes.c_long, ctypes.c_int, ctypes.c_long,
+                                           ctypes.c_int]
+            lib.oracle_softmax.restype = ctypes.c_int
             _lib = lib
     return _lib
 
@@ -130,3 +133,16 @@ def attention_from_bits(qb, kb, vb, dtype: str, causal: bool, scale: float, nthr
     if rows is None:
         return attention(q, k, v, causal, scale, nthreads=nthreads)
     return attention_rows(q, k, v, causal, scale, rows, nthreads=nthreads)
+
+
+def softmax(x, mode: str = "two_pass", tile: int = 64, nthreads: int = 0) -> np.ndarray:
+    """Row softmax of a float64-convertible [M, N] matrix, in float64 (``softmax_ref.cpp``)."""
+    x = _f64(x)
+    if x.ndim != 2:
+        raise ValueError("x must be [M, N]")
+    y = np.empty_like(x)
+    m = {"two_pass": MODE_TWO_PASS, "online": MODE_ONLINE}[mode]
+    rc = _load().oracle_softmax(_dptr(x), _dptr(y), x.shape[0], x.shape[1], m, int(tile), nthreads)
+    if rc != 0:
+        raise ValueError("oracle_softmax rejected its arguments")
+    return y
