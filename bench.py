@@ -384,6 +384,32 @@ def bench_ours(args, w):
                "tflops": round(flops / (med * 1e-3) / 1e12, 1)}
         del gq, gk, gv, go, gl
 
+    # Online row softmax (fp32): an HBM-bound kernel, one read and one write per element.
+    row_softmax = {}
+    if not args.no_sweep and rank == 0:
+        peaks_rs, kind_rs = measured_peaks()
+        for (M, Ncols, seed), label in ((inputs.SOFTMAX_HBM_SHAPE, "hbm"), (inputs.SOFTMAX_PAGE_SHAPE, "page")):
+            xs = inputs.uniform_matrix(M, Ncols, seed).to(dev)
+            ys = torch.empty_like(xs)
+            times = []
+            for i in range(13):
+                if label == "page":
+                    flush.zero_()
+                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a.record(stream)
+                eca.row_softmax(xs, ys, stream=stream)
+                b.record(stream)
+                times.append((a, b))
+            torch.cuda.synchronize(dev)
+            ms = sorted(a.elapsed_time(b) for a, b in times[3:])
+            med = ms[len(ms) // 2]
+            gbs = 8.0 * M * Ncols / (med * 1e-3) / 1e9
+            row_softmax[label] = {"M": M, "N": Ncols, "us": round(med * 1e3, 2), "GB_s": round(gbs, 1),
+                                  "frac_of_hbm": round(gbs / float(peaks_rs["hbm_gbs"]), 3)}
+            del xs, ys
+        row_softmax["hbm_peak_gbs"] = float(peaks_rs["hbm_gbs"])
+        row_softmax["peak_kind"] = kind_rs
+
     fp16_peak = None
     if not args.no_peak and rank == 0:
         a = torch.randn(8192, 8192, device=dev, dtype=torch.float16)
@@ -436,6 +462,7 @@ def bench_ours(args, w):
         "sweep": sweep,
         "splitkv": splitkv,
         "gqa": gqa,
+        "row_softmax": row_softmax,
         "fp16_matmul_peak_tflops": fp16_peak,
         "frac_of_measured_fp16_matmul": (achieved / fp16_peak) if fp16_peak else None,
         "frac_of_datasheet_dense_fp16": achieved / 2250.0,

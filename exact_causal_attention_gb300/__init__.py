@@ -13,7 +13,7 @@ import os
 import threading
 
 __all__ = ["attn_fwd", "attn_fwd_into", "attn_fwd_gqa", "attn_fwd_splitkv", "splitkv_workspace_bytes",
-           "splitkv_default_splits", "load_library", "device_status", "watchdog_selftest", "AttnError",
+           "splitkv_default_splits", "row_softmax", "load_library", "device_status", "watchdog_selftest", "AttnError",
            "STATUS"]
 
 _LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "_build", "libeca_attn.so")
@@ -44,6 +44,7 @@ SIGNATURES = {
     "attn_fwd_splitkv_noalloc": (_I, [_VP, _VP, _VP, _VP, _VP, _I, _I, _I, _I, _I, _F, _I, _VP]),
     "attn_splitkv_workspace_bytes": (_SZ, [_I, _I, _I, _I, _I]),
     "attn_splitkv_default_splits": (_I, [_I, _I, _I, _I]),
+    "attn_row_softmax_f32": (_I, [_VP, _VP, ctypes.c_longlong, _I, _VP]),
     "attn_device_status": (_I, [_VP]),
     "attn_watchdog_selftest": (_I, [_U, _VP]),
     "attn_status_string": (ctypes.c_char_p, [_I]),
@@ -223,6 +224,24 @@ def attn_fwd_splitkv(q, k, v, o=None, lse=None, kv_splits: int | None = None, wo
     if rc != 0:
         raise AttnError(rc, "attn_fwd_splitkv")
     return o, lse
+
+
+def row_softmax(x, out=None, stream=None):
+    """Row softmax of a contiguous 2-D float32 CUDA tensor (online (m, d) kernel)."""
+    import torch
+
+    if not isinstance(x, torch.Tensor) or not x.is_cuda or x.dim() != 2 or x.dtype != torch.float32:
+        raise TypeError("x must be a 2-D float32 CUDA tensor")
+    if not x.is_contiguous():
+        raise ValueError("x must be contiguous")
+    if out is None:
+        out = torch.empty_like(x)
+    M, N = x.shape
+    with torch.cuda.device(x.device):
+        rc = load_library().attn_row_softmax_f32(x.data_ptr(), out.data_ptr(), M, N, _stream_handle(stream))
+    if rc != 0:
+        raise AttnError(rc, "attn_row_softmax_f32")
+    return out
 
 
 def device_status(stream=None) -> int:

@@ -10,6 +10,7 @@
 
 #include "attn.h"
 #include "attn_fwd_kernel.cuh"
+#include "row_softmax.cuh"
 #include "splitkv_combine.cuh"
 
 // Scratch of attn_fwd_splitkv_noalloc: one fixed array per device that loads this
@@ -377,6 +378,54 @@ int attn_splitkv_default_splits(int B, int H, int N, int D) {
   if (s > n_tiles) s = n_tiles;
   if (s > kMaxSplits) s = kMaxSplits;
   return s < 1 ? 1 : static_cast<int>(s);
+}
+
+int attn_row_softmax_f32(const float* x, float* y, long long M, int N, attn_stream_t stream) {
+  if (!x || !y || M < 1 || N < 1) return ATTN_ERR_INVALID_ARG;
+  if (!aligned(x, 4) || !aligned(y, 4)) return ATTN_ERR_UNALIGNED;
+  const uint64_t bytes = static_cast<uint64_t>(M) * static_cast<uint64_t>(N) * 4;
+  if (bytes >= (1ull << 62) || M > 0x7fffffffLL) return ATTN_ERR_INVALID_ARG;
+  if (x != y && overlaps(x, bytes, y, bytes)) return ATTN_ERR_INVALID_ARG;  // in place is fine, partial overlap not
+  {
+    std::lock_guard<std::mutex> lock(g_mutex);
+    DeviceState* st = nullptr;
+    const int r = device_state(&st);
+    if (r != ATTN_OK) return r;
+  }
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const bool vec = (N % 4) == 0 && aligned(x, 16) && aligned(y, 16);
+  const unsigned warp_blocks = static_cast<unsigned>((M + 7) / 8);  // 8 rows (warps) per block
+  const unsigned row_blocks = static_cast<unsigned>(M);
+#define ECA_WARP_ROWS(ITEMS)                                                                          \
+  (vec ? eca::row_softmax_cached<32, ITEMS, true><<<warp_blocks, 256, 0, s>>>(x, y, M, N)            \
+       : eca::row_softmax_cached<32, ITEMS, false><<<warp_blocks, 256, 0, s>>>(x, y, M, N))
+#define ECA_BLOCK_ROWS(ITEMS)                                                                         \
+  (vec ? eca::row_softmax_cached<256, ITEMS, true><<<row_blocks, 256, 0, s>>>(x, y, M, N)            \
+       : eca::row_softmax_cached<256, ITEMS, false><<<row_blocks, 256, 0, s>>>(x, y, M, N))
+  if (N <= 32 * 4) {
+    ECA_WARP_ROWS(4);
+  } else if (N <= 32 * 8) {
+    ECA_WARP_ROWS(8);
+  } else if (N <= 32 * 16) {
+    ECA_WARP_ROWS(16);
+  } else if (N <= 32 * 32) {
+    ECA_WARP_ROWS(32);
+  } else if (N <= 32 * 64) {
+    ECA_WARP_ROWS(64);
+  } else if (N <= 256 * 16) {
+    ECA_BLOCK_ROWS(16);
+  } else if (N <= 256 * 32) {
+    ECA_BLOCK_ROWS(32);
+  } else if (N <= 256 * 64) {
+    ECA_BLOCK_ROWS(64);
+  } else if (vec) {
+    eca::row_softmax_stream<true><<<row_blocks, 256, 0, s>>>(x, y, M, N);
+  } else {
+    eca::row_softmax_stream<false><<<row_blocks, 256, 0, s>>>(x, y, M, N);
+  }
+#undef ECA_WARP_ROWS
+#undef ECA_BLOCK_ROWS
+  return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_LAUNCH;
 }
 
 int attn_device_status(attn_stream_t stream) {

@@ -99,3 +99,16 @@ def bits(t: torch.Tensor):
 
 def sha256(t: torch.Tensor) -> str:
     return hashlib.sha256(bits(t).tobytes()).hexdigest()
+
+
+def uniform_matrix(M: int, N: int, seed: int, lo: float = -10.0, hi: float = 10.0):
+    """A CPU float32 [M, N] matrix of i.i.d. U[lo, hi) draws (float64 draw, one rounding), the
+    input recipe of the row-softmax page's section 6.1 (U[-10, 10), seeded)."""
+    g = torch.Generator(device="cpu").manual_seed(int(seed))
+    x = torch.rand(M, N, generator=g, dtype=torch.float64)
+    return (x * (hi - lo) + lo).to(torch.float32)
+
+
+# The row-softmax workload of that section (M=1024, N=4096, seed 42) and a larger one for HBM.
+SOFTMAX_PAGE_SHAPE = (1024, 4096, 42)
+SOFTMAX_HBM_SHAPE = (65536, 4096, 43)

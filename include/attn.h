@@ -153,6 +153,23 @@ size_t attn_splitkv_workspace_bytes(int B, int H, int N, int D, int kv_splits);
 int attn_splitkv_default_splits(int B, int H, int N, int D);
 
 /*
+ * attn_row_softmax_f32 -- row softmax of an fp32 matrix with the online (m, d)
+ * recurrence of the page "Softmax kernels V1-V9" (lpnh.cn/news/2830604,
+ * sections 4.4-4.9): y_ij = exp(x_ij - m_i) / sum_j exp(x_ij - m_i), m_i the row
+ * max, in one pass over memory when a row fits on chip (N <= 16384), two passes
+ * over the row otherwise.
+ *   x : device, [M, N] fp32, rows contiguous, 4-byte aligned (16-byte aligned
+ *       with N a multiple of 4 selects 16-byte accesses), read only.
+ *   y : device, [M, N] fp32, written in full; y == x (in place) is allowed, any
+ *       other overlap is rejected.
+ *   M : 1 .. 2^31 - 1 rows.   N : >= 1.
+ * Entries of -inf contribute nothing; a row of -inf only is written as zeros.
+ * exp is the hardware approximation (__expf): elements stay within 1e-6 of the
+ * exact result.  Returns ATTN_OK or a negative attn_status.
+ */
+int attn_row_softmax_f32(const float* x, float* y, long long M, int N, attn_stream_t stream);
+
+/*
  * attn_device_status -- synchronises `stream`, then reads and clears the
  * library's device status word for the current device.  Returns ATTN_OK, or
  * ATTN_ERR_TIMEOUT if a kernel enqueued since the last call gave up on a

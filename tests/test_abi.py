@@ -140,3 +140,12 @@ def test_gqa_argument_errors_without_gpu(lib, fn):
     assert f(*args(8, 0)) == -1
     assert f(*args(8, 16)) == -1
     assert f(*args(8, 2, 96)) == -3
+
+
+def test_row_softmax_argument_errors_without_gpu(lib):
+    f = lib.attn_row_softmax_f32
+    assert f(None, A, 4, 8, None) == -1
+    assert f(A, A + SZ, 0, 8, None) == -1
+    assert f(A, A + SZ, 4, 0, None) == -1
+    assert f(A + 1, A + SZ, 4, 8, None) == -2
+    assert f(A, A + 16, 4, 8, None) == -1  # y overlaps x without being x
