@@ -146,3 +146,43 @@ def softmax(x, mode: str = "two_pass", tile: int = 64, nthreads: int = 0) -> np.
     if rc != 0:
         raise ValueError("oracle_softmax rejected its arguments")
     return y
+
+
+# ------------------------------------------------------------- paged KV cache
+
+def gather_paged(cache, block_table, lengths, page_size: int):
+    """Logical K and V of each request from a paged cache (page "CUDA KV Cache：分页存储
+    与长上下文 Decode 极致优化", section 2): cache is [P, 2, T, Hkv, D]; token t of
+    request b sits on physical page block_table[b, t // T] at offset t % T.
+    Returns a list of (k, v), each [Hkv, lengths[b], D] float64."""
+    cache = np.asarray(cache)
+    out = []
+    for b, L in enumerate(np.asarray(lengths).tolist()):
+        t = np.arange(L)
+        pages = np.asarray(block_table)[b, t // page_size]
+        offs = t % page_size
+        k = cache[pages, 0, offs].astype(np.float64)  # [L, Hkv, D]
+        v = cache[pages, 1, offs].astype(np.float64)
+        out.append((np.ascontiguousarray(k.transpose(1, 0, 2)), np.ascontiguousarray(v.transpose(1, 0, 2))))
+    return out
+
+
+def decode_paged(q, cache, block_table, lengths, page_size: int, scale: float, nthreads: int = 0):
+    """One decode query per request against its whole paged context: O [B, Hq, D] and
+    lse [B, Hq] in float64.  The query attends every one of its lengths[b] tokens, which
+    is the last row of the causal attention over the logical sequence; a request with no
+    token gets O = 0 and lse = -inf."""
+    q = np.asarray(q, dtype=np.float64)
+    B, Hq, D = q.shape
+    o = np.zeros((B, Hq, D))
+    lse = np.full((B, Hq), -np.inf)
+    for b, (k, v) in enumerate(gather_paged(cache, block_table, lengths, page_size)):
+        L = k.shape[1]
+        if L == 0:
+            continue
+        qq = np.zeros((1, Hq, L, D))
+        qq[0, :, L - 1] = q[b]
+        ob, lb = attention_rows(qq, k[None], v[None], True, scale, [(h, L - 1) for h in range(Hq)],
+                                nthreads=nthreads)
+        o[b], lse[b] = ob, lb
+    return o, lse
