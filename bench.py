@@ -410,6 +410,59 @@ def bench_ours(args, w):
         row_softmax["hbm_peak_gbs"] = float(peaks_rs["hbm_gbs"])
         row_softmax["peak_kind"] = kind_rs
 
+    # Paged GQA decode over the decode page's geometry (B=8, Hq=32, Hkv=8, D=128, page size 16):
+    # HBM-bound, it must stream 2 B L Hkv D s bytes of K/V per step.
+    paged = {}
+    if not args.no_sweep and rank == 0:
+        peaks_pd, _ = measured_peaks()
+        pw = inputs.PAGED_BENCH
+        gen = torch.Generator(device=dev).manual_seed(pw.seed)
+        for ctx in inputs.PAGED_CONTEXTS:
+            pages = (ctx + pw.page_size - 1) // pw.page_size
+            P = pw.B * pages
+            cache = torch.randn(P, 2, pw.page_size, pw.Hkv, pw.D, generator=gen, device=dev, dtype=torch.float16)
+            table = torch.randperm(P, generator=gen, device=dev).to(torch.int32).view(pw.B, pages).contiguous()
+            lens = torch.full((pw.B,), ctx, dtype=torch.int32, device=dev)
+            qd = torch.randn(pw.B, pw.Hq, pw.D, generator=gen, device=dev, dtype=torch.float16)
+            outd = torch.empty_like(qd)
+            lsed = torch.empty((pw.B, pw.Hq), dtype=torch.float32, device=dev)
+            splits = eca.load_library().attn_decode_default_splits(pw.B, pw.Hq, pw.Hkv, pw.page_size, pages)
+            need = int(eca.load_library().attn_decode_workspace_bytes(pw.B, pw.Hq, pw.D, splits))
+            ws = torch.empty(need + 256, dtype=torch.uint8, device=dev) if need else None
+            if ws is not None:
+                off = (-ws.data_ptr()) % 256
+                ws = ws[off:off + need]
+            times = []
+            for i in range(13):
+                flush.zero_()
+                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a.record(stream)
+                eca.decode_paged(qd, cache, table, lens, kv_splits=splits, out=outd, lse=lsed, workspace=ws,
+                                 stream=stream)
+                b.record(stream)
+                times.append((a, b))
+            torch.cuda.synchronize(dev)
+            ms = sorted(a.elapsed_time(b) for a, b in times[3:])
+            med = ms[len(ms) // 2]
+            kv = 2 * pw.B * ctx * pw.Hkv * pw.D * 2
+            paged[str(ctx)] = {"us": round(med * 1e3, 2), "GB_s": round(kv / (med * 1e-3) / 1e9, 1),
+                               "frac_of_hbm": round(kv / (med * 1e-3) / 1e9 / float(peaks_pd["hbm_gbs"]), 3),
+                               "kv_splits": splits}
+            if ctx == inputs.PAGED_CONTEXTS[-1]:
+                newkv = torch.randn(pw.B, 2, pw.Hkv, pw.D, generator=gen, device=dev, dtype=torch.float16)
+                at = []
+                for i in range(13):
+                    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                    a.record(stream)
+                    eca.paged_append(newkv, cache, table, lens, stream=stream)
+                    b.record(stream)
+                    at.append((a, b))
+                torch.cuda.synchronize(dev)
+                ams = sorted(a.elapsed_time(b) for a, b in at[3:])
+                paged["append_us"] = round(ams[len(ams) // 2] * 1e3, 2)
+            del cache, table, lens, qd, outd, lsed, ws
+        paged["workload"] = pw.name.replace("ctx32768", "ctx1024..32768")
+
     fp16_peak = None
     if not args.no_peak and rank == 0:
         a = torch.randn(8192, 8192, device=dev, dtype=torch.float16)
@@ -463,6 +516,7 @@ def bench_ours(args, w):
         "splitkv": splitkv,
         "gqa": gqa,
         "row_softmax": row_softmax,
+        "paged_decode": paged,
         "fp16_matmul_peak_tflops": fp16_peak,
         "frac_of_measured_fp16_matmul": (achieved / fp16_peak) if fp16_peak else None,
         "frac_of_datasheet_dense_fp16": achieved / 2250.0,

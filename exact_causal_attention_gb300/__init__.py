@@ -13,7 +13,7 @@ import os
 import threading
 
 __all__ = ["attn_fwd", "attn_fwd_into", "attn_fwd_gqa", "attn_fwd_splitkv", "splitkv_workspace_bytes",
-           "splitkv_default_splits", "row_softmax", "load_library", "device_status", "watchdog_selftest", "AttnError",
+           "splitkv_default_splits", "row_softmax", "decode_paged", "paged_append", "load_library", "device_status", "watchdog_selftest", "AttnError",
            "STATUS"]
 
 _LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "_build", "libeca_attn.so")
@@ -30,6 +30,7 @@ STATUS = {
     -6: "ATTN_ERR_TIMEOUT",
     -7: "ATTN_ERR_CUDA",
     -8: "ATTN_ERR_SCRATCH_LIMIT",
+    -9: "ATTN_ERR_BAD_INDEX",
 }
 
 # Every exported symbol of include/attn.h with its ctypes signature.
@@ -45,6 +46,12 @@ SIGNATURES = {
     "attn_splitkv_workspace_bytes": (_SZ, [_I, _I, _I, _I, _I]),
     "attn_splitkv_default_splits": (_I, [_I, _I, _I, _I]),
     "attn_row_softmax_f32": (_I, [_VP, _VP, ctypes.c_longlong, _I, _VP]),
+    "attn_decode_paged": (_I, [_VP, _VP, _VP, _VP, _VP, _VP, _I, _I, _I, _I, _I, _I, _I, _F, _I, _VP, _SZ, _VP]),
+    "attn_decode_paged_bf16": (_I, [_VP, _VP, _VP, _VP, _VP, _VP, _I, _I, _I, _I, _I, _I, _I, _F, _I, _VP, _SZ,
+                                    _VP]),
+    "attn_decode_workspace_bytes": (_SZ, [_I, _I, _I, _I]),
+    "attn_decode_default_splits": (_I, [_I, _I, _I, _I, _I]),
+    "attn_paged_append": (_I, [_VP, _VP, _VP, _VP, _I, _I, _I, _I, _I, _I, _VP]),
     "attn_device_status": (_I, [_VP]),
     "attn_watchdog_selftest": (_I, [_U, _VP]),
     "attn_status_string": (ctypes.c_char_p, [_I]),
@@ -242,6 +249,63 @@ def row_softmax(x, out=None, stream=None):
     if rc != 0:
         raise AttnError(rc, "attn_row_softmax_f32")
     return out
+
+
+def decode_paged(q, cache, block_table, lengths, scale: float | None = None, kv_splits: int | None = None,
+                 out=None, lse=None, workspace=None, stream=None):
+    """One decode step over a paged cache: q [B,Hq,D], cache [P,2,T,Hkv,D] (16-bit),
+    block_table [B,max_pages] int32, lengths [B] int32 (all CUDA).  Returns (out, lse)."""
+    import torch
+
+    B, Hq, D = q.shape
+    P, two, T, Hkv, D2 = cache.shape
+    if two != 2 or D2 != D or q.dtype != cache.dtype or q.dtype not in (torch.float16, torch.bfloat16):
+        raise ValueError("cache must be [P, 2, T, Hkv, D] in q's dtype")
+    if block_table.dtype != torch.int32 or lengths.dtype != torch.int32 or block_table.shape[0] != B:
+        raise ValueError("block_table [B, max_pages] and lengths [B] must be int32")
+    for t in (q, cache, block_table, lengths):
+        if not t.is_cuda or not t.is_contiguous():
+            raise ValueError("all tensors must be contiguous CUDA tensors")
+    max_pages = block_table.shape[1]
+    lib = load_library()
+    with torch.cuda.device(q.device):
+        if kv_splits is None:
+            kv_splits = lib.attn_decode_default_splits(B, Hq, Hkv, T, max_pages)
+            if kv_splits < 0:
+                raise AttnError(kv_splits, "attn_decode_default_splits")
+        if out is None:
+            out = torch.empty_like(q)
+        if lse is None:
+            lse = torch.empty((B, Hq), dtype=torch.float32, device=q.device)
+        need = int(lib.attn_decode_workspace_bytes(B, Hq, D, kv_splits))
+        if workspace is None and need > 0:
+            raw = torch.empty(need + 256, dtype=torch.uint8, device=q.device)
+            off = (-raw.data_ptr()) % 256
+            workspace = raw[off:off + need]
+        if scale is None:
+            scale = 1.0 / math.sqrt(D)
+        fn = lib.attn_decode_paged_bf16 if q.dtype == torch.bfloat16 else lib.attn_decode_paged
+        rc = fn(q.data_ptr(), cache.data_ptr(), block_table.data_ptr(), lengths.data_ptr(), out.data_ptr(),
+                lse.data_ptr() if lse is not None else None, B, Hq, Hkv, D, T, max_pages, P, float(scale),
+                int(kv_splits), workspace.data_ptr() if workspace is not None else None,
+                (workspace.numel() if workspace is not None else 0), _stream_handle(stream))
+    if rc != 0:
+        raise AttnError(rc, "attn_decode_paged")
+    return out, lse
+
+
+def paged_append(new_kv, cache, block_table, lengths, stream=None) -> None:
+    """Write new_kv [B, 2, Hkv, D] at position lengths[b] - 1 of every request's pages."""
+    import torch
+
+    B, two, Hkv, D = new_kv.shape
+    P, _, T, _, _ = cache.shape
+    with torch.cuda.device(cache.device):
+        rc = load_library().attn_paged_append(new_kv.data_ptr(), cache.data_ptr(), block_table.data_ptr(),
+                                              lengths.data_ptr(), B, Hkv, D, T, block_table.shape[1], P,
+                                              _stream_handle(stream))
+    if rc != 0:
+        raise AttnError(rc, "attn_paged_append")
 
 
 def device_status(stream=None) -> int:

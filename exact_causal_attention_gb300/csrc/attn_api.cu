@@ -10,6 +10,7 @@
 
 #include "attn.h"
 #include "attn_fwd_kernel.cuh"
+#include "paged_decode.cuh"
 #include "row_softmax.cuh"
 #include "splitkv_combine.cuh"
 
@@ -40,6 +41,7 @@ struct DeviceState {
   int* status = nullptr;    // address of g_device_status on this device
   void* scratch = nullptr;  // address of g_splitkv_scratch on this device, set by its first use
   unsigned configured = 0;  // bitmask of kernel instantiations with smem attribute set
+  unsigned configured_decode = 0;
 };
 
 std::mutex g_mutex;
@@ -290,6 +292,156 @@ __global__ void watchdog_selftest_kernel(int* status, unsigned long long limit_n
   }
 }
 
+// ------------------------------------------------------------- paged decode
+
+struct DecodeShape {
+  int hc;          // query heads per CTA
+  int head_chunks;
+  int seg_pages;
+  int splits;
+};
+
+DecodeShape decode_shape(int Hq, int Hkv, int page_size, int max_pages, int kv_splits) {
+  const int group = Hq / Hkv;
+  int hc = 8;
+  while (group % hc != 0) hc /= 2;
+  const int ppt = eca::kDecTile / page_size;
+  int seg = (max_pages + kv_splits - 1) / kv_splits;
+  seg = (seg + ppt - 1) / ppt * ppt;  // whole tiles per segment
+  return DecodeShape{hc, group / hc, seg, (max_pages + seg - 1) / seg};
+}
+
+// Paged cache [P, 2, T, Hkv, D] as a rank-3 map (D, Hkv, P*2*T): one box is the
+// T x 64 block of one head on one page, 128-byte swizzle.
+int encode_cache_map(EncodeTiledFn encode, CUtensorMap* map, const void* cache, bool bf16, int D, int Hkv, int T,
+                     int P) {
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(Hkv),
+                              static_cast<cuuint64_t>(P) * 2 * static_cast<cuuint64_t>(T)};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(D) * 2, static_cast<cuuint64_t>(Hkv) * D * 2};
+  const cuuint32_t box[3] = {64, 1, static_cast<cuuint32_t>(T)};
+  const cuuint32_t elem_strides[3] = {1, 1, 1};
+  const CUresult r =
+      encode(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3,
+             const_cast<void*>(cache), dims, strides, box, elem_strides, CU_TENSOR_MAP_INTERLEAVE_NONE,
+             CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? ATTN_OK : ATTN_ERR_INVALID_ARG;
+}
+
+int check_paged_args(const void* cache, const int* block_table, const int* lengths, int B, int Hkv, int D,
+                     int page_size, int max_pages, int num_pages) {
+  if (!cache || !block_table || !lengths) return ATTN_ERR_INVALID_ARG;
+  if (B < 1 || Hkv < 1 || max_pages < 1 || num_pages < 1) return ATTN_ERR_INVALID_ARG;
+  if (D != 64 && D != 128) return ATTN_ERR_UNSUPPORTED_D;
+  if (page_size != 8 && page_size != 16 && page_size != 32 && page_size != 64) return ATTN_ERR_INVALID_ARG;
+  if (!aligned(cache, 16) || !aligned(block_table, 4) || !aligned(lengths, 4)) return ATTN_ERR_UNALIGNED;
+  const uint64_t rows = static_cast<uint64_t>(num_pages) * 2 * static_cast<uint64_t>(page_size);
+  if (rows > 0xffffffffull || static_cast<uint64_t>(max_pages) * page_size > 0x7fffffffull) return ATTN_ERR_INVALID_ARG;
+  if (static_cast<uint64_t>(B) * static_cast<uint64_t>(max_pages) > 0x7fffffffull) return ATTN_ERR_INVALID_ARG;
+  return ATTN_OK;
+}
+
+uint64_t decode_ws_bytes(uint64_t B, uint64_t Hq, uint64_t D, uint64_t splits, uint64_t* lse_off) {
+  const uint64_t o = splits * B * Hq * D * 4;
+  if (lse_off) *lse_off = align256(o);
+  return align256(o) + align256(splits * B * Hq * 4);
+}
+
+template <int D, bool BF16>
+int launch_decode(const CUtensorMap& tm, eca::DecodeParams& p, const DecodeShape& sh, DeviceState* st,
+                  cudaStream_t stream) {
+  using L = eca::DecodeSmem<D>;
+  const long long ctas = static_cast<long long>(p.B) * p.Hkv * sh.head_chunks * sh.splits;
+  if (ctas > 0x7fffffffLL) return ATTN_ERR_INVALID_ARG;
+  const unsigned grid = static_cast<unsigned>(ctas);
+  auto run = [&](auto kernel, unsigned bit) -> int {
+    if (!(st->configured_decode & bit)) {
+      if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kDynamicBytes) !=
+          cudaSuccess) {
+        return ATTN_ERR_CUDA;
+      }
+      st->configured_decode |= bit;
+    }
+    kernel<<<grid, eca::kDecThreads, L::kDynamicBytes, stream>>>(tm, p);
+    return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_LAUNCH;
+  };
+  const unsigned base = (D == 128 ? 0u : 8u) + (BF16 ? 4u : 0u);
+  int rc;
+  switch (sh.hc) {
+    case 8: rc = run(eca::paged_decode_kernel<D, BF16, 8>, 1u << (base + 3)); break;
+    case 4: rc = run(eca::paged_decode_kernel<D, BF16, 4>, 1u << (base + 2)); break;
+    case 2: rc = run(eca::paged_decode_kernel<D, BF16, 2>, 1u << (base + 1)); break;
+    default: rc = run(eca::paged_decode_kernel<D, BF16, 1>, 1u << base); break;
+  }
+  if (rc != ATTN_OK || p.part_o == nullptr) return rc;
+  const long long rows = static_cast<long long>(p.B) * p.Hq;
+  const long long want = (rows + 7) / 8, cap = static_cast<long long>(st->sm_count) * 8;
+  eca::paged_decode_combine<D, BF16><<<static_cast<unsigned>(want < cap ? want : cap), 256, 0, stream>>>(p);
+  return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_LAUNCH;
+}
+
+int decode_impl(bool bf16, const void* q, const void* cache, const int* block_table, const int* lengths, void* out,
+                float* lse, int B, int Hq, int Hkv, int D, int page_size, int max_pages, int num_pages, float scale,
+                int kv_splits, void* workspace, size_t workspace_bytes, attn_stream_t stream) {
+  int rc = check_paged_args(cache, block_table, lengths, B, Hkv, D, page_size, max_pages, num_pages);
+  if (rc != ATTN_OK) return rc;
+  if (!q || !out || Hq < 1 || Hq % Hkv != 0) return ATTN_ERR_INVALID_ARG;
+  if (!std::isfinite(scale) || !(scale > 0.f)) return ATTN_ERR_INVALID_ARG;
+  if (kv_splits < 1 || kv_splits > kMaxSplits) return ATTN_ERR_INVALID_ARG;
+  if (!aligned(q, 16) || !aligned(out, 16) || (lse && !aligned(lse, 4))) return ATTN_ERR_UNALIGNED;
+  const uint64_t qbytes = static_cast<uint64_t>(B) * Hq * D * 2;
+  if (overlaps(out, qbytes, q, qbytes)) return ATTN_ERR_INVALID_ARG;
+  const DecodeShape sh = decode_shape(Hq, Hkv, page_size, max_pages, kv_splits);
+  float* part_o = nullptr;
+  float* part_lse = nullptr;
+  if (sh.splits > 1) {
+    if (workspace == nullptr) return ATTN_ERR_INVALID_ARG;
+    if (!aligned(workspace, 256)) return ATTN_ERR_UNALIGNED;
+    uint64_t lse_off = 0;
+    const uint64_t need = decode_ws_bytes(B, Hq, D, sh.splits, &lse_off);
+    if (static_cast<uint64_t>(workspace_bytes) < need) return ATTN_ERR_INVALID_ARG;
+    if (overlaps(workspace, need, out, qbytes) || overlaps(workspace, need, q, qbytes)) return ATTN_ERR_INVALID_ARG;
+    part_o = static_cast<float*>(workspace);
+    part_lse = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + lse_off);
+  }
+  std::lock_guard<std::mutex> lock(g_mutex);
+  DeviceState* st = nullptr;
+  rc = device_state(&st);
+  if (rc != ATTN_OK) return rc;
+  EncodeTiledFn encode = nullptr;
+  rc = get_encode_fn(&encode);
+  if (rc != ATTN_OK) return rc;
+  CUtensorMap tm;
+  rc = encode_cache_map(encode, &tm, cache, bf16, D, Hkv, page_size, num_pages);
+  if (rc != ATTN_OK) return rc;
+  eca::DecodeParams p;
+  p.q = q;
+  p.block_table = block_table;
+  p.lengths = lengths;
+  p.out = out;
+  p.lse = lse;
+  p.part_o = part_o;
+  p.part_lse = part_lse;
+  p.status = st->status;
+  p.B = B;
+  p.Hq = Hq;
+  p.Hkv = Hkv;
+  p.page_size = page_size;
+  p.max_pages = max_pages;
+  p.num_pages = num_pages;
+  p.head_chunks = sh.head_chunks;
+  p.splits = sh.splits;
+  p.seg_pages = sh.seg_pages;
+  p.scale_log2e = scale * 1.4426950408889634f;
+  p.wait_limit_ns = kWaitLimitNs;
+  p.timeout_code = ATTN_ERR_TIMEOUT;
+  p.bad_index_code = ATTN_ERR_BAD_INDEX;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (D == 128) {
+    return bf16 ? launch_decode<128, true>(tm, p, sh, st, s) : launch_decode<128, false>(tm, p, sh, st, s);
+  }
+  return bf16 ? launch_decode<64, true>(tm, p, sh, st, s) : launch_decode<64, false>(tm, p, sh, st, s);
+}
+
 }  // namespace
 
 extern "C" {
@@ -380,6 +532,75 @@ int attn_splitkv_default_splits(int B, int H, int N, int D) {
   return s < 1 ? 1 : static_cast<int>(s);
 }
 
+int attn_decode_paged(const void* q, const void* cache, const int* block_table, const int* lengths, void* out,
+                      float* lse, int B, int Hq, int Hkv, int D, int page_size, int max_pages, int num_pages,
+                      float scale, int kv_splits, void* workspace, size_t workspace_bytes, attn_stream_t stream) {
+  return decode_impl(false, q, cache, block_table, lengths, out, lse, B, Hq, Hkv, D, page_size, max_pages, num_pages,
+                     scale, kv_splits, workspace, workspace_bytes, stream);
+}
+
+int attn_decode_paged_bf16(const void* q, const void* cache, const int* block_table, const int* lengths, void* out,
+                           float* lse, int B, int Hq, int Hkv, int D, int page_size, int max_pages, int num_pages,
+                           float scale, int kv_splits, void* workspace, size_t workspace_bytes,
+                           attn_stream_t stream) {
+  return decode_impl(true, q, cache, block_table, lengths, out, lse, B, Hq, Hkv, D, page_size, max_pages, num_pages,
+                     scale, kv_splits, workspace, workspace_bytes, stream);
+}
+
+size_t attn_decode_workspace_bytes(int B, int Hq, int D, int kv_splits) {
+  if (B < 1 || Hq < 1 || (D != 64 && D != 128) || kv_splits < 1 || kv_splits > kMaxSplits) return 0;
+  if (kv_splits == 1) return 0;
+  return static_cast<size_t>(decode_ws_bytes(B, Hq, D, kv_splits, nullptr));
+}
+
+int attn_decode_default_splits(int B, int Hq, int Hkv, int page_size, int max_pages) {
+  if (B < 1 || Hq < 1 || Hkv < 1 || Hq % Hkv != 0 || max_pages < 1) return ATTN_ERR_INVALID_ARG;
+  if (page_size != 8 && page_size != 16 && page_size != 32 && page_size != 64) return ATTN_ERR_INVALID_ARG;
+  std::lock_guard<std::mutex> lock(g_mutex);
+  DeviceState* st = nullptr;
+  const int r = device_state(&st);
+  if (r != ATTN_OK) return r;
+  const DecodeShape one = decode_shape(Hq, Hkv, page_size, max_pages, 1);
+  const long long ctas = static_cast<long long>(B) * Hkv * one.head_chunks;
+  const long long tiles = (static_cast<long long>(max_pages) * page_size + eca::kDecTile - 1) / eca::kDecTile;
+  long long s = (4LL * st->sm_count + ctas - 1) / ctas;  // about four CTAs per SM
+  if (s > tiles) s = tiles;
+  if (s > kMaxSplits) s = kMaxSplits;
+  return s < 1 ? 1 : static_cast<int>(s);
+}
+
+int attn_paged_append(const void* new_kv, void* cache, const int* block_table, const int* lengths, int B, int Hkv,
+                      int D, int page_size, int max_pages, int num_pages, attn_stream_t stream) {
+  int rc = check_paged_args(cache, block_table, lengths, B, Hkv, D, page_size, max_pages, num_pages);
+  if (rc != ATTN_OK) return rc;
+  if (!new_kv) return ATTN_ERR_INVALID_ARG;
+  if (!aligned(new_kv, 16)) return ATTN_ERR_UNALIGNED;
+  DeviceState* st = nullptr;
+  {
+    std::lock_guard<std::mutex> lock(g_mutex);
+    rc = device_state(&st);
+    if (rc != ATTN_OK) return rc;
+  }
+  eca::AppendParams p;
+  p.new_kv = new_kv;
+  p.cache = cache;
+  p.block_table = block_table;
+  p.lengths = lengths;
+  p.status = st->status;
+  p.B = B;
+  p.Hkv = Hkv;
+  p.D = D;
+  p.page_size = page_size;
+  p.max_pages = max_pages;
+  p.num_pages = num_pages;
+  p.bad_index_code = ATTN_ERR_BAD_INDEX;
+  const long long rows = static_cast<long long>(B) * 2 * Hkv;
+  const long long want = (rows + 7) / 8, cap = static_cast<long long>(st->sm_count) * 8;
+  eca::paged_append_kernel<<<static_cast<unsigned>(want < cap ? want : cap), 256, 0,
+                             reinterpret_cast<cudaStream_t>(stream)>>>(p);
+  return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_LAUNCH;
+}
+
 int attn_row_softmax_f32(const float* x, float* y, long long M, int N, attn_stream_t stream) {
   if (!x || !y || M < 1 || N < 1) return ATTN_ERR_INVALID_ARG;
   if (!aligned(x, 4) || !aligned(y, 4)) return ATTN_ERR_UNALIGNED;
@@ -463,6 +684,7 @@ const char* attn_status_string(int status) {
     case ATTN_ERR_TIMEOUT: return "a bounded device wait timed out";
     case ATTN_ERR_CUDA: return "CUDA runtime/driver call failed";
     case ATTN_ERR_SCRATCH_LIMIT: return "the split needs more than the library's fixed 64 MiB scratch";
+    case ATTN_ERR_BAD_INDEX: return "a block-table entry or a length was out of range (those tokens were skipped)";
     default: return "unknown status";
   }
 }

@@ -33,7 +33,6 @@ __global__ void __launch_bounds__(256) splitkv_combine_kernel(const CombineParam
   const long long warps = static_cast<long long>(gridDim.x) * (blockDim.x / 32);
   for (long long r = static_cast<long long>(blockIdx.x) * (blockDim.x / 32) + threadIdx.x / 32; r < rows;
        r += warps) {
-    const int bh = static_cast<int>(r / p.N);
     const int row = static_cast<int>(r % p.N);
     // Segments holding at least one key this row's 128-row query tile looks at.
     const int need = p.causal ? row / 128 + 1 : p.n_tiles;

@@ -112,3 +112,50 @@ def uniform_matrix(M: int, N: int, seed: int, lo: float = -10.0, hi: float = 10.
 # The row-softmax workload of that section (M=1024, N=4096, seed 42) and a larger one for HBM.
 SOFTMAX_PAGE_SHAPE = (1024, 4096, 42)
 SOFTMAX_HBM_SHAPE = (65536, 4096, 43)
+
+
+@dataclasses.dataclass(frozen=True)
+class PagedWorkload:
+    """One decode step over a paged K/V cache (the decode page's section 8 shapes)."""
+    name: str
+    B: int
+    Hq: int
+    Hkv: int
+    D: int
+    page_size: int
+    context: int      # tokens per request (every request the same length here)
+    dtype: str
+    seed: int
+
+    @property
+    def kv_bytes(self) -> int:
+        """K and V bytes the decode step must read: 2 B L Hkv D s."""
+        return 2 * self.B * self.context * self.Hkv * self.D * 2
+
+
+def paged_decode_inputs(B: int, Hq: int, Hkv: int, D: int, page_size: int, lengths, dtype: str, seed: int,
+                        spare_pages: int = 3):
+    """CPU tensors for one paged decode step: q [B, Hq, D], cache [P, 2, T, Hkv, D],
+    block_table [B, max_pages] int32 (entries past a request's last page are -1),
+    lengths [B] int32.  Physical pages are a seeded permutation, so logical order and
+    physical order differ; values are N(0, 1) drawn in float64 and rounded once."""
+    lengths = [int(x) for x in lengths]
+    pages_per = [(L + page_size - 1) // page_size for L in lengths]
+    max_pages = max(1, max(pages_per))
+    P = sum(pages_per) + spare_pages
+    g = torch.Generator(device="cpu").manual_seed(int(seed))
+    perm = torch.randperm(P, generator=g)
+    table = torch.full((B, max_pages), -1, dtype=torch.int32)
+    nxt = 0
+    for b, n in enumerate(pages_per):
+        table[b, :n] = perm[nxt:nxt + n].to(torch.int32)
+        nxt += n
+    t = TORCH_DTYPES[dtype]
+    q = torch.randn(B, Hq, D, generator=g, dtype=torch.float64).to(torch.float32).to(t)
+    cache = torch.randn(P, 2, page_size, Hkv, D, generator=g, dtype=torch.float64).to(torch.float32).to(t)
+    return q, cache, table, torch.tensor(lengths, dtype=torch.int32)
+
+
+PAGED_BENCH = PagedWorkload("paged_decode_b8_hq32_hkv8_d128_t16_ctx32768_fp16", 8, 32, 8, 128, 16, 32768,
+                            "fp16", 11)
+PAGED_CONTEXTS = (1024, 4096, 8192, 16384, 32768)

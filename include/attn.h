@@ -54,7 +54,9 @@ enum attn_status {
   ATTN_ERR_LAUNCH = -5,         /* the CUDA runtime refused the launch (cudaGetLastError) */
   ATTN_ERR_TIMEOUT = -6,        /* a kernel's bounded wait expired (reported by attn_device_status) */
   ATTN_ERR_CUDA = -7,           /* another CUDA runtime/driver call failed */
-  ATTN_ERR_SCRATCH_LIMIT = -8   /* attn_fwd_splitkv_noalloc: the split needs more than its fixed scratch */
+  ATTN_ERR_SCRATCH_LIMIT = -8,  /* attn_fwd_splitkv_noalloc: the split needs more than its fixed scratch */
+  ATTN_ERR_BAD_INDEX = -9       /* paged cache: a block-table entry or length out of range (reported by
+                                   attn_device_status; those tokens were skipped, not read) */
 };
 
 /*
@@ -151,6 +153,67 @@ size_t attn_splitkv_workspace_bytes(int B, int H, int N, int D, int kv_splits);
  * the number of 128-key tiles and by 64.  Negative attn_status on bad sizes or a
  * non-sm_103 device. */
 int attn_splitkv_default_splits(int B, int H, int N, int D);
+
+/*
+ * attn_decode_paged -- one decode step of attention over a paged K/V cache with
+ * grouped heads (page "CUDA KV Cache：分页存储与长上下文 Decode 极致优化": layout
+ * and address rule of section 2, GQA head map of section 3.3, warp dataflow of
+ * section 5, split-KV of section 6.4).  Request b's query (one token per head)
+ * attends all lengths[b] tokens of its context:
+ *     O[b, h] = softmax_t(scale * q[b, h] . K[b, t, h / g]) V[b, t, h / g],  g = Hq / Hkv,
+ * where token t of request b lives on page block_table[b, t / page_size] at
+ * offset t % page_size.
+ *   q           : device, [B, Hq, D] fp16, 16-byte aligned.
+ *   cache       : device, [num_pages, 2, page_size, Hkv, D] fp16 (index 0 = K,
+ *                 1 = V), 16-byte aligned, read only.
+ *   block_table : device, [B, max_pages] int32; entries past a request's last
+ *                 page are never read.
+ *   lengths     : device, [B] int32, 0 .. max_pages * page_size.
+ *   out         : device, [B, Hq, D] fp16, written in full.
+ *   lse         : device, [B, Hq] fp32 natural-log log-sum-exp, or NULL.
+ *   Hq % Hkv == 0.  D : 64 or 128.  page_size : 8, 16, 32 or 64.
+ *   scale       : finite and > 0.
+ *   kv_splits   : 1 .. 64 segments of the context (see attn_decode_default_splits);
+ *                 more than one needs `workspace` (256-byte aligned, at least
+ *                 attn_decode_workspace_bytes(B, Hq, D, kv_splits) bytes,
+ *                 contents on entry irrelevant); with 1 it may be NULL.
+ * A request with length 0 gets O = 0 and lse = -inf.  A block-table entry
+ * outside [0, num_pages) or a length outside [0, max_pages * page_size] is not
+ * followed: the tokens it names are skipped and attn_device_status reports
+ * ATTN_ERR_BAD_INDEX.  Probabilities stay fp32 (no 16-bit rounding of P).
+ */
+int attn_decode_paged(const void* q, const void* cache, const int* block_table, const int* lengths,
+                      void* out, float* lse, int B, int Hq, int Hkv, int D, int page_size,
+                      int max_pages, int num_pages, float scale, int kv_splits, void* workspace,
+                      size_t workspace_bytes, attn_stream_t stream);
+
+/* attn_decode_paged_bf16 -- the same with bf16 q, cache and out. */
+int attn_decode_paged_bf16(const void* q, const void* cache, const int* block_table,
+                           const int* lengths, void* out, float* lse, int B, int Hq, int Hkv, int D,
+                           int page_size, int max_pages, int num_pages, float scale, int kv_splits,
+                           void* workspace, size_t workspace_bytes, attn_stream_t stream);
+
+/* Workspace bytes of attn_decode_paged for kv_splits > 1 (0 when none is needed or
+ * the sizes are invalid).  Needs no GPU. */
+size_t attn_decode_workspace_bytes(int B, int Hq, int D, int kv_splits);
+
+/* A context split for the current device: about four CTAs per SM, capped by the
+ * 64-token tiles of max_pages * page_size and by 64.  Negative attn_status on bad
+ * sizes or a non-sm_103 device. */
+int attn_decode_default_splits(int B, int Hq, int Hkv, int page_size, int max_pages);
+
+/*
+ * attn_paged_append -- writes the newest token of every request into the paged
+ * cache (the same page's section 4): row (b, kind, head) of new_kv
+ * [B, 2, Hkv, D] (16-bit, 16-byte aligned) goes to
+ * cache[block_table[b, t / page_size]][kind][t % page_size][head] with
+ * t = lengths[b] - 1, as 16-byte stores.  Sizes and layout as attn_decode_paged;
+ * element type does not matter (a copy of 16-bit values).  Out-of-range entries
+ * are skipped and reported as ATTN_ERR_BAD_INDEX by attn_device_status.
+ */
+int attn_paged_append(const void* new_kv, void* cache, const int* block_table, const int* lengths,
+                      int B, int Hkv, int D, int page_size, int max_pages, int num_pages,
+                      attn_stream_t stream);
 
 /*
  * attn_row_softmax_f32 -- row softmax of an fp32 matrix with the online (m, d)

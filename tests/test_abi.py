@@ -149,3 +149,28 @@ def test_row_softmax_argument_errors_without_gpu(lib):
     assert f(A, A + SZ, 4, 0, None) == -1
     assert f(A + 1, A + SZ, 4, 8, None) == -2
     assert f(A, A + 16, 4, 8, None) == -1  # y overlaps x without being x
+
+
+def test_paged_argument_errors_without_gpu(lib):
+    f = lib.attn_decode_paged
+    Q, C, BT, LN, O, W = A, A + SZ, A + 2 * SZ, A + 3 * SZ, A + 4 * SZ, A + 6 * SZ
+
+    def c(B=2, Hq=8, Hkv=2, D=128, T=16, mp=4, np_=8, scale=0.1, splits=1, ws=None, wsb=0, q=Q, bt=BT):
+        return f(q, C, bt, LN, O, None, B, Hq, Hkv, D, T, mp, np_, scale, splits, ws, wsb, None)
+
+    assert c(Hkv=3) == -1
+    assert c(D=96) == -3
+    assert c(T=12) == -1
+    assert c(splits=0) == -1
+    assert c(splits=65) == -1
+    assert c(splits=2, mp=16) == -1  # a real split (16 pages = 4 tiles) needs a workspace
+    assert c(splits=2, mp=16, ws=W + 8, wsb=1 << 20) == -2
+    assert c(scale=-1.0) == -1
+    assert c(q=Q + 2) == -2
+    assert c(bt=BT + 2) == -2
+    assert lib.attn_decode_workspace_bytes(2, 8, 128, 1) == 0
+    assert lib.attn_decode_workspace_bytes(2, 8, 128, 4) == 4 * 2 * 8 * 128 * 4 + 256
+    g = lib.attn_paged_append
+    assert g(None, C, BT, LN, 2, 2, 128, 16, 4, 8, None) == -1
+    assert g(A + 8, C, BT, LN, 2, 2, 128, 16, 4, 8, None) == -2
+    assert g(A, C, BT, LN, 2, 2, 128, 24, 4, 8, None) == -1
