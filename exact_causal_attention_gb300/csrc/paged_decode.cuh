@@ -15,9 +15,14 @@
 // 64-token tiles; thread 0 issues the copies.  With M = HC <= 8 query rows the
 // arithmetic is far below the tensor-core shapes and the kernel is HBM-bound
 // (about 4 FLOP per byte), so scores and P V run on the FP32 pipes:
-//   scores: one thread per (head, token) dot product, reading the swizzled K row;
+//   scores: two threads per token row, each converting half of the K row to fp32
+//           once and using it for every head of the chunk (one shuffle joins
+//           the halves);
 //   softmax: one warp per head, lanes over the tile's tokens (shuffle reductions);
-//   P V: one thread per output column, HC accumulators in registers.
+//   P V: one thread per column pair and run of tokens, HC packed accumulators,
+//        p stored token-major so one vector load serves four heads; the runs'
+//        partial sums meet once per unit.
+// Page and row offsets use shifts (page sizes are powers of two).
 // Page ids outside [0, P) and lengths outside [0, max_pages * T] are not read:
 // the kernel records ATTN_ERR_BAD_INDEX in the status word and treats them as
 // empty.
@@ -32,6 +37,7 @@ namespace eca {
 constexpr int kDecTile = 64;     // tokens per tile
 constexpr int kDecStages = 3;
 constexpr int kDecThreads = 128;
+constexpr int kDecIdRing = 64;  // page ids staged in shared memory, a rolling window of the segment
 
 struct DecodeParams {
   const void* q;            // [B, Hq, D] 16-bit
@@ -56,21 +62,16 @@ struct DecodeSmem {
   static constexpr int kStageBytes = 2 * kKindBytes;
   static constexpr int kRingOff = 0;
   static constexpr int kQOff = kDecStages * kStageBytes;           // fp32 [8][D], pre-scaled query
-  static constexpr int kSOff = kQOff + 8 * D * 4;                  // fp32 [8][64] scores, then p
-  static constexpr int kStatOff = kSOff + 8 * kDecTile * 4;        // fp32 [8] alpha, [8] m, [8] l
+  static constexpr int kSOff = kQOff + 8 * D * 4;                  // fp32 [8][64] scores
+  static constexpr int kPOff = kSOff + 8 * kDecTile * 4;           // fp32 [64][8] p, token-major
+  static constexpr int kRedOff = kPOff + kDecTile * 8 * 4;         // fp32 partial outputs, 8 KB
+  static constexpr int kIdsOff = kRedOff + 8192;                   // int32 page ids of the segment
+  static constexpr int kStatOff = kIdsOff + kDecIdRing * 4;      // fp32 [8] alpha, [8] m, [8] l
   static constexpr int kBarOff = kStatOff + 3 * 8 * 4;
   static constexpr int kMiscOff = kBarOff + kDecStages * 8;        // abort flag
   static constexpr int kBytes = kMiscOff + 16;
   static constexpr int kDynamicBytes = kBytes + 1024;
 };
-
-// Element d of token row r of a tile kind (K or V) staged as swizzled T x 64 boxes.
-template <int D>
-__device__ __forceinline__ int dec_elem_offset(int r, int d, int T) {
-  const int page = r / T, rr = r % T, half = d / 64, c = (d % 64) / 8;
-  const int box = page * (D / 64) + half;
-  return box * T * 128 + rr * 128 + ((c ^ (rr % 8)) * 16) + (d % 8) * 2;  // bytes
-}
 
 template <bool BF16>
 __device__ __forceinline__ float to_f32(uint16_t h) {
@@ -88,6 +89,17 @@ __device__ __forceinline__ float2 to_f32x2(uint32_t w) {
   return make_float2(to_f32<BF16>(static_cast<uint16_t>(w & 0xffffu)), to_f32<BF16>(static_cast<uint16_t>(w >> 16)));
 }
 
+// Byte offset, inside one kind of a tile, of the 16-byte chunk c (0 .. D/8 - 1) of
+// token row r.  Rows are staged as swizzled (T x 64) boxes: box (page, half) holds
+// T rows of 128 B, and chunk index c % 8 is stored at position (c % 8) ^ (row % 8).
+template <int D>
+__device__ __forceinline__ int dec_chunk_offset(int r, int c, int log2T) {
+  const int T = 1 << log2T;
+  const int page = r >> log2T, rr = r & (T - 1);
+  const int box = page * (D / 64) + (c >> 3);
+  return ((box * T + rr) << 7) + (((c & 7) ^ (rr & 7)) << 4);
+}
+
 template <int D, bool BF16, int HC>
 __global__ void __launch_bounds__(kDecThreads) paged_decode_kernel(const __grid_constant__ CUtensorMap tm_cache,
                                                                    const DecodeParams p) {
@@ -98,6 +110,9 @@ __global__ void __launch_bounds__(kDecThreads) paged_decode_kernel(const __grid_
   uint8_t* smem = smem_raw + (sbase - raw_base);
   float* q_s = reinterpret_cast<float*>(smem + L::kQOff);
   float* s_s = reinterpret_cast<float*>(smem + L::kSOff);
+  float* p_s = reinterpret_cast<float*>(smem + L::kPOff);
+  float* red_s = reinterpret_cast<float*>(smem + L::kRedOff);
+  int* ids_s = reinterpret_cast<int*>(smem + L::kIdsOff);
   float* alpha_s = reinterpret_cast<float*>(smem + L::kStatOff);
   float* m_s = alpha_s + 8;
   float* l_s = alpha_s + 16;
@@ -116,14 +131,15 @@ __global__ void __launch_bounds__(kDecThreads) paged_decode_kernel(const __grid_
   const int group = p.Hq / p.Hkv;
   const int qh0 = kvh * group + chunk * HC;  // first query head of this CTA
   const int T = p.page_size;
-  const int pages_per_tile = kDecTile / T;
+  const int log2T = 31 - __clz(T);
+  const int pages_per_tile = kDecTile >> log2T;
 
   int len = p.lengths[b];
   if (len < 0 || len > p.max_pages * T) {
     if (tid == 0) atomicExch(p.status, p.bad_index_code);
     len = len < 0 ? 0 : p.max_pages * T;
   }
-  const int n_pages = (len + T - 1) / T;
+  const int n_pages = (len + T - 1) >> log2T;
   const int pg_begin = seg * p.seg_pages;
   const int pg_end = min(n_pages, pg_begin + p.seg_pages);
   const int n_tiles = pg_end > pg_begin ? (pg_end - pg_begin + pages_per_tile - 1) / pages_per_tile : 0;
@@ -133,6 +149,17 @@ __global__ void __launch_bounds__(kDecThreads) paged_decode_kernel(const __grid_
     *abort_flag = 0;
     fence_barrier_init();
   }
+  // Page ids of the segment in a rolling window of kDecIdRing slots (slot = page % ring),
+  // read from global memory once each; rejected ids become -1.
+  auto checked_id = [&](int id) {
+    if (id < 0 || id >= p.num_pages) {
+      atomicExch(p.status, p.bad_index_code);
+      return -1;
+    }
+    return id;
+  };
+  const int* table_row = p.block_table + static_cast<size_t>(b) * p.max_pages;
+  if (tid < kDecIdRing && pg_begin + tid < pg_end) ids_s[tid] = checked_id(table_row[pg_begin + tid]);
   // query rows of this chunk, scaled by scale * log2(e), in fp32
   const uint16_t* qg = static_cast<const uint16_t*>(p.q) + (static_cast<size_t>(b) * p.Hq + qh0) * D;
   for (int i = tid; i < HC * D; i += kDecThreads) q_s[i] = to_f32<BF16>(qg[i]) * p.scale_log2e;
@@ -149,39 +176,33 @@ __global__ void __launch_bounds__(kDecThreads) paged_decode_kernel(const __grid_
   auto issue_tile = [&](int i) {
     const int slot = i % kDecStages;
     const uint32_t stage = sbase + L::kRingOff + slot * L::kStageBytes;
-    const int first = pg_begin + i * pages_per_tile;
-    const int np = min(pages_per_tile, pg_end - first);
+    const int first = i * pages_per_tile;  // within the segment
+    const int np = min(pages_per_tile, pg_end - pg_begin - first);
     int good = 0;
-    int ids[kDecTile / 8];
-    for (int pp = 0; pp < np; ++pp) {
-      const int id = p.block_table[static_cast<size_t>(b) * p.max_pages + first + pp];
-      if (id < 0 || id >= p.num_pages) {
-        atomicExch(p.status, p.bad_index_code);
-        ids[pp] = -1;
-      } else {
-        ids[pp] = id;
-        ++good;
-      }
-    }
+    for (int pp = 0; pp < np; ++pp) good += ids_s[(first + pp) % kDecIdRing] >= 0 ? 1 : 0;
     mbar_arrive_expect_tx(bar(slot), static_cast<uint32_t>(good * 2 * (D / 64) * T * 128));
     for (int pp = 0; pp < np; ++pp) {
-      if (ids[pp] < 0) continue;
+      const int id = ids_s[(first + pp) % kDecIdRing];
+      if (id < 0) continue;
       for (int kind = 0; kind < 2; ++kind) {
         for (int h = 0; h < D / 64; ++h) {
           const uint32_t dst = stage + kind * L::kKindBytes + (pp * (D / 64) + h) * T * 128;
-          tma_load_3d(dst, &tm_cache, bar(slot), 64 * h, kvh, (ids[pp] * 2 + kind) * T, pol);
+          tma_load_3d(dst, &tm_cache, bar(slot), 64 * h, kvh, (id * 2 + kind) * T, pol);
         }
       }
     }
   };
 
-  float o[HC];
+  // Score mapping: two threads per token row, each owning half of the D columns.
+  const int s_row = tid >> 1, s_half = tid & 1;
+  // P V mapping: one thread per column pair, the tile's 64 tokens split into kTokSplit runs.
+  constexpr int kPairs = D / 2;
+  constexpr int kTokSplit = kDecThreads / kPairs;  // 2 (D = 128) or 4 (D = 64)
+  constexpr int kRun = kDecTile / kTokSplit;
+  const int cp = tid % kPairs, run = tid / kPairs;
+  float2 acc[HC];
 #pragma unroll
-  for (int k = 0; k < HC; ++k) o[k] = 0.f;
-  constexpr int kColsPerPass = D;                      // one output column per thread per head set
-  constexpr int kHeadSets = kDecThreads / kColsPerPass;  // 1 (D = 128) or 2 (D = 64)
-  const int col = tid % D;
-  const int hset = tid / D;
+  for (int k = 0; k < HC; ++k) acc[k] = make_float2(0.f, 0.f);
 
   int issued = 0;  // tiles whose copies thread 0 has started
   if (tid == 0) {
@@ -190,6 +211,11 @@ __global__ void __launch_bounds__(kDecThreads) paged_decode_kernel(const __grid_
   }
   bool ok = true;
   for (int i = 0; i < n_tiles && ok; ++i) {
+    // The pages of this tile leave the id window after it; their slots take the pages
+    // kDecIdRing further on.  The load starts now and is stored at the end of the tile.
+    const int refill = i * pages_per_tile + kDecIdRing + tid;  // within the segment
+    const bool refills = tid < pages_per_tile && pg_begin + refill < pg_end;
+    const int refill_id = refills ? table_row[pg_begin + refill] : -1;
     if (tid == 0 && i + kDecStages - 1 < n_tiles) issue_tile(issued++);
     const int slot = i % kDecStages;
     const bool got = wd.wait(bar(slot), static_cast<uint32_t>(i / kDecStages) & 1u);
@@ -200,42 +226,54 @@ __global__ void __launch_bounds__(kDecThreads) paged_decode_kernel(const __grid_
     const uint8_t* kt = smem + L::kRingOff + slot * L::kStageBytes;
     const uint8_t* vt = kt + L::kKindBytes;
     const int first_page = pg_begin + i * pages_per_tile;
-    const int tok0 = first_page * T;  // logical token of tile row 0
+    const int tok0 = first_page << log2T;  // logical token of tile row 0
     // Rows that hold a token of this segment on an accepted page; the rest (past the
     // length, past the segment, or on a rejected page) are empty.
     uint64_t rows_ok = 0;
     for (int pp = 0; pp < pages_per_tile && first_page + pp < pg_end; ++pp) {
-      const int id = p.block_table[static_cast<size_t>(b) * p.max_pages + first_page + pp];
-      if (id < 0 || id >= p.num_pages) continue;
-      const int lo = pp * T, hi = min((pp + 1) * T, len - tok0);
-      for (int r = lo; r < hi; ++r) rows_ok |= 1ull << r;
+      if (ids_s[(first_page - pg_begin + pp) % kDecIdRing] < 0) continue;
+      const int lo = pp << log2T, hi = min((pp + 1) << log2T, len - tok0);
+      if (hi > lo) rows_ok |= (hi - lo == 64 ? ~0ull : ((1ull << (hi - lo)) - 1)) << lo;
     }
-    auto row_ok = [&](int r) { return ((rows_ok >> r) & 1ull) != 0; };
 
-    // scores: s = q . k (already in the base-2 domain)
-    for (int w = tid; w < HC * kDecTile; w += kDecThreads) {
-      const int qh = w / kDecTile, r = w % kDecTile;
-      float acc = 0.f;
-      if (row_ok(r)) {
+    // scores s = q . k in the base-2 domain: this thread's half row of K, converted once,
+    // against every head of the chunk; the two halves meet through one shuffle.
+    {
+      const bool live = (rows_ok >> s_row) & 1ull;
+      float kf[D / 2];
+      if (live) {
 #pragma unroll
-        for (int c = 0; c < D / 8; ++c) {
-          const uint4 kv = *reinterpret_cast<const uint4*>(kt + dec_elem_offset<D>(r, c * 8, T));
-          const float* qq = q_s + qh * D + c * 8;
-          const float2 k0 = to_f32x2<BF16>(kv.x), k1 = to_f32x2<BF16>(kv.y);
-          const float2 k2 = to_f32x2<BF16>(kv.z), k3 = to_f32x2<BF16>(kv.w);
-          acc = fmaf(qq[0], k0.x, acc);
-          acc = fmaf(qq[1], k0.y, acc);
-          acc = fmaf(qq[2], k1.x, acc);
-          acc = fmaf(qq[3], k1.y, acc);
-          acc = fmaf(qq[4], k2.x, acc);
-          acc = fmaf(qq[5], k2.y, acc);
-          acc = fmaf(qq[6], k3.x, acc);
-          acc = fmaf(qq[7], k3.y, acc);
+        for (int c = 0; c < D / 16; ++c) {
+          const uint4 w = *reinterpret_cast<const uint4*>(kt + dec_chunk_offset<D>(s_row, s_half * (D / 16) + c, log2T));
+          const float2 a = to_f32x2<BF16>(w.x), bb = to_f32x2<BF16>(w.y), cc = to_f32x2<BF16>(w.z),
+                       dd = to_f32x2<BF16>(w.w);
+          kf[8 * c + 0] = a.x;
+          kf[8 * c + 1] = a.y;
+          kf[8 * c + 2] = bb.x;
+          kf[8 * c + 3] = bb.y;
+          kf[8 * c + 4] = cc.x;
+          kf[8 * c + 5] = cc.y;
+          kf[8 * c + 6] = dd.x;
+          kf[8 * c + 7] = dd.y;
         }
       } else {
-        acc = -INFINITY;
+#pragma unroll
+        for (int e = 0; e < D / 2; ++e) kf[e] = 0.f;
       }
-      s_s[qh * kDecTile + r] = acc;
+#pragma unroll
+      for (int k = 0; k < HC; ++k) {
+        const float4* qq = reinterpret_cast<const float4*>(q_s + k * D + s_half * (D / 2));
+        float2 a2 = make_float2(0.f, 0.f), b2 = make_float2(0.f, 0.f);
+#pragma unroll
+        for (int e = 0; e < D / 8; ++e) {
+          const float4 qv = qq[e];
+          a2 = __ffma2_rn(make_float2(qv.x, qv.y), make_float2(kf[4 * e], kf[4 * e + 1]), a2);
+          b2 = __ffma2_rn(make_float2(qv.z, qv.w), make_float2(kf[4 * e + 2], kf[4 * e + 3]), b2);
+        }
+        float dot = (a2.x + a2.y) + (b2.x + b2.y);
+        dot += __shfl_xor_sync(0xffffffffu, dot, 1);
+        if (s_half == 0) s_s[k * kDecTile + s_row] = live ? dot : -INFINITY;
+      }
     }
     __syncthreads();
 
@@ -253,8 +291,8 @@ __global__ void __launch_bounds__(kDecThreads) paged_decode_kernel(const __grid_
 #pragma unroll
       for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
       const float alpha = m_old == -INFINITY ? 0.f : ex2(m_old - m_new);
-      s_s[qh * kDecTile + lane] = p0;
-      s_s[qh * kDecTile + lane + 32] = p1;
+      p_s[lane * 8 + qh] = p0;
+      p_s[(lane + 32) * 8 + qh] = p1;
       __syncwarp();
       if (lane == 0) {
         alpha_s[qh] = alpha;
@@ -264,44 +302,81 @@ __global__ void __launch_bounds__(kDecThreads) paged_decode_kernel(const __grid_
     }
     __syncthreads();
 
-    // o = alpha o + sum_r p_r v_r for this thread's column; rows with p = 0 are skipped
-    // (an empty row's V is never read: its data may not be a number).
+    // o = alpha o + sum_r p_r v_r: this thread's column pair over its run of rows.
+    // Empty rows are skipped (their V is never read: its data may not be a number).
 #pragma unroll
     for (int k = 0; k < HC; ++k) {
-      if (k % kHeadSets == hset) o[k] *= alpha_s[k];
+      const float al = alpha_s[k];
+      acc[k] = __fmul2_rn(acc[k], make_float2(al, al));
     }
-    for (int r = 0; r < kDecTile; ++r) {
-      if (!row_ok(r)) continue;
-      const float v = to_f32<BF16>(*reinterpret_cast<const uint16_t*>(vt + dec_elem_offset<D>(r, col, T)));
+    const int c = (2 * cp) >> 3, within = ((2 * cp) & 7) * 2;  // 16-byte chunk and byte inside it
+    const uint64_t run_mask = (rows_ok >> (run * kRun)) & ((kRun == 64 ? ~0ull : (1ull << kRun) - 1));
+    if (run_mask == (kRun == 64 ? ~0ull : (1ull << kRun) - 1)) {
+#pragma unroll 4
+      for (int j = 0; j < kRun; ++j) {
+        const int r = run * kRun + j;
+        const float2 v = to_f32x2<BF16>(*reinterpret_cast<const uint32_t*>(vt + dec_chunk_offset<D>(r, c, log2T) + within));
+        const float4* pp = reinterpret_cast<const float4*>(p_s + r * 8);
+        const float4 pa = pp[0];
+        const float pr[8] = {pa.x, pa.y, pa.z, pa.w, 0.f, 0.f, 0.f, 0.f};
+        float4 pb = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (HC > 4) pb = pp[1];
 #pragma unroll
-      for (int k = 0; k < HC; ++k) {
-        if (k % kHeadSets == hset) o[k] = fmaf(s_s[k * kDecTile + r], v, o[k]);
+        for (int k = 0; k < HC; ++k) {
+          const float pk = k < 4 ? pr[k] : (k == 4 ? pb.x : (k == 5 ? pb.y : (k == 6 ? pb.z : pb.w)));
+          acc[k] = __ffma2_rn(make_float2(pk, pk), v, acc[k]);
+        }
+      }
+    } else {
+      for (int j = 0; j < kRun; ++j) {
+        if (!((run_mask >> j) & 1ull)) continue;
+        const int r = run * kRun + j;
+        const float2 v = to_f32x2<BF16>(*reinterpret_cast<const uint32_t*>(vt + dec_chunk_offset<D>(r, c, log2T) + within));
+#pragma unroll
+        for (int k = 0; k < HC; ++k) {
+          const float pk = p_s[r * 8 + k];
+          acc[k] = __ffma2_rn(make_float2(pk, pk), v, acc[k]);
+        }
       }
     }
-    __syncthreads();  // the stage and the scores may be overwritten now
+    if (refills) ids_s[refill % kDecIdRing] = checked_id(refill_id);
+    __syncthreads();  // the stage, the scores and p may be overwritten now
   }
 
   if (ok) {
-    // epilogue: O = o / l, lse = (m + log2 l) ln 2; an empty context gives O = 0, lse = -inf
+    // the runs' partial outputs meet in shared memory, then O = o / l and
+    // lse = (m + log2 l) ln 2; an empty context gives O = 0 and lse = -inf
+    if (run > 0) {
 #pragma unroll
-    for (int k = 0; k < HC; ++k) {
-      if (k % kHeadSets != hset) continue;
-      const float l = l_s[k];
-      const float val = l > 0.f ? o[k] / l : 0.f;
-      const size_t row = static_cast<size_t>(b) * p.Hq + qh0 + k;
-      if (p.part_o != nullptr) {
-        p.part_o[(static_cast<size_t>(seg) * p.B * p.Hq + row) * D + col] = val;
-      } else {
-        uint16_t* dst = static_cast<uint16_t*>(p.out) + row * D + col;
-        const uint32_t packed = pack2<BF16>(val, 0.f);
-        *dst = static_cast<uint16_t>(packed & 0xffffu);
-      }
-      if (col == 0) {
-        const float lse = l > 0.f ? (m_s[k] + log2f(l)) * 0.69314718055994530942f : -INFINITY;
+      for (int k = 0; k < HC; ++k)
+        *reinterpret_cast<float2*>(red_s + ((run - 1) * 8 + k) * D + 2 * cp) = acc[k];
+    }
+    __syncthreads();
+    if (run == 0) {
+#pragma unroll
+      for (int k = 0; k < HC; ++k) {
+        float2 o = acc[k];
+        for (int rr = 1; rr < kTokSplit; ++rr) {
+          const float2 part = *reinterpret_cast<const float2*>(red_s + ((rr - 1) * 8 + k) * D + 2 * cp);
+          o.x += part.x;
+          o.y += part.y;
+        }
+        const float l = l_s[k];
+        const float inv = l > 0.f ? 1.f / l : 0.f;
+        const size_t row = static_cast<size_t>(b) * p.Hq + qh0 + k;
         if (p.part_o != nullptr) {
-          p.part_lse[static_cast<size_t>(seg) * p.B * p.Hq + row] = lse;
-        } else if (p.lse != nullptr) {
-          p.lse[row] = lse;
+          *reinterpret_cast<float2*>(p.part_o + (static_cast<size_t>(seg) * p.B * p.Hq + row) * D + 2 * cp) =
+              make_float2(o.x * inv, o.y * inv);
+        } else {
+          *reinterpret_cast<uint32_t*>(static_cast<uint16_t*>(p.out) + row * D + 2 * cp) = pack2<BF16>(o.x * inv, o.y * inv);
+        }
+        if (cp == 0) {
+          const float lse = l > 0.f ? (m_s[k] + log2f(l)) * 0.69314718055994530942f : -INFINITY;
+          if (p.part_o != nullptr) {
+            p.part_lse[static_cast<size_t>(seg) * p.B * p.Hq + row] = lse;
+          } else if (p.lse != nullptr) {
+            p.lse[row] = lse;
+          }
         }
       }
     }
