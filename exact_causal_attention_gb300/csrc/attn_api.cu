@@ -356,7 +356,9 @@ int launch_decode(const CUtensorMap& tm, eca::DecodeParams& p, const DecodeShape
   auto run = [&](auto kernel, unsigned bit) -> int {
     if (!(st->configured_decode & bit)) {
       if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kDynamicBytes) !=
-          cudaSuccess) {
+              cudaSuccess ||
+          cudaFuncSetAttribute(kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+                               cudaSharedmemCarveoutMaxShared) != cudaSuccess) {
         return ATTN_ERR_CUDA;
       }
       st->configured_decode |= bit;
@@ -563,7 +565,8 @@ int attn_decode_default_splits(int B, int Hq, int Hkv, int page_size, int max_pa
   const DecodeShape one = decode_shape(Hq, Hkv, page_size, max_pages, 1);
   const long long ctas = static_cast<long long>(B) * Hkv * one.head_chunks;
   const long long tiles = (static_cast<long long>(max_pages) * page_size + eca::kDecTile - 1) / eca::kDecTile;
-  long long s = (4LL * st->sm_count + ctas - 1) / ctas;  // about four CTAs per SM
+  // One wave of the three CTAs an SM holds, at least one segment each.
+  long long s = 3LL * st->sm_count / ctas;
   if (s > tiles) s = tiles;
   if (s > kMaxSplits) s = kMaxSplits;
   return s < 1 ? 1 : static_cast<int>(s);

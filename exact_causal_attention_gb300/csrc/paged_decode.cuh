@@ -21,7 +21,9 @@
 //   softmax: one warp per head, lanes over the tile's tokens (shuffle reductions);
 //   P V: one thread per column pair and run of tokens, HC packed accumulators,
 //        p stored token-major so one vector load serves four heads; the runs'
-//        partial sums meet once per unit.
+//        partial sums meet once per unit, in the ring's memory once every copy
+//        has been consumed.
+// About 73 KB of shared memory, so three CTAs share an SM.
 // Page and row offsets use shifts (page sizes are powers of two).
 // Page ids outside [0, P) and lengths outside [0, max_pages * T] are not read:
 // the kernel records ATTN_ERR_BAD_INDEX in the status word and treats them as
@@ -35,7 +37,7 @@
 namespace eca {
 
 constexpr int kDecTile = 64;     // tokens per tile
-constexpr int kDecStages = 3;
+constexpr int kDecStages = 2;
 constexpr int kDecThreads = 128;
 constexpr int kDecIdRing = 64;  // page ids staged in shared memory, a rolling window of the segment
 
@@ -64,8 +66,8 @@ struct DecodeSmem {
   static constexpr int kQOff = kDecStages * kStageBytes;           // fp32 [8][D], pre-scaled query
   static constexpr int kSOff = kQOff + 8 * D * 4;                  // fp32 [8][64] scores
   static constexpr int kPOff = kSOff + 8 * kDecTile * 4;           // fp32 [64][8] p, token-major
-  static constexpr int kRedOff = kPOff + kDecTile * 8 * 4;         // fp32 partial outputs, 8 KB
-  static constexpr int kIdsOff = kRedOff + 8192;                   // int32 page ids of the segment
+  static constexpr int kRedOff = kRingOff;  // fp32 partial outputs (8 KB), over the ring once it is idle
+  static constexpr int kIdsOff = kPOff + kDecTile * 8 * 4;         // int32 page-id window
   static constexpr int kStatOff = kIdsOff + kDecIdRing * 4;      // fp32 [8] alpha, [8] m, [8] l
   static constexpr int kBarOff = kStatOff + 3 * 8 * 4;
   static constexpr int kMiscOff = kBarOff + kDecStages * 8;        // abort flag
