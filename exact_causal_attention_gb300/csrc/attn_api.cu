@@ -94,12 +94,12 @@ int device_state(DeviceState** out) {
 // [B*H, N, D] 16-bit tensor as a rank-3 map (D, N, B*H) with 64 x 128 x 1 boxes,
 // 128-byte swizzle; rows past N read as zero.
 int encode_qkv_map(EncodeTiledFn encode, CUtensorMap* map, const void* ptr, bool bf16, int D, int N,
-                   int BH) {
+                   int BH, unsigned box_rows = 128) {
   const cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(N),
                               static_cast<cuuint64_t>(BH)};
   const cuuint64_t strides[2] = {static_cast<cuuint64_t>(D) * 2,
                                  static_cast<cuuint64_t>(N) * static_cast<cuuint64_t>(D) * 2};
-  const cuuint32_t box[3] = {64, 128, 1};
+  const cuuint32_t box[3] = {64, box_rows, 1};
   const cuuint32_t elem_strides[3] = {1, 1, 1};
   const CUresult r =
       encode(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3,
@@ -180,10 +180,12 @@ int launch(const void* q, const void* k, const void* v, void* o, float* lse, int
     }
     st->configured |= bit;
   }
-  CUtensorMap tq, tk, tv;
+  CUtensorMap tq, tk, tv, to;
   int rc = encode_qkv_map(encode, &tq, q, BF16, D, N, BH);
   if (rc == ATTN_OK) rc = encode_qkv_map(encode, &tk, k, BF16, D, N, B * Hkv);
   if (rc == ATTN_OK) rc = encode_qkv_map(encode, &tv, v, BF16, D, N, B * Hkv);
+  // Output: stored by each softmax warp in 32-row slabs.
+  if (rc == ATTN_OK) rc = encode_qkv_map(encode, &to, o, BF16, D, N, BH, 32);
   if (rc != ATTN_OK) return rc;
 
   eca::FwdParams p;
@@ -207,7 +209,7 @@ int launch(const void* q, const void* k, const void* v, void* o, float* lse, int
   p.timeout_code = ATTN_ERR_TIMEOUT;
   // Persistent: one CTA per SM (the shared-memory footprint admits only one), never more than the units.
   const unsigned grid = static_cast<unsigned>(p.n_units < st->sm_count ? p.n_units : st->sm_count);
-  kernel<<<grid, eca::kThreads, L::kDynamicBytes, stream>>>(tq, tk, tv, p);
+  kernel<<<grid, eca::kThreads, L::kDynamicBytes, stream>>>(tq, tk, tv, to, p);
   if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_LAUNCH;
   if (part_o == nullptr) return ATTN_OK;
 

@@ -97,7 +97,12 @@ struct FwdSmem {
   static constexpr int kStages = D == 128 ? 2 : 4;
   static constexpr int kQOff = 0;
   static constexpr int kRingOff = 2 * kTileBytes;
-  static constexpr int kBarOff = kRingOff + kStages * kStageBytes;
+  // Per query tile, 16 KB staging for the output: 128 rows x 64 columns of
+  // 16-bit values in the 128-B swizzled box layout the TMA store reads, one
+  // 32-row slab per softmax warp.
+  static constexpr int kStageOutBytes = 128 * 128;
+  static constexpr int kOutOff = kRingOff + kStages * kStageBytes;
+  static constexpr int kBarOff = kOutOff + 2 * kStageOutBytes;
   // barrier indices
   static constexpr int kBarQFull = 0;
   static constexpr int kBarQFree = 1;                // two arrivals: both issuers
@@ -112,6 +117,7 @@ struct FwdSmem {
   static constexpr int kMiscOff = kBarOff + kNumBars * 8;  // TMEM base, abort flag, issue lock
   static constexpr int kBytes = kMiscOff + 16;
   static constexpr int kDynamicBytes = kBytes + 1024;  // slack for 1024-B alignment
+  static_assert(kDynamicBytes <= 227 * 1024, "shared memory exceeds the per-block limit");
 };
 
 // One work unit: query tiles 2*pair and 2*pair + 1 of slice bh, against the
@@ -184,7 +190,8 @@ __device__ __forceinline__ uint32_t parity(int count) { return static_cast<uint3
 template <int D, bool BF16>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                    const __grid_constant__ CUtensorMap tm_v, const FwdParams p) {
+                    const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
+                    const FwdParams p) {
   using L = FwdSmem<D>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_base = smem_u32(smem_raw);
@@ -428,16 +435,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (32 * q + i >= valid) s[q][i] = __float_as_uint(-INFINITY);
           }
         };
-        // p = 2^(s c - m_ref) for the row, packed for the P V MMA; returns sum p.
+        // p = 2^(s c - m_ref), packed for the P V MMA.
         uint32_t pk[2][32];
-        auto exponentiate = [&](float neg_m) -> float {
+        // Columns 32 q0 .. 32 q1 - 1 of the row into acc; called with (0, 4), or
+        // with (0, 2) then (2, 4) when keys 64-127 are still loading.
+        auto exp_quarters = [&](int q0, int q1, float neg_m, float2 (&acc)[8]) {
           const float2 c2 = make_float2(c, c);
           const float2 nm2 = make_float2(neg_m, neg_m);
-          float2 acc[8];
 #pragma unroll
-          for (int a = 0; a < 8; ++a) acc[a] = make_float2(0.f, 0.f);
-#pragma unroll
-          for (int q = 0; q < 4; ++q) {
+          for (int q = q0; q < q1; ++q) {
 #pragma unroll
             for (int i = 0; i < 32; i += 2) {
               const float2 x = __ffma2_rn(make_float2(__uint_as_float(s[q][i]), __uint_as_float(s[q][i + 1])), c2, nm2);
@@ -446,17 +452,46 @@ __global__ void __launch_bounds__(kThreads, 1)
               pk[q / 2][(q % 2) * 16 + i / 2] = pack2<BF16>(e.x, e.y);
             }
           }
+        };
+        auto row_total = [](const float2 (&acc)[8]) -> float {
           const float2 a = __fadd2_rn(__fadd2_rn(__fadd2_rn(acc[0], acc[1]), __fadd2_rn(acc[2], acc[3])),
                                       __fadd2_rn(__fadd2_rn(acc[4], acc[5]), __fadd2_rn(acc[6], acc[7])));
           return a.x + a.y;
+        };
+        // p = 2^(s c - m_ref) for the whole row in registers; returns sum p.
+        auto exponentiate = [&](float neg_m) -> float {
+          float2 acc[8];
+#pragma unroll
+          for (int a = 0; a < 8; ++a) acc[a] = make_float2(0.f, 0.f);
+          exp_quarters(0, 4, neg_m, acc);
+          return row_total(acc);
         };
 
         float alpha = 1.f;
         float row_sum = 0.f;
         bool move = true;  // the first key tile of a unit has no reference yet
         if (j > 0) {
-          load_scores();
-          row_sum = exponentiate(-m_ref);
+          const bool masked = (p.causal && w.kv0 + j == tile) || (ragged_keys && w.kv0 + j == p.n_tiles - 1);
+          if (masked) {
+            load_scores();
+            row_sum = exponentiate(-m_ref);
+          } else {
+            // Keys 64-127 load while keys 0-63 are exponentiated.
+            tmem_ld_x32(t_s, s[0]);
+            tmem_ld_x32(t_s + 32u, s[1]);
+            tmem_wait_ld_x32(s[0]);
+            tmem_wait_ld_x32(s[1]);
+            tmem_ld_x32(t_s + 64u, s[2]);
+            tmem_ld_x32(t_s + 96u, s[3]);
+            float2 acc[8];
+#pragma unroll
+            for (int a = 0; a < 8; ++a) acc[a] = make_float2(0.f, 0.f);
+            exp_quarters(0, 2, -m_ref, acc);
+            tmem_wait_ld_x32(s[2]);
+            tmem_wait_ld_x32(s[3]);
+            exp_quarters(2, 4, -m_ref, acc);
+            row_sum = row_total(acc);
+          }
           move = !(row_sum <= kMaxRowSum);  // also true for an overflowed (inf) sum
         }
         if (__any_sync(0xffffffffu, move)) {
@@ -539,34 +574,49 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (row < p.N) p.part_lse[prow] = row_lse;
         continue;
       }
-      uint16_t* orow = static_cast<uint16_t*>(p.o) +
-                       (static_cast<size_t>(w.bh) * p.N + static_cast<size_t>(row)) * D;
+      // O = o / l rounded to the output type, 64 columns at a time.  Each warp
+      // sends its 32 rows through its slab of the staging buffer with TMA stores
+      // (rows past N are clipped by the tensor map).
+      const uint32_t slab = sbase + L::kOutOff + t * L::kStageOutBytes + wq * 4096;
 #pragma unroll
-      for (int c0 = 0; c0 < D; c0 += 32) {
-        uint32_t o[32];
-        tmem_ld_x32(t_o + c0, o);
-        tmem_wait_ld_x32(o);
-        uint32_t h[16];
+      for (int c64 = 0; c64 < D / 64; ++c64) {
+        uint32_t h[32];
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          const float2 v = __fmul2_rn(make_float2(__uint_as_float(o[2 * i]), __uint_as_float(o[2 * i + 1])), il2);
-          h[i] = pack2<BF16>(v.x, v.y);
+        for (int half = 0; half < 2; ++half) {
+          uint32_t o[32];
+          tmem_ld_x32(t_o + 64 * c64 + 32 * half, o);
+          tmem_wait_ld_x32(o);
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const float2 v = __fmul2_rn(make_float2(__uint_as_float(o[2 * i]), __uint_as_float(o[2 * i + 1])), il2);
+            h[16 * half + i] = pack2<BF16>(v.x, v.y);
+          }
         }
-        if (row < p.N) {
-          uint4* dst = reinterpret_cast<uint4*>(orow + c0);
+        if (c64 == D / 64 - 1) {
+          // O_t has been read: the next unit's first P V may overwrite it.
+          tc_fence_before_sync();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bar(L::kBarOFree + t));
+        }
+        if (lane == 0) bulk_wait_read_all();  // the slab's previous contents have been read
+        __syncwarp();
 #pragma unroll
-          for (int v4 = 0; v4 < 4; ++v4)
-            dst[v4] = make_uint4(h[4 * v4], h[4 * v4 + 1], h[4 * v4 + 2], h[4 * v4 + 3]);
+        for (int ch = 0; ch < 8; ++ch) {
+          const uint32_t dst = slab + lane * 128 + ((ch ^ (lane & 7)) << 4);
+          st_shared_v4(dst, h[4 * ch], h[4 * ch + 1], h[4 * ch + 2], h[4 * ch + 3]);
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          tma_store_3d(&tm_o, slab, 64 * c64, tile * kBlockM + wq * 32, w.bh);
+          bulk_commit_group();
         }
       }
-      // O_t has been read: the next unit's first P V may overwrite it.
-      tc_fence_before_sync();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar(L::kBarOFree + t));
       if (p.lse != nullptr && row < p.N) {
         p.lse[static_cast<size_t>(w.bh) * p.N + row] = row_lse;
       }
     }
+    if (lane == 0) bulk_wait_all();  // every output store has landed before the block exits
   }
 
   tc_fence_before_sync();
