@@ -23,19 +23,20 @@
 //     section 6.4).  Grouped heads (same page, section 3.3): query head h
 //     reads key/value head h / (H / Hkv) directly, with no copy; the heads of
 //     one group are adjacent in the unit order so their K/V tiles come from L2.
-//     352 threads:
+//     384 threads:
 //       warps 0-3  softmax for query tile 0     warps 4-7  softmax for query tile 1
-//       warp 8     TMA producer (Q once per unit, then ring items {V_j, K_j+1})
+//       warp 8     TMA producer of the ring items {V_j, K_j+1}
 //       warp 9     TMEM owner; tcgen05.mma issuer for query tile 0
 //       warp 10    tcgen05.mma issuer for query tile 1
-//     One issuing thread per query tile: an MMA costs its issuing thread about
-//     as long to issue as a 128x128x16 MMA takes to run, so a single issuer
-//     that also waits and commits leaves the tensor pipe idle; two issuers
-//     overlap each other's waits and commits.  Each tile's P V -> Q K^T order
-//     stays within one thread, where tcgen05.mma executes in issue order, and a
-//     shared-memory lock keeps each turn's MMAs contiguous in the pipe so the
-//     two tiles alternate (one tile's softmax overlaps the other's MMAs) instead
-//     of advancing together.
+//       warp 11    TMA loads of Q, per query tile
+//     One issuing warp per query tile, run as a converged warp with an elected
+//     lane issuing each MMA (operands stay warp-uniform; the same instructions
+//     from a one-lane branch cost several times more issue time, and the pipe
+//     then starves while a turn is being issued).  Each tile's P V -> Q K^T
+//     order stays within one issuing lane, where tcgen05.mma executes in issue
+//     order.  The two issuers pass a turn token (an mbarrier each), one turn per
+//     ring item, tile 0 first, so each turn's MMAs are contiguous in the pipe
+//     and the tiles alternate: one tile's softmax overlaps the other's MMAs.
 //   * TMEM (512 columns x 128 lanes): S_t at column 128 t (128 fp32 columns),
 //     O_t at column 256 + D t.  P_t (16-bit, two per column) is written over the
 //     first 64 columns of S_t and read by the P V MMA straight from TMEM.
@@ -60,7 +61,7 @@ namespace eca {
 constexpr int kBlockM = 128;            // query rows per tile (one per TMEM lane)
 constexpr int kBlockN = 128;            // keys per K/V tile
 constexpr int kSubTileBytes = 128 * 128;  // 128 rows x 64 16-bit elements (one 128-B swizzle span)
-constexpr int kThreads = 352;
+constexpr int kThreads = 384;
 constexpr int kTmemCols = 512;
 constexpr float kMaxRowSum = 32768.0f;  // bound on sum_j p_ij that keeps every p in fp16 range
 
@@ -104,17 +105,18 @@ struct FwdSmem {
   static constexpr int kOutOff = kRingOff + kStages * kStageBytes;
   static constexpr int kBarOff = kOutOff + 2 * kStageOutBytes;
   // barrier indices
-  static constexpr int kBarQFull = 0;
-  static constexpr int kBarQFree = 1;                // two arrivals: both issuers
-  static constexpr int kBarFull = 2;
+  static constexpr int kBarQFull = 0;                // + t: Q of tile t loaded
+  static constexpr int kBarQFree = 2;                // + t: issuer t's last Q K^T of the unit done
+  static constexpr int kBarFull = 4;
   static constexpr int kBarEmpty = kBarFull + kStages;  // two arrivals: both issuers
   static constexpr int kBarS = kBarEmpty + kStages;  // + t: S_t computed
   static constexpr int kBarP = kBarS + 2;            // + t: P_t written (and O_t rescaled)
   static constexpr int kBarO = kBarP + 2;            // + t: last P V of the unit done
   static constexpr int kBarOFree = kBarO + 2;        // + t: epilogue has read O_t
   static constexpr int kBarDrain = kBarOFree + 2;    // + t: issuer t's MMAs all done
-  static constexpr int kNumBars = kBarDrain + 2;
-  static constexpr int kMiscOff = kBarOff + kNumBars * 8;  // TMEM base, abort flag, issue lock
+  static constexpr int kBarTurn = kBarDrain + 2;    // + t: issuer t may put its next turn into the pipe
+  static constexpr int kNumBars = kBarTurn + 2;
+  static constexpr int kMiscOff = kBarOff + kNumBars * 8;  // TMEM base, abort flag
   static constexpr int kBytes = kMiscOff + 16;
   static constexpr int kDynamicBytes = kBytes + 1024;  // slack for 1024-B alignment
   static_assert(kDynamicBytes <= 227 * 1024, "shared memory exceeds the per-block limit");
@@ -169,7 +171,7 @@ __device__ __forceinline__ void issue_qk(uint32_t s_tmem, uint64_t q_desc, uint6
 #pragma unroll
   for (int kk = 0; kk < D / 16; ++kk) {
     const uint64_t off = static_cast<uint64_t>((kk / 4) * (kSubTileBytes >> 4) + (kk % 4) * 2);
-    mma_ss(s_tmem, q_desc + off, k_desc + off, idesc, kk > 0 ? 1u : 0u);
+    mma_ss_warp(s_tmem, q_desc + off, k_desc + off, idesc, kk > 0 ? 1u : 0u);
   }
 }
 
@@ -180,7 +182,7 @@ __device__ __forceinline__ void issue_pv(uint32_t o_tmem, uint32_t p_tmem, uint6
   constexpr uint32_t idesc = idesc_f16_f32acc(kBlockM, D, BF16, true);
 #pragma unroll
   for (int kk = 0; kk < kBlockN / 16; ++kk) {
-    mma_ts(o_tmem, p_tmem + kk * 8, v_desc + static_cast<uint64_t>(kk * (2048 >> 4)), idesc,
+    mma_ts_warp(o_tmem, p_tmem + kk * 8, v_desc + static_cast<uint64_t>(kk * (2048 >> 4)), idesc,
            (accumulate || kk > 0) ? 1u : 0u);
   }
 }
@@ -200,14 +202,17 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto bar = [&](int i) -> uint32_t { return sbase + L::kBarOff + 8u * static_cast<uint32_t>(i); };
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kMiscOff);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kMiscOff + 4);
-  int* issue_lock = reinterpret_cast<int*>(smem + L::kMiscOff + 8);
 
-  const int warp = threadIdx.x / 32;
+  // Broadcast from lane 0 so the compiler sees the role index (and the TMEM base
+  // below) as warp-uniform.
+  const int warp = __shfl_sync(0xffffffffu, static_cast<int>(threadIdx.x / 32), 0);
   const int lane = threadIdx.x % 32;
 
   if (threadIdx.x == 0) {
-    mbar_init(bar(L::kBarQFull), 1);
-    mbar_init(bar(L::kBarQFree), 2);
+    for (int t = 0; t < 2; ++t) {
+      mbar_init(bar(L::kBarQFull + t), 1);
+      mbar_init(bar(L::kBarQFree + t), 1);
+    }
     for (int s = 0; s < L::kStages; ++s) {
       mbar_init(bar(L::kBarFull + s), 1);
       mbar_init(bar(L::kBarEmpty + s), 2);
@@ -218,9 +223,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(bar(L::kBarO + t), 1);
       mbar_init(bar(L::kBarOFree + t), 4);
       mbar_init(bar(L::kBarDrain + t), 1);
+      mbar_init(bar(L::kBarTurn + t), 1);
     }
+    mbar_arrive(bar(L::kBarTurn + 0));  // issuer 0 takes the first turn
     *abort_flag = 0;
-    *issue_lock = 0;
     fence_barrier_init();
   }
   if (warp == 9) {
@@ -230,34 +236,20 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_before_sync();
   __syncthreads();
   tc_fence_after_sync();
-  const uint32_t tmem = *tmem_slot;
+  const uint32_t tmem = __shfl_sync(0xffffffffu, *tmem_slot, 0);
   const Watchdog wd{abort_flag, p.status, p.wait_limit_ns, p.timeout_code};
 
   if (warp == 8) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
-      tma_prefetch_map(&tm_q);
       tma_prefetch_map(&tm_k);
       tma_prefetch_map(&tm_v);
-      const uint64_t pol_q = policy_evict_first();
       const uint64_t pol_kv = policy_evict_last();
       int it = 0;      // ring items issued
-      int units = 0;   // Q loads issued
       bool ok = true;
       Unit w;
       for (int k = 0; ok && unit_at(k, p, w); ++k) {
         if (w.n_max == 0) continue;  // a key segment past this pair's last key tile
-        // The Q buffer is reused: wait until both issuers' last Q K^T of the previous unit is done.
-        if (units > 0 && !wd.wait(bar(L::kBarQFree), parity(units - 1))) break;
-        const int nq = w.n_kv1 > 0 ? 2 : 1;
-        mbar_arrive_expect_tx(bar(L::kBarQFull), nq * L::kTileBytes);
-        for (int t = 0; t < nq; ++t) {
-          for (int s = 0; s < L::kSub; ++s) {
-            tma_load_3d(sbase + L::kQOff + t * L::kTileBytes + s * kSubTileBytes, &tm_q,
-                        bar(L::kBarQFull), 64 * s, (w.tile0 + t) * kBlockM, w.bh, pol_q);
-          }
-        }
-        ++units;
         // Items i = 0 .. n_max: {V_(i-1) if i > 0, K_i if i < n_max}.
         for (int i = 0; i <= w.n_max; ++i) {
           const int slot = it % L::kStages;
@@ -281,14 +273,47 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       // Let every copy this thread started land before the block can exit.
-      if (units > 0) wd.drain(bar(L::kBarQFull), parity(units - 1));
       for (int x = (it > L::kStages ? it - L::kStages : 0); x < it; ++x) {
         wd.drain(bar(L::kBarFull + x % L::kStages), parity(x / L::kStages));
       }
     }
+  } else if (warp == 11) {
+    // ------------------------------------------------------ Q loader, per query tile
+    // Each tile's Q buffer is refilled as soon as that tile's last Q K^T of the
+    // unit is done, so a tile that finishes first starts its next unit without
+    // waiting for the other.
+    if (lane == 0) {
+      tma_prefetch_map(&tm_q);
+      const uint64_t pol_q = policy_evict_first();
+      int loads[2] = {0, 0};
+      bool ok = true;
+      Unit w;
+      for (int k = 0; ok && unit_at(k, p, w); ++k) {
+        for (int t = 0; t < 2; ++t) {
+          if ((t ? w.n_kv1 : w.n_kv0) == 0) continue;
+          if (loads[t] > 0 && !wd.wait(bar(L::kBarQFree + t), parity(loads[t] - 1))) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(bar(L::kBarQFull + t), L::kTileBytes);
+          for (int s = 0; s < L::kSub; ++s) {
+            tma_load_3d(sbase + L::kQOff + t * L::kTileBytes + s * kSubTileBytes, &tm_q, bar(L::kBarQFull + t),
+                        64 * s, (w.tile0 + t) * kBlockM, w.bh, pol_q);
+          }
+          ++loads[t];
+        }
+      }
+      // Let every copy this thread started land before the block can exit.
+      for (int t = 0; t < 2; ++t) {
+        if (loads[t] > 0) wd.drain(bar(L::kBarQFull + t), parity(loads[t] - 1));
+      }
+    }
   } else if (warp >= 9) {
     // ------------------------------------------------- MMA issuer of query tile t
-    if (lane == 0) {
+    // The whole warp runs this loop: waits are taken by every lane and decided by
+    // a vote, descriptors are warp-uniform, and one elected lane issues each MMA
+    // and commit.
+    {
       const int t = warp - 9;
       const uint32_t s_tmem = tmem + 128u * t;                           // S_t, and P_t over it
       const uint32_t o_tmem = tmem + 256u + static_cast<uint32_t>(D) * t;  // O_t
@@ -298,24 +323,22 @@ __global__ void __launch_bounds__(kThreads, 1)
       auto stage_off = [&](int item) {  // stage offset in the descriptors' >>4 address field
         return static_cast<uint64_t>((item % L::kStages) * (L::kStageBytes >> 4));
       };
-      // One issuer at a time puts its turn's MMAs into the pipe.
-      auto lock = [&]() -> bool {
-        if (atomicCAS_block(issue_lock, 0, 1) == 0) return true;
-        const uint64_t t0 = global_timer_ns();
-        while (atomicCAS_block(issue_lock, 0, 1) != 0) {
-          if (wd.aborted()) return false;
-          if (global_timer_ns() - t0 > wd.limit_ns) {
-            wd.fire();
-            return false;
-          }
-        }
-        return true;
+      auto warp_wait = [&](uint32_t b, uint32_t ph) -> bool {
+        return __all_sync(0xffffffffu, wd.wait(b, ph)) != 0;
       };
-      auto unlock = [&]() { atomicExch_block(issue_lock, 0); };
+      // The issuers take turns, one per ring item each, tile 0 first: a turn's
+      // MMAs stay contiguous in the pipe, so one tile's MMAs run while the other
+      // tile's softmax works.
+      int turns = 0;
+      auto take_turn = [&]() -> bool { return warp_wait(bar(L::kBarTurn + t), parity(turns++)); };
+      auto pass_turn = [&]() {
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(L::kBarTurn + (1 - t)));
+      };
       int it = 0;       // ring items consumed
       int p_waits = 0;  // P_t handshakes consumed
       int used = 0;     // earlier units in which tile t existed (its O_t is read by an epilogue)
-      int units = 0;    // units with work, in the producer's Q-load order
+      int q_loads = 0;  // Q loads of tile t consumed
       bool ok = true;
       Unit w;
       for (int k = 0; ok && unit_at(k, p, w); ++k) {
@@ -323,61 +346,63 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int n_kv = t ? w.n_kv1 : w.n_kv0;
         // Item 0 (K_0).  Every item is waited for and released by both issuers,
         // whether or not this tile uses it, so the ring's two-arrival phases stay aligned.
-        if (!wd.wait(bar(L::kBarQFull), parity(units++)) ||
-            !wd.wait(bar(L::kBarFull + it % L::kStages), parity(it / L::kStages))) {
+        if ((n_kv > 0 && !warp_wait(bar(L::kBarQFull + t), parity(q_loads++))) ||
+            !warp_wait(bar(L::kBarFull + it % L::kStages), parity(it / L::kStages))) {
           ok = false;
           break;
         }
         tc_fence_after_sync();
-        if (n_kv > 0) {
-          if (!lock()) {
-            ok = false;
-            break;
-          }
-          issue_qk<D, BF16>(s_tmem, q_desc, ring_k_desc + stage_off(it));
-          unlock();
-          tc_commit(bar(L::kBarS + t));
+        if (!take_turn()) {
+          ok = false;
+          break;
         }
-        if (n_kv <= 1) tc_commit(bar(L::kBarQFree));  // this tile's Q K^T are all issued
-        tc_commit(bar(L::kBarEmpty + it % L::kStages));
+        if (n_kv > 0) issue_qk<D, BF16>(s_tmem, q_desc, ring_k_desc + stage_off(it));
+        pass_turn();
+        if (n_kv > 0) tc_commit_warp(bar(L::kBarS + t));
+        if (n_kv == 1) tc_commit_warp(bar(L::kBarQFree + t));  // this tile's Q K^T are all issued
+        tc_commit_warp(bar(L::kBarEmpty + it % L::kStages));
         ++it;
         for (int j = 0; j < w.n_max; ++j, ++it) {
-          if (!wd.wait(bar(L::kBarFull + it % L::kStages), parity(it / L::kStages))) {
+          if (!warp_wait(bar(L::kBarFull + it % L::kStages), parity(it / L::kStages))) {
             ok = false;
             break;
           }
           if (j < n_kv) {
             // O_t is overwritten by the first P V of a unit: the previous epilogue must have read it.
-            if (j == 0 && used > 0 && !wd.wait(bar(L::kBarOFree + t), parity(used - 1))) {
+            if (j == 0 && used > 0 && !warp_wait(bar(L::kBarOFree + t), parity(used - 1))) {
               ok = false;
               break;
             }
-            if (!wd.wait(bar(L::kBarP + t), parity(p_waits))) {
+            if (!warp_wait(bar(L::kBarP + t), parity(p_waits))) {
               ok = false;
               break;
             }
             ++p_waits;
             tc_fence_after_sync();
-            if (!lock()) {
-              ok = false;
-              break;
-            }
+          }
+          if (!take_turn()) {
+            ok = false;
+            break;
+          }
+          if (j < n_kv) {
             issue_pv<D, BF16>(o_tmem, s_tmem, ring_v_desc + stage_off(it), j > 0);
             if (j + 1 < n_kv) issue_qk<D, BF16>(s_tmem, q_desc, ring_k_desc + stage_off(it));
-            unlock();
+          }
+          pass_turn();
+          if (j < n_kv) {
             if (j + 1 < n_kv) {
-              tc_commit(bar(L::kBarS + t));
-              if (j + 2 == n_kv) tc_commit(bar(L::kBarQFree));
+              tc_commit_warp(bar(L::kBarS + t));
+              if (j + 2 == n_kv) tc_commit_warp(bar(L::kBarQFree + t));
             } else {
-              tc_commit(bar(L::kBarO + t));
+              tc_commit_warp(bar(L::kBarO + t));
             }
           }
-          tc_commit(bar(L::kBarEmpty + it % L::kStages));
+          tc_commit_warp(bar(L::kBarEmpty + it % L::kStages));
         }
         used += n_kv > 0 ? 1 : 0;
       }
       // Every MMA issued above must finish before TMEM is released.
-      tc_commit(bar(L::kBarDrain + t));
+      tc_commit_warp(bar(L::kBarDrain + t));
       wd.drain(bar(L::kBarDrain + t), 0);
     }
   } else {

@@ -189,34 +189,47 @@ __device__ __forceinline__ void tmem_wait_st() {
   asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 
-// Arrive (once) on `bar` when every tcgen05.mma issued so far by this thread is done.
-__device__ __forceinline__ void tc_commit(uint32_t bar) {
-  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
-                   bar)
-               : "memory");
+// The MMA and commit helpers below are warp-collective: the whole warp executes
+// them with warp-uniform operands and `elect.sync` picks the one lane that
+// issues the instruction.  For a fully active warp the same lane is elected
+// every time, so a commit tracks the MMAs issued before it.  Issued this way
+// from a converged warp, an MMA costs its warp a fraction of what the same
+// instruction costs from a one-lane branch.
+
+// Arrive (once) on `bar` when every tcgen05.mma issued so far by the elected lane is done.
+__device__ __forceinline__ void tc_commit_warp(uint32_t bar) {
+  asm volatile(
+      "{\n"
+      "  .reg .pred e;\n"
+      "  elect.sync _|e, 0xffffffff;\n"
+      "  @e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n"
+      "}\n" ::"r"(bar)
+      : "memory");
 }
 
 // D[tmem] (+)= A[smem] * B[smem]^T-by-descriptor.
-__device__ __forceinline__ void mma_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
-                                       uint32_t idesc, uint32_t accumulate) {
+__device__ __forceinline__ void mma_ss_warp(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                            uint32_t idesc, uint32_t accumulate) {
   asm volatile(
       "{\n"
-      "  .reg .pred p;\n"
+      "  .reg .pred p, e;\n"
+      "  elect.sync _|e, 0xffffffff;\n"
       "  setp.ne.b32 p, %4, 0;\n"
-      "  tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n"
+      "  @e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n"
       "}\n" ::"r"(d_tmem),
       "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
 
 // D[tmem] (+)= A[tmem] * B[smem].
-__device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
-                                       uint32_t idesc, uint32_t accumulate) {
+__device__ __forceinline__ void mma_ts_warp(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                            uint32_t idesc, uint32_t accumulate) {
   asm volatile(
       "{\n"
-      "  .reg .pred p;\n"
+      "  .reg .pred p, e;\n"
+      "  elect.sync _|e, 0xffffffff;\n"
       "  setp.ne.b32 p, %4, 0;\n"
-      "  tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n"
+      "  @e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n"
       "}\n" ::"r"(d_tmem),
       "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
       : "memory");
