@@ -45,11 +45,15 @@
 //   * exp is computed as 2^(s * scale * log2 e - m) with the MUFU ex2.
 //   * stale reference max: o and l share one reference m, and any reference
 //     gives the same O and lse (exact algebra), so p is formed against the
-//     current reference without first taking the new tile's row max.  The row
-//     sum bounds every p of the row, so a sum of at most 2^15 proves that no p
-//     overflows the 16-bit P; only the first key tile of a unit and the rare
-//     rows whose sum exceeds the bound take the row max, move the reference
-//     (rescaling O and l) and redo the tile from S, still intact in TMEM.
+//     current reference without first taking the new tile's row max.  No p may
+//     overflow the 16-bit P: a sum of at most 2^15 over keys 0-63 bounds each of
+//     their p, and a max score of keys 64-127 at most 15 above the reference
+//     bounds theirs.  Only the first key tile of a unit and the rare rows that
+//     fail a check take the row max, move the reference (rescaling O and l) and
+//     redo the tile from S, still intact in TMEM.
+//   * P reaches the issuer in two halves: the P V MMAs of keys 0-63 run while
+//     the softmax exponentiates keys 64-127 (whose S columns it loaded while
+//     exponentiating keys 0-63).
 #pragma once
 #include <cuda.h>
 #include <cstdint>
@@ -110,8 +114,9 @@ struct FwdSmem {
   static constexpr int kBarFull = 4;
   static constexpr int kBarEmpty = kBarFull + kStages;  // two arrivals: both issuers
   static constexpr int kBarS = kBarEmpty + kStages;  // + t: S_t computed
-  static constexpr int kBarP = kBarS + 2;            // + t: P_t written (and O_t rescaled)
-  static constexpr int kBarO = kBarP + 2;            // + t: last P V of the unit done
+  static constexpr int kBarPa = kBarS + 2;           // + t: P_t of keys 0-63 written (and O_t rescaled)
+  static constexpr int kBarPb = kBarPa + 2;          // + t: P_t of keys 64-127 written
+  static constexpr int kBarO = kBarPb + 2;           // + t: last P V of the unit done
   static constexpr int kBarOFree = kBarO + 2;        // + t: epilogue has read O_t
   static constexpr int kBarDrain = kBarOFree + 2;    // + t: issuer t's MMAs all done
   static constexpr int kBarTurn = kBarDrain + 2;    // + t: issuer t may put its next turn into the pipe
@@ -178,10 +183,11 @@ __device__ __forceinline__ void issue_qk(uint32_t s_tmem, uint64_t q_desc, uint6
 // O (+)= P V: A = P from TMEM (16 keys = 8 columns per step), B = V (MN-major,
 // 16 keys = 16 rows of 128 B = 2048 B per step, 64-column blocks 16 KB apart).
 template <int D, bool BF16>
-__device__ __forceinline__ void issue_pv(uint32_t o_tmem, uint32_t p_tmem, uint64_t v_desc, bool accumulate) {
+__device__ __forceinline__ void issue_pv(uint32_t o_tmem, uint32_t p_tmem, uint64_t v_desc, bool accumulate, int k0 = 0,
+                                         int k1 = kBlockN / 16) {
   constexpr uint32_t idesc = idesc_f16_f32acc(kBlockM, D, BF16, true);
 #pragma unroll
-  for (int kk = 0; kk < kBlockN / 16; ++kk) {
+  for (int kk = k0; kk < k1; ++kk) {
     mma_ts_warp(o_tmem, p_tmem + kk * 8, v_desc + static_cast<uint64_t>(kk * (2048 >> 4)), idesc,
            (accumulate || kk > 0) ? 1u : 0u);
   }
@@ -219,7 +225,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int t = 0; t < 2; ++t) {
       mbar_init(bar(L::kBarS + t), 1);
-      mbar_init(bar(L::kBarP + t), 4);
+      mbar_init(bar(L::kBarPa + t), 4);
+      mbar_init(bar(L::kBarPb + t), 4);
       mbar_init(bar(L::kBarO + t), 1);
       mbar_init(bar(L::kBarOFree + t), 4);
       mbar_init(bar(L::kBarDrain + t), 1);
@@ -373,7 +380,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               ok = false;
               break;
             }
-            if (!warp_wait(bar(L::kBarP + t), parity(p_waits))) {
+            if (!warp_wait(bar(L::kBarPa + t), parity(p_waits))) {
               ok = false;
               break;
             }
@@ -385,7 +392,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             break;
           }
           if (j < n_kv) {
-            issue_pv<D, BF16>(o_tmem, s_tmem, ring_v_desc + stage_off(it), j > 0);
+            // P V of keys 0-63 goes in while the softmax still works on keys 64-127.
+            issue_pv<D, BF16>(o_tmem, s_tmem, ring_v_desc + stage_off(it), j > 0, 0, 4);
+            if (!warp_wait(bar(L::kBarPb + t), parity(p_waits - 1))) {
+              ok = false;
+              break;
+            }
+            tc_fence_after_sync();
+            issue_pv<D, BF16>(o_tmem, s_tmem, ring_v_desc + stage_off(it), true, 4, 8);
             if (j + 1 < n_kv) issue_qk<D, BF16>(s_tmem, q_desc, ring_k_desc + stage_off(it));
           }
           pass_turn();
@@ -512,10 +526,39 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int a = 0; a < 8; ++a) acc[a] = make_float2(0.f, 0.f);
             exp_quarters(0, 2, -m_ref, acc);
+            const float sum_a = row_total(acc);
             tmem_wait_ld_x32(s[2]);
             tmem_wait_ld_x32(s[3]);
-            exp_quarters(2, 4, -m_ref, acc);
-            row_sum = row_total(acc);
+            float mx[2] = {-INFINITY, -INFINITY};
+#pragma unroll
+            for (int i = 0; i < 32; i += 2) {
+              mx[0] = fmax3(mx[0], __uint_as_float(s[2][i]), __uint_as_float(s[2][i + 1]));
+              mx[1] = fmax3(mx[1], __uint_as_float(s[3][i]), __uint_as_float(s[3][i + 1]));
+            }
+            // Keys 0-63 are handed over before keys 64-127 are exponentiated, so the
+            // reference must hold for the whole row now: keys 0-63 are safe when
+            // their sum of p is at most the bound, keys 64-127 when their max score
+            // is at most log2(bound) = 15 above the reference.
+            const bool fast = sum_a <= kMaxRowSum && fmaxf(mx[0], mx[1]) * c - m_ref <= 15.f;
+            if (__all_sync(0xffffffffu, fast)) {
+              tmem_st_x32(t_s, pk[0]);
+              tmem_wait_st();
+              tc_fence_before_sync();
+              __syncwarp();
+              if (lane == 0) mbar_arrive(bar(L::kBarPa + t));
+#pragma unroll
+              for (int a = 0; a < 8; ++a) acc[a] = make_float2(0.f, 0.f);
+              exp_quarters(2, 4, -m_ref, acc);
+              tmem_st_x32(t_s + 32u, pk[1]);
+              tmem_wait_st();
+              tc_fence_before_sync();
+              __syncwarp();
+              if (lane == 0) mbar_arrive(bar(L::kBarPb + t));
+              l += sum_a + row_total(acc);
+              continue;
+            }
+            load_scores();
+            row_sum = exponentiate(-m_ref);
           }
           move = !(row_sum <= kMaxRowSum);  // also true for an overflowed (inf) sum
         }
@@ -561,7 +604,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_wait_st();
         tc_fence_before_sync();
         __syncwarp();
-        if (lane == 0) mbar_arrive(bar(L::kBarP + t));
+        if (lane == 0) {
+          mbar_arrive(bar(L::kBarPa + t));
+          mbar_arrive(bar(L::kBarPb + t));
+        }
       }
       if (!ok || !warp_wait(bar(L::kBarO + t), parity(o_waits))) {
         ok = false;
