@@ -58,13 +58,16 @@ def measured_peaks():
     return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
 
 
+# Sources that define the attention kernel measured by the roofline line.
+KERNEL_SOURCES = ("attn_fwd_kernel.cuh", "ptx.cuh", "tmem_ldst.cuh")
+
+
 def kernel_source_hash():
     csrc = os.path.join(ROOT, "exact_causal_attention_gb300", "csrc")
     h = hashlib.sha256()
-    for name in sorted(os.listdir(csrc)):
-        if name.endswith((".cu", ".cuh")):
-            with open(os.path.join(csrc, name), "rb") as f:
-                h.update(name.encode() + f.read())
+    for name in KERNEL_SOURCES:
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(name.encode() + f.read())
     return h.hexdigest()[:16]
 
 

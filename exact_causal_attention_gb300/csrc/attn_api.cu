@@ -6,7 +6,9 @@
 #include <cmath>
 #include <cstdint>
 #include <cstring>
+#include <algorithm>
 #include <mutex>
+#include <vector>
 
 #include "attn.h"
 #include "attn_fwd_kernel.cuh"
@@ -153,6 +155,58 @@ KeySplit key_split(int N, int requested) {
   const int r = requested < 1 ? 1 : (requested > n_tiles ? n_tiles : requested);
   const int seg = (n_tiles + r - 1) / r;
   return KeySplit{seg, (n_tiles + seg - 1) / seg};
+}
+
+// Split count with the shortest predicted time, from a replay of the kernel's
+// static schedule: unit l goes to CTA (l mod G) or (G - 1 - l mod G) in
+// alternate waves, a unit costs the longer of its two tiles' key-tile counts
+// plus a fixed start/end cost, and a split adds the merge kernel's traffic.
+// The constants are rough (a key tile of both query tiles is about 1.2 us on a
+// busy SM, a unit boundary about three of those, the merge about 4 TB/s); only
+// their ratios matter.  Without a shortage of units the answer is 1.
+int predicted_best_splits(int B, int H, int N, int D, int sm_count) {
+  const int n_tiles = (N + eca::kBlockN - 1) / eca::kBlockN;
+  const int n_pairs = (n_tiles + 1) / 2;
+  const long long bh = static_cast<long long>(B) * H;
+  if (static_cast<long long>(n_pairs) * bh >= 2LL * sm_count) return 1;
+  constexpr double kStepUs = 1.2, kUnitSteps = 3.0, kMergeBytesPerUs = 4.0e6, kMergeFixedUs = 4.0;
+  const int G = sm_count;
+  std::vector<double> load(static_cast<size_t>(G));
+  int best = 1;
+  double best_t = 0.0;
+  int last_eff = 0;
+  for (int req = 1; req <= kMaxSplits && req <= n_tiles; ++req) {
+    const KeySplit ks = key_split(N, req);
+    if (ks.splits == last_eff) continue;  // same segmentation as a smaller request
+    last_eff = ks.splits;
+    std::fill(load.begin(), load.end(), 0.0);
+    const long long n_units = static_cast<long long>(n_pairs) * bh * ks.splits;
+    for (long long l = 0; l < n_units; ++l) {
+      const long long k = l / G, pos = l % G;
+      const int c = static_cast<int>((k & 1) ? G - 1 - pos : pos);
+      const int seg = static_cast<int>(l % ks.splits);
+      const int pair = n_pairs - 1 - static_cast<int>((l / ks.splits) / bh);
+      const int kv0 = seg * ks.seg_tiles;
+      const int kv_end = kv0 + ks.seg_tiles < n_tiles ? kv0 + ks.seg_tiles : n_tiles;
+      const int t0 = 2 * pair;
+      const int need0 = t0 + 1;
+      const int need1 = t0 + 1 < n_tiles ? t0 + 2 : 0;
+      const int n0 = (need0 < kv_end ? need0 : kv_end) - kv0;
+      const int n1 = (need1 < kv_end ? need1 : kv_end) - kv0;
+      const int n = n0 > n1 ? n0 : n1;
+      if (n > 0) load[static_cast<size_t>(c)] += n + kUnitSteps;
+    }
+    double t = *std::max_element(load.begin(), load.end()) * kStepUs;
+    if (ks.splits > 1) {
+      const double merge_bytes = static_cast<double>(bh) * N * D * (4.0 * ks.splits + 2.0);
+      t += merge_bytes / kMergeBytesPerUs + kMergeFixedUs;
+    }
+    if (req == 1 || t < best_t) {
+      best_t = t;
+      best = ks.splits;
+    }
+  }
+  return best;
 }
 
 uint64_t align256(uint64_t x) { return (x + 255) & ~static_cast<uint64_t>(255); }
@@ -527,13 +581,7 @@ int attn_splitkv_default_splits(int B, int H, int N, int D) {
   DeviceState* st = nullptr;
   const int r = device_state(&st);
   if (r != ATTN_OK) return r;
-  const long long n_tiles = (static_cast<long long>(N) + 127) / 128;
-  const long long units = (n_tiles + 1) / 2 * static_cast<long long>(B) * H;
-  // Enough segments for about two units per SM; never more than the key tiles.
-  long long s = (2LL * st->sm_count + units - 1) / units;
-  if (s > n_tiles) s = n_tiles;
-  if (s > kMaxSplits) s = kMaxSplits;
-  return s < 1 ? 1 : static_cast<int>(s);
+  return predicted_best_splits(B, H, N, D, st->sm_count);
 }
 
 int attn_decode_paged(const void* q, const void* cache, const int* block_table, const int* lengths, void* out,
