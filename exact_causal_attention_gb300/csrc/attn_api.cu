@@ -6,8 +6,9 @@
 #include <cmath>
 #include <cstdint>
 #include <cstring>
-#include <algorithm>
+#include <functional>
 #include <mutex>
+#include <queue>
 #include <vector>
 
 #include "attn.h"
@@ -31,6 +32,13 @@ constexpr unsigned long long kWaitLimitNs = 2000000000ull;  // 2 s per single wa
 // Device status word: 0, or the code of the last bounded wait that gave up.
 __device__ int g_device_status = 0;
 
+// Work counters of the attention kernel, one 256-byte slot per launch, taken in
+// turn: a launch hands its units out from slot[0] and counts finished CTAs in
+// slot[32]; its last CTA sets both back to zero.  64 slots let up to 64 launches
+// run at once (on different streams) without sharing one.
+constexpr int kSchedSlots = 64;
+__device__ int g_sched_pool[kSchedSlots * 64] = {};
+
 using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
                                    const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
                                    const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
@@ -42,6 +50,8 @@ struct DeviceState {
   int sm_count = 0;
   int* status = nullptr;    // address of g_device_status on this device
   void* scratch = nullptr;  // address of g_splitkv_scratch on this device, set by its first use
+  int* sched_pool = nullptr;  // address of g_sched_pool on this device
+  unsigned sched_next = 0;    // slot of the next attention launch
   unsigned configured = 0;  // bitmask of kernel instantiations with smem attribute set
   unsigned configured_decode = 0;
 };
@@ -85,6 +95,8 @@ int device_state(DeviceState** out) {
       void* addr = nullptr;
       if (cudaGetSymbolAddress(&addr, g_device_status) != cudaSuccess) return ATTN_ERR_CUDA;
       st.status = static_cast<int*>(addr);
+      if (cudaGetSymbolAddress(&addr, g_sched_pool) != cudaSuccess) return ATTN_ERR_CUDA;
+      st.sched_pool = static_cast<int*>(addr);
     }
     st.probed = true;
   }
@@ -157,21 +169,34 @@ KeySplit key_split(int N, int requested) {
   return KeySplit{seg, (n_tiles + seg - 1) / seg};
 }
 
+// Slices per group of the kernel's unit order: the smallest whole number of
+// query heads sharing K/V heads that divides B*H and gives a group at least 1.5
+// SMs' worth of units.  Small groups keep the CTAs' concurrent K/V reads within
+// a few heads (so they stay in L2); equal groups of that size keep the
+// heaviest-first order within each group enough to end the launch evenly.  When
+// all of K and V fit in L2 anyway (64 MiB or less), one group.
+int unit_group_heads(int BH, int q_per_kv, int units_per_slice, int sm_count, unsigned long long kv_bytes) {
+  if (kv_bytes <= (64ull << 20)) return BH;
+  const double target = 1.5 * sm_count / units_per_slice;
+  for (int g = q_per_kv; g < BH; g += q_per_kv) {
+    if (BH % g == 0 && g >= target) return g;
+  }
+  return BH;
+}
+
 // Split count with the shortest predicted time, from a replay of the kernel's
-// static schedule: unit l goes to CTA (l mod G) or (G - 1 - l mod G) in
-// alternate waves, a unit costs the longer of its two tiles' key-tile counts
-// plus a fixed start/end cost, and a split adds the merge kernel's traffic.
-// The constants are rough (a key tile of both query tiles is about 1.2 us on a
-// busy SM, a unit boundary about three of those, the merge about 4 TB/s); only
-// their ratios matter.  Without a shortage of units the answer is 1.
+// schedule: units are taken in launch order by whichever CTA is free first, a
+// unit costs the longer of its two tiles' key-tile counts plus a fixed
+// start/end cost, and a split adds the merge kernel's traffic.  The constants
+// are rough (a key tile of both query tiles is about 1.2 us on a busy SM, a
+// unit boundary about three of those, the merge about 4 TB/s); only their
+// ratios matter.  Without a shortage of units the answer is 1.
 int predicted_best_splits(int B, int H, int N, int D, int sm_count) {
   const int n_tiles = (N + eca::kBlockN - 1) / eca::kBlockN;
   const int n_pairs = (n_tiles + 1) / 2;
   const long long bh = static_cast<long long>(B) * H;
   if (static_cast<long long>(n_pairs) * bh >= 2LL * sm_count) return 1;
   constexpr double kStepUs = 1.2, kUnitSteps = 3.0, kMergeBytesPerUs = 4.0e6, kMergeFixedUs = 4.0;
-  const int G = sm_count;
-  std::vector<double> load(static_cast<size_t>(G));
   int best = 1;
   double best_t = 0.0;
   int last_eff = 0;
@@ -179,24 +204,30 @@ int predicted_best_splits(int B, int H, int N, int D, int sm_count) {
     const KeySplit ks = key_split(N, req);
     if (ks.splits == last_eff) continue;  // same segmentation as a smaller request
     last_eff = ks.splits;
-    std::fill(load.begin(), load.end(), 0.0);
-    const long long n_units = static_cast<long long>(n_pairs) * bh * ks.splits;
-    for (long long l = 0; l < n_units; ++l) {
-      const long long k = l / G, pos = l % G;
-      const int c = static_cast<int>((k & 1) ? G - 1 - pos : pos);
-      const int seg = static_cast<int>(l % ks.splits);
-      const int pair = n_pairs - 1 - static_cast<int>((l / ks.splits) / bh);
-      const int kv0 = seg * ks.seg_tiles;
-      const int kv_end = kv0 + ks.seg_tiles < n_tiles ? kv0 + ks.seg_tiles : n_tiles;
-      const int t0 = 2 * pair;
-      const int need0 = t0 + 1;
-      const int need1 = t0 + 1 < n_tiles ? t0 + 2 : 0;
-      const int n0 = (need0 < kv_end ? need0 : kv_end) - kv0;
-      const int n1 = (need1 < kv_end ? need1 : kv_end) - kv0;
-      const int n = n0 > n1 ? n0 : n1;
-      if (n > 0) load[static_cast<size_t>(c)] += n + kUnitSteps;
+    // The order within a group of slices does not change the costs: pairs heaviest
+    // first, every slice and segment of a pair in turn.
+    std::priority_queue<double, std::vector<double>, std::greater<double>> free_at;
+    for (int c = 0; c < sm_count; ++c) free_at.push(0.0);
+    double makespan = 0.0;
+    for (int pair = n_pairs - 1; pair >= 0; --pair) {
+      for (long long x = 0; x < bh; ++x) {
+        for (int seg = 0; seg < ks.splits; ++seg) {
+          const int kv0 = seg * ks.seg_tiles;
+          const int kv_end = kv0 + ks.seg_tiles < n_tiles ? kv0 + ks.seg_tiles : n_tiles;
+          const int need0 = 2 * pair + 1;
+          const int need1 = 2 * pair + 1 < n_tiles ? 2 * pair + 2 : 0;
+          const int n0 = (need0 < kv_end ? need0 : kv_end) - kv0;
+          const int n1 = (need1 < kv_end ? need1 : kv_end) - kv0;
+          const int n = n0 > n1 ? n0 : n1;
+          if (n <= 0) continue;
+          const double t = free_at.top() + n + kUnitSteps;
+          free_at.pop();
+          free_at.push(t);
+          if (t > makespan) makespan = t;
+        }
+      }
     }
-    double t = *std::max_element(load.begin(), load.end()) * kStepUs;
+    double t = makespan * kStepUs;
     if (ks.splits > 1) {
       const double merge_bytes = static_cast<double>(bh) * N * D * (4.0 * ks.splits + 2.0);
       t += merge_bytes / kMergeBytesPerUs + kMergeFixedUs;
@@ -225,14 +256,15 @@ int launch(const void* q, const void* k, const void* v, void* o, float* lse, int
            float* part_o, float* part_lse) {
   const int BH = B * H;
   using L = eca::FwdSmem<D>;
-  auto kernel = eca::attn_fwd_kernel<D, BF16>;
-  const unsigned bit = 1u << ((D == 128 ? 2 : 0) + (BF16 ? 1 : 0));
-  if (!(st->configured & bit)) {
-    if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kDynamicBytes) !=
-        cudaSuccess) {
+  if (!(st->configured & (1u << ((D == 128 ? 2 : 0) + (BF16 ? 1 : 0))))) {
+    // Both assignment modes of this instantiation.
+    if (cudaFuncSetAttribute(eca::attn_fwd_kernel<D, BF16, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             L::kDynamicBytes) != cudaSuccess ||
+        cudaFuncSetAttribute(eca::attn_fwd_kernel<D, BF16, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             L::kDynamicBytes) != cudaSuccess) {
       return ATTN_ERR_CUDA;
     }
-    st->configured |= bit;
+    st->configured |= 1u << ((D == 128 ? 2 : 0) + (BF16 ? 1 : 0));
   }
   CUtensorMap tq, tk, tv, to;
   int rc = encode_qkv_map(encode, &tq, q, BF16, D, N, BH);
@@ -257,13 +289,21 @@ int launch(const void* q, const void* k, const void* v, void* o, float* lse, int
   p.splits = ks.splits;
   p.seg_tiles = ks.seg_tiles;
   p.n_units = p.n_pairs * BH * ks.splits;
+  const unsigned long long kv_bytes = 4ull * static_cast<unsigned long long>(B) * Hkv * N * D;  // K and V, 16-bit
+  p.group_heads = unit_group_heads(BH, H / Hkv, p.n_pairs * ks.splits, st->sm_count, kv_bytes);
+  const bool dynamic = p.group_heads < BH;
+  p.sched = st->sched_pool + 64 * (st->sched_next++ % kSchedSlots);
   p.causal = causal ? 1 : 0;
   p.scale_log2e = scale * 1.4426950408889634f;
   p.wait_limit_ns = kWaitLimitNs;
   p.timeout_code = ATTN_ERR_TIMEOUT;
   // Persistent: one CTA per SM (the shared-memory footprint admits only one), never more than the units.
   const unsigned grid = static_cast<unsigned>(p.n_units < st->sm_count ? p.n_units : st->sm_count);
-  kernel<<<grid, eca::kThreads, L::kDynamicBytes, stream>>>(tq, tk, tv, to, p);
+  if (dynamic) {
+    eca::attn_fwd_kernel<D, BF16, true><<<grid, eca::kThreads, L::kDynamicBytes, stream>>>(tq, tk, tv, to, p);
+  } else {
+    eca::attn_fwd_kernel<D, BF16, false><<<grid, eca::kThreads, L::kDynamicBytes, stream>>>(tq, tk, tv, to, p);
+  }
   if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_LAUNCH;
   if (part_o == nullptr) return ATTN_OK;
 

@@ -12,11 +12,14 @@
 //
 // GB300 mapping (differs from the page's mma.sync / cp.async design):
 //   * persistent CTAs, one per SM; a work unit is two consecutive 128-row query
-//     tiles of one (batch, head).  Units are ordered heaviest first (causal work
-//     grows with the tile index) and dealt to the CTAs in zig-zag waves.  The
-//     next unit's Q load starts as soon as the current unit's last Q K^T MMA is
-//     done, and its first P V only waits until that tile's epilogue has read O,
-//     so unit boundaries overlap.  With a key split (long sequences, few
+//     tiles of one (batch, head).  A CTA takes the next unit of the launch from
+//     a global counter when its producer warp is ready for one, and passes the
+//     index to its other warps through a small shared-memory queue.  Units are
+//     ordered by groups of heads (so the K/V tiles in use at any time stay in
+//     L2), heaviest first within a group (causal work grows with the tile index).
+//     Each query tile's next Q load starts as soon as that tile's last Q K^T MMA
+//     is done, and its first P V only waits until that tile's epilogue has read
+//     O, so unit boundaries overlap.  With a key split (long sequences, few
 //     heads), a unit also names a segment of key tiles and its epilogue writes
 //     the segment's normalised partial output and log-sum-exp in fp32 for a
 //     separate merge ("CUDA KV Cache：分页存储与长上下文 Decode 极致优化",
@@ -25,7 +28,7 @@
 //     one group are adjacent in the unit order so their K/V tiles come from L2.
 //     384 threads:
 //       warps 0-3  softmax for query tile 0     warps 4-7  softmax for query tile 1
-//       warp 8     TMA producer of the ring items {V_j, K_j+1}
+//       warp 8     takes units; TMA producer of the ring items {V_j, K_j+1}
 //       warp 9     TMEM owner; tcgen05.mma issuer for query tile 0
 //       warp 10    tcgen05.mma issuer for query tile 1
 //       warp 11    TMA loads of Q, per query tile
@@ -68,6 +71,8 @@ constexpr int kSubTileBytes = 128 * 128;  // 128 rows x 64 16-bit elements (one 
 constexpr int kThreads = 384;
 constexpr int kTmemCols = 512;
 constexpr float kMaxRowSum = 32768.0f;  // bound on sum_j p_ij that keeps every p in fp16 range
+constexpr int kUnitQueue = 4;           // depth of the shared-memory queue of unit indices
+constexpr int kUnitReaders = 11;        // warps that read each queue entry: 8 softmax, 2 issuers, Q loader
 
 struct FwdParams {
   void* o;        // [BH, N, D] 16-bit (unused when part_o is set)
@@ -84,6 +89,8 @@ struct FwdParams {
   int splits;     // key segments (1 = no split)
   int seg_tiles;  // key tiles per segment
   int n_units;    // n_pairs * BH * splits
+  int group_heads;  // slices per group in the unit order (the last group may be smaller)
+  int* sched;     // [0]: next unit to hand out, [32]: CTAs finished; both back to 0 at exit
   int causal;
   float scale_log2e;  // scale * log2(e)
   unsigned long long wait_limit_ns;
@@ -120,9 +127,11 @@ struct FwdSmem {
   static constexpr int kBarOFree = kBarO + 2;        // + t: epilogue has read O_t
   static constexpr int kBarDrain = kBarOFree + 2;    // + t: issuer t's MMAs all done
   static constexpr int kBarTurn = kBarDrain + 2;    // + t: issuer t may put its next turn into the pipe
-  static constexpr int kNumBars = kBarTurn + 2;
-  static constexpr int kMiscOff = kBarOff + kNumBars * 8;  // TMEM base, abort flag
-  static constexpr int kBytes = kMiscOff + 16;
+  static constexpr int kBarUnitFull = kBarTurn + 2;          // + slot: queue entry written
+  static constexpr int kBarUnitFree = kBarUnitFull + kUnitQueue;  // + slot: queue entry read by every reader
+  static constexpr int kNumBars = kBarUnitFree + kUnitQueue;
+  static constexpr int kMiscOff = kBarOff + kNumBars * 8;  // TMEM base, abort flag, unit queue
+  static constexpr int kBytes = kMiscOff + 8 + 4 * kUnitQueue;
   static constexpr int kDynamicBytes = kBytes + 1024;  // slack for 1024-B alignment
   static_assert(kDynamicBytes <= 227 * 1024, "shared memory exceeds the per-block limit");
 };
@@ -139,19 +148,28 @@ struct Unit {
   int n_max;
 };
 
-// The k-th unit of this CTA (zig-zag over waves of gridDim.x units, heaviest
-// first).  False once the CTA has no more work.
-__device__ __forceinline__ bool unit_at(int k, const FwdParams& p, Unit& u) {
-  const int G = static_cast<int>(gridDim.x);
-  const int c = static_cast<int>(blockIdx.x);
-  const long long L = static_cast<long long>(k) * G + ((k & 1) ? (G - 1 - c) : c);
-  if (L >= p.n_units) return false;
-  const int l = static_cast<int>(L);
-  u.seg = l % p.splits;
-  const int r = l / p.splits;
-  u.bh = r % p.BH;
+// Unit l of the launch.  Units are handed out in increasing l to whichever CTA
+// asks next.  The order is by groups of group_heads slices (so the K/V tiles the
+// CTAs read at any time belong to a few heads and stay in L2), then heaviest
+// query-tile pair first (causal work grows with the tile index, so the light
+// units come last in every group and the launch ends evenly), then slice, then
+// key segment.
+__device__ __forceinline__ void unit_from(int l, const FwdParams& p, Unit& u) {
+  const int per_slice = p.n_pairs * p.splits;
+  const int full_groups = p.BH / p.group_heads;
+  int grp = l / (p.group_heads * per_slice);
+  int g = p.group_heads;
+  int local = l - grp * (p.group_heads * per_slice);
+  if (grp >= full_groups) {  // the smaller last group
+    grp = full_groups;
+    g = p.BH - full_groups * p.group_heads;
+    local = l - full_groups * (p.group_heads * per_slice);
+  }
+  u.seg = local % p.splits;
+  const int r = local / p.splits;
+  u.bh = grp * p.group_heads + r % g;
   u.kvh = (u.bh / p.H) * p.Hkv + (u.bh % p.H) / (p.H / p.Hkv);
-  const int pair = p.n_pairs - 1 - r / p.BH;
+  const int pair = p.n_pairs - 1 - r / g;
   u.tile0 = 2 * pair;
   u.kv0 = u.seg * p.seg_tiles;
   const int kv_end = u.kv0 + p.seg_tiles < p.n_tiles ? u.kv0 + p.seg_tiles : p.n_tiles;
@@ -164,7 +182,6 @@ __device__ __forceinline__ bool unit_at(int k, const FwdParams& p, Unit& u) {
   u.n_kv0 = e0 > u.kv0 ? e0 - u.kv0 : 0;
   u.n_kv1 = e1 > u.kv0 ? e1 - u.kv0 : 0;
   u.n_max = u.n_kv0 > u.n_kv1 ? u.n_kv0 : u.n_kv1;
-  return true;
 }
 
 // S = Q K^T: A = Q (K-major, 128-B swizzle), B = K (K-major).  Descriptors are
@@ -195,7 +212,9 @@ __device__ __forceinline__ void issue_pv(uint32_t o_tmem, uint32_t p_tmem, uint6
 
 __device__ __forceinline__ uint32_t parity(int count) { return static_cast<uint32_t>(count) & 1u; }
 
-template <int D, bool BF16>
+// kDynamic: units taken from the launch's counter and queued to the CTA's warps
+// (grouped head order); otherwise each warp follows the fixed zig-zag waves.
+template <int D, bool BF16, bool kDynamic>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
@@ -208,6 +227,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto bar = [&](int i) -> uint32_t { return sbase + L::kBarOff + 8u * static_cast<uint32_t>(i); };
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kMiscOff);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kMiscOff + 4);
+  volatile int* unit_queue = reinterpret_cast<volatile int*>(smem + L::kMiscOff + 8);
 
   // Broadcast from lane 0 so the compiler sees the role index (and the TMEM base
   // below) as warp-uniform.
@@ -232,6 +252,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(bar(L::kBarDrain + t), 1);
       mbar_init(bar(L::kBarTurn + t), 1);
     }
+    for (int q = 0; q < kUnitQueue; ++q) {
+      mbar_init(bar(L::kBarUnitFull + q), 1);
+      mbar_init(bar(L::kBarUnitFree + q), kUnitReaders);
+    }
     mbar_arrive(bar(L::kBarTurn + 0));  // issuer 0 takes the first turn
     *abort_flag = 0;
     fence_barrier_init();
@@ -245,6 +269,49 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after_sync();
   const uint32_t tmem = __shfl_sync(0xffffffffu, *tmem_slot, 0);
   const Watchdog wd{abort_flag, p.status, p.wait_limit_ns, p.timeout_code};
+  // Readers of the unit queue: entry n holds the n-th unit this CTA works on,
+  // or -1 after the last.  `read_unit` is called by a whole warp (lane 0 alone
+  // for the Q loader); it is false when a wait gave up.
+  int units_read = 0;
+  auto read_unit = [&](int& l, bool whole_warp) -> bool {
+    const int q = units_read % kUnitQueue;
+    bool got = wd.wait(bar(L::kBarUnitFull + q), parity(units_read / kUnitQueue));
+    if (whole_warp) got = __all_sync(0xffffffffu, got) != 0;
+    if (!got) return false;
+    l = unit_queue[q];
+    if (whole_warp) {
+      __syncwarp();
+      l = __reduce_max_sync(0xffffffffu, l);  // the same in every lane; warp-uniform for the compiler
+    }
+    if (lane == 0) mbar_arrive(bar(L::kBarUnitFree + q));
+    ++units_read;
+    return true;
+  };
+  // The k-th unit of this CTA under the fixed assignment: unit k G + c of wave k,
+  // the waves dealt to the CTAs in alternating directions; -1 past the last.
+  auto fixed_unit = [&](int k) -> int {
+    const int c = static_cast<int>(blockIdx.x), G = static_cast<int>(gridDim.x);
+    const long long l = static_cast<long long>(k) * G + ((k & 1) ? G - 1 - c : c);
+    return l < p.n_units ? static_cast<int>(l) : -1;
+  };
+  // Next unit with work for a role: from the fixed assignment, or from the queue
+  // under dynamic assignment.  1: got one in w; 0: no more; -1: a wait gave up.
+  int units_fixed = 0;
+  auto next_unit = [&](Unit& w, bool whole_warp) -> int {
+    if (!kDynamic) {
+      while (true) {
+        const int l = fixed_unit(units_fixed++);
+        if (l < 0) return 0;
+        unit_from(l, p, w);
+        if (w.n_max > 0) return 1;
+      }
+    }
+    int l;
+    if (!read_unit(l, whole_warp)) return -1;
+    if (l < 0) return 0;
+    unit_from(l, p, w);
+    return 1;
+  };
 
   if (warp == 8) {
     // ------------------------------------------------------------ TMA producer
@@ -253,10 +320,38 @@ __global__ void __launch_bounds__(kThreads, 1)
       tma_prefetch_map(&tm_v);
       const uint64_t pol_kv = policy_evict_last();
       int it = 0;      // ring items issued
+      int pushed = 0;  // unit queue entries written
+      auto push_unit = [&](int l) -> bool {
+        const int q = pushed % kUnitQueue;
+        if (!wd.wait(bar(L::kBarUnitFree + q), parity(pushed / kUnitQueue) ^ 1u)) return false;
+        unit_queue[q] = l;
+        mbar_arrive(bar(L::kBarUnitFull + q));
+        ++pushed;
+        return true;
+      };
+      // Under dynamic assignment this warp takes the CTA's units from the launch's
+      // counter (skipping key segments past a pair's last key tile, which have no
+      // work) when it is about to load their items, and queues them for the other
+      // warps; so a unit goes to the CTA that is free first.
+      auto take_unit = [&]() -> int {
+        while (true) {
+          const int l = atomicAdd(p.sched, 1);
+          if (l >= p.n_units) return -1;
+          Unit u;
+          unit_from(l, p, u);
+          if (u.n_max > 0) return l;
+        }
+      };
       bool ok = true;
       Unit w;
-      for (int k = 0; ok && unit_at(k, p, w); ++k) {
-        if (w.n_max == 0) continue;  // a key segment past this pair's last key tile
+      while (ok) {
+        if (kDynamic) {
+          const int l = take_unit();
+          if (!push_unit(l) || l < 0) break;
+          unit_from(l, p, w);
+        } else if (next_unit(w, false) != 1) {
+          break;
+        }
         // Items i = 0 .. n_max: {V_(i-1) if i > 0, K_i if i < n_max}.
         for (int i = 0; i <= w.n_max; ++i) {
           const int slot = it % L::kStages;
@@ -295,7 +390,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       int loads[2] = {0, 0};
       bool ok = true;
       Unit w;
-      for (int k = 0; ok && unit_at(k, p, w); ++k) {
+      while (ok && next_unit(w, false) == 1) {
         for (int t = 0; t < 2; ++t) {
           if ((t ? w.n_kv1 : w.n_kv0) == 0) continue;
           if (loads[t] > 0 && !wd.wait(bar(L::kBarQFree + t), parity(loads[t] - 1))) {
@@ -348,8 +443,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       int q_loads = 0;  // Q loads of tile t consumed
       bool ok = true;
       Unit w;
-      for (int k = 0; ok && unit_at(k, p, w); ++k) {
-        if (w.n_max == 0) continue;
+      while (ok) {
+        const int got = next_unit(w, true);
+        if (got != 1) {
+          ok = got == 0;
+          break;
+        }
         const int n_kv = t ? w.n_kv1 : w.n_kv0;
         // Item 0 (K_0).  Every item is waited for and released by both issuers,
         // whether or not this tile uses it, so the ring's two-arrival phases stay aligned.
@@ -437,7 +536,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     int s_waits = 0, o_waits = 0;
     bool ok = true;
     Unit w;
-    for (int k = 0; ok && unit_at(k, p, w); ++k) {
+    while (ok) {
+      const int got = next_unit(w, true);
+      if (got != 1) {
+        ok = got == 0;
+        break;
+      }
       const int n_kv = t ? w.n_kv1 : w.n_kv0;
       if (n_kv == 0) continue;
       const int tile = w.tile0 + t;
@@ -692,6 +796,14 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   tc_fence_before_sync();
   __syncthreads();
+  if (kDynamic && threadIdx.x == 0) {
+    // The last CTA to finish returns the launch's counters to zero for the next launch.
+    __threadfence();
+    if (atomicAdd(p.sched + 32, 1) == static_cast<int>(gridDim.x) - 1) {
+      atomicExch(p.sched, 0);
+      atomicExch(p.sched + 32, 0);
+    }
+  }
   if (warp == 9) {
     __syncwarp();
     tc_fence_after_sync();
