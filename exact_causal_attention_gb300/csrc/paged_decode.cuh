@@ -9,21 +9,23 @@
 // (section 6.3), looks a page id up once per page (section 6.1) and splits long
 // contexts into segments merged with the online-softmax law (section 6.4).
 //
-// GB300 mapping: one CTA per (request, K/V head, chunk of HC query heads of the
-// group, key segment); 128 threads.  TMA brings each page of one K/V head as a
-// (T tokens x 64 dims) box with the 128-byte swizzle into a 3-stage ring of
-// 64-token tiles; thread 0 issues the copies.  With M = HC <= 8 query rows the
-// arithmetic is far below the tensor-core shapes and the kernel is HBM-bound
-// (about 4 FLOP per byte), so scores and P V run on the FP32 pipes:
-//   scores: two threads per token row, each converting half of the K row to fp32
-//           once and using it for every head of the chunk (one shuffle joins
-//           the halves);
-//   softmax: one warp per head, lanes over the tile's tokens (shuffle reductions);
-//   P V: one thread per column pair and run of tokens, HC packed accumulators,
-//        p stored token-major so one vector load serves four heads; the runs'
-//        partial sums meet once per unit, in the ring's memory once every copy
-//        has been consumed.
-// About 73 KB of shared memory, so three CTAs share an SM.
+// GB300 mapping: one CTA per (request, K/V head, chunk of HC <= 8 query heads of
+// the group, key segment); five warps.  A producer warp issues the TMA copies:
+// each page of one K/V head as (T tokens x 64 dims) boxes with the 128-byte
+// swizzle, into a 2-stage ring of 64-token tiles, with the page ids in a rolling
+// window in shared memory and the tile's valid-row mask beside it.  Four compute
+// warps each take 16 tokens of every tile and run their own online softmax over
+// them (section 5's recurrence, per warp), merged once at the end with the
+// section 6.4 law.  The HC query heads are the rows of mma.sync m16n8k16
+// products padded to 16 (the decode is HBM-bound at a few FLOP per byte, so the
+// padding costs nothing; tcgen05 would need M >= 64):
+//   S^T-free scores: S (heads x 8 tokens) = Q (heads x 16 dims) K^T, K^T fragments
+//                    read with ldmatrix straight from the swizzled boxes, fp32
+//                    accumulation, Q fragments held in registers;
+//   softmax: the S accumulator layout is the A-operand layout of the next
+//            product, so p goes to 16 bits in registers with no shared memory;
+//   O += P V: V fragments read with ldmatrix.trans, fp32 accumulators per warp.
+// No K/V element is converted to fp32 and no block barrier is taken per tile.
 // Page and row offsets use shifts (page sizes are powers of two).
 // Page ids outside [0, P) and lengths outside [0, max_pages * T] are not read:
 // the kernel records ATTN_ERR_BAD_INDEX in the status word and treats them as
@@ -38,7 +40,8 @@ namespace eca {
 
 constexpr int kDecTile = 64;     // tokens per tile
 constexpr int kDecStages = 2;
-constexpr int kDecThreads = 128;
+constexpr int kDecWarps = 4;     // compute warps: 16 tokens of every tile each
+constexpr int kDecThreads = 32 * (kDecWarps + 1);  // and one producer warp
 constexpr int kDecIdRing = 64;  // page ids staged in shared memory, a rolling window of the segment
 
 struct DecodeParams {
@@ -63,16 +66,17 @@ struct DecodeSmem {
   static constexpr int kKindBytes = kDecTile * D * 2;  // one kind (K or V) of a tile
   static constexpr int kStageBytes = 2 * kKindBytes;
   static constexpr int kRingOff = 0;
-  static constexpr int kQOff = kDecStages * kStageBytes;           // fp32 [8][D], pre-scaled query
-  static constexpr int kSOff = kQOff + 8 * D * 4;                  // fp32 [8][64] scores
-  static constexpr int kPOff = kSOff + 8 * kDecTile * 4;           // fp32 [64][8] p, token-major
-  static constexpr int kRedOff = kRingOff;  // fp32 partial outputs (8 KB), over the ring once it is idle
-  static constexpr int kIdsOff = kPOff + kDecTile * 8 * 4;         // int32 page-id window
-  static constexpr int kStatOff = kIdsOff + kDecIdRing * 4;      // fp32 [8] alpha, [8] m, [8] l
-  static constexpr int kBarOff = kStatOff + 3 * 8 * 4;
-  static constexpr int kMiscOff = kBarOff + kDecStages * 8;        // abort flag
+  static constexpr int kRedOff = kRingOff;  // fp32 [warps][8][D] partial outputs at the end, over the idle ring
+  static constexpr int kRowsOff = kDecStages * kStageBytes;         // uint64 [stages]: valid rows of the staged tile
+  static constexpr int kIdsOff = kRowsOff + 8 * kDecStages;         // int32 page-id window
+  static constexpr int kQFragOff = kIdsOff + kDecIdRing * 4;        // uint32 [D/16][32 lanes][2] query fragments
+  static constexpr int kStatOff = kQFragOff + (D / 16) * 32 * 8;     // fp32 [warps][8] m, then [warps][8] l
+  static constexpr int kBarOff = kStatOff + 2 * kDecWarps * 8 * 4;  // full[stages], then empty[stages]
+  static constexpr int kMiscOff = kBarOff + 2 * kDecStages * 8;     // abort flag
   static constexpr int kBytes = kMiscOff + 16;
   static constexpr int kDynamicBytes = kBytes + 1024;
+  static_assert(kDecWarps * 8 * D * 4 <= kDecStages * kStageBytes, "reduction buffer fits over the ring");
+  static_assert(kBarOff % 8 == 0, "mbarriers are 8-byte aligned");
 };
 
 template <bool BF16>
@@ -102,24 +106,58 @@ __device__ __forceinline__ int dec_chunk_offset(int r, int c, int log2T) {
   return ((box * T + rr) << 7) + (((c & 7) ^ (rr & 7)) << 4);
 }
 
+// Four 8x8 16-bit matrices from shared memory; lane l gives the address of row
+// l % 8 of matrix l / 8 (16 contiguous bytes), and receives row l / 4, elements
+// 2 (l % 4) and 2 (l % 4) + 1 of each matrix (transposed with .trans).
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t (&r)[4]) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr));
+}
+__device__ __forceinline__ void ldsm_x4_trans(uint32_t addr, uint32_t (&r)[4]) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr));
+}
+
+// D (16 x 8, fp32) += A (16 x 16, row) B (16 x 8, col), 16-bit inputs; d0, d1 hold
+// row l / 4 of the accumulator, d2, d3 row l / 4 + 8.
+template <bool BF16>
+__device__ __forceinline__ void mma_16816(float& d0, float& d1, float& d2, float& d3, uint32_t a0, uint32_t a1,
+                                          uint32_t a2, uint32_t a3, uint32_t b0, uint32_t b1) {
+  if constexpr (BF16) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+        "{%0, %1, %2, %3};"
+        : "+f"(d0), "+f"(d1), "+f"(d2), "+f"(d3)
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+  } else {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+        "{%0, %1, %2, %3};"
+        : "+f"(d0), "+f"(d1), "+f"(d2), "+f"(d3)
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+  }
+}
+
 template <int D, bool BF16, int HC>
-__global__ void __launch_bounds__(kDecThreads) paged_decode_kernel(const __grid_constant__ CUtensorMap tm_cache,
+__global__ void __maxnreg__(128) paged_decode_kernel(const __grid_constant__ CUtensorMap tm_cache,
                                                                    const DecodeParams p) {
+  static_assert(HC >= 1 && HC <= 8, "query heads per CTA are rows 0-7 of the padded products");
   using L = DecodeSmem<D>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_base = smem_u32(smem_raw);
   const uint32_t sbase = (raw_base + 1023u) & ~1023u;
   uint8_t* smem = smem_raw + (sbase - raw_base);
-  float* q_s = reinterpret_cast<float*>(smem + L::kQOff);
-  float* s_s = reinterpret_cast<float*>(smem + L::kSOff);
-  float* p_s = reinterpret_cast<float*>(smem + L::kPOff);
   float* red_s = reinterpret_cast<float*>(smem + L::kRedOff);
+  volatile unsigned long long* rows_s = reinterpret_cast<volatile unsigned long long*>(smem + L::kRowsOff);
   int* ids_s = reinterpret_cast<int*>(smem + L::kIdsOff);
-  float* alpha_s = reinterpret_cast<float*>(smem + L::kStatOff);
-  float* m_s = alpha_s + 8;
-  float* l_s = alpha_s + 16;
+  uint2* qfrag_s = reinterpret_cast<uint2*>(smem + L::kQFragOff);
+  float* wm_s = reinterpret_cast<float*>(smem + L::kStatOff);  // [warp][8] running max
+  float* wl_s = wm_s + kDecWarps * 8;                            // [warp][8] running sum
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kMiscOff);
-  auto bar = [&](int i) -> uint32_t { return sbase + L::kBarOff + 8u * static_cast<uint32_t>(i); };
+  auto full = [&](int s) -> uint32_t { return sbase + L::kBarOff + 8u * static_cast<uint32_t>(s); };
+  auto empty = [&](int s) -> uint32_t { return sbase + L::kBarOff + 8u * static_cast<uint32_t>(kDecStages + s); };
 
   const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
   // unit: (b, kv head, head chunk, segment), segment fastest
@@ -147,12 +185,16 @@ __global__ void __launch_bounds__(kDecThreads) paged_decode_kernel(const __grid_
   const int n_tiles = pg_end > pg_begin ? (pg_end - pg_begin + pages_per_tile - 1) / pages_per_tile : 0;
 
   if (tid == 0) {
-    for (int s = 0; s < kDecStages; ++s) mbar_init(bar(s), 1);
+    for (int s = 0; s < kDecStages; ++s) {
+      mbar_init(full(s), 1);
+      mbar_init(empty(s), kDecWarps);
+    }
     *abort_flag = 0;
     fence_barrier_init();
   }
   // Page ids of the segment in a rolling window of kDecIdRing slots (slot = page % ring),
-  // read from global memory once each; rejected ids become -1.
+  // read from global memory once each and range-checked when used (rejected ids
+  // are recorded and their pages skipped).
   auto checked_id = [&](int id) {
     if (id < 0 || id >= p.num_pages) {
       atomicExch(p.status, p.bad_index_code);
@@ -161,235 +203,259 @@ __global__ void __launch_bounds__(kDecThreads) paged_decode_kernel(const __grid_
     return id;
   };
   const int* table_row = p.block_table + static_cast<size_t>(b) * p.max_pages;
-  if (tid < kDecIdRing && pg_begin + tid < pg_end) ids_s[tid] = checked_id(table_row[pg_begin + tid]);
-  // query rows of this chunk, scaled by scale * log2(e), in fp32
-  const uint16_t* qg = static_cast<const uint16_t*>(p.q) + (static_cast<size_t>(b) * p.Hq + qh0) * D;
-  for (int i = tid; i < HC * D; i += kDecThreads) q_s[i] = to_f32<BF16>(qg[i]) * p.scale_log2e;
-  if (tid < HC) {
-    m_s[tid] = -INFINITY;
-    l_s[tid] = 0.f;
+  if (tid < kDecIdRing && pg_begin + tid < pg_end) ids_s[tid] = table_row[pg_begin + tid];
+  // Q of the chunk as A fragments of the score products (rows = heads, padded with
+  // zeros to 16), the same for every compute warp: entry [k][l] holds, for lane l,
+  // dims 16 k + 2 (l % 4) .. + 1 and the same + 8 of head l / 4.
+  for (int e = tid; e < (D / 16) * 32; e += kDecThreads) {
+    const int k = e / 32, l = e % 32, h = l >> 2;
+    uint2 v = make_uint2(0u, 0u);
+    if (h < HC) {
+      const uint32_t* qg = reinterpret_cast<const uint32_t*>(static_cast<const uint16_t*>(p.q) +
+                                                             (static_cast<size_t>(b) * p.Hq + qh0 + h) * D);
+      v = make_uint2(qg[8 * k + (l & 3)], qg[8 * k + 4 + (l & 3)]);
+    }
+    qfrag_s[e] = v;
   }
   __syncthreads();
   const Watchdog wd{abort_flag, p.status, p.wait_limit_ns, p.timeout_code};
-
-  // Copies of tile i: both kinds of its pages; a page id out of range is not read.
-  // Each decode step reads its K/V once: evict-first.
-  const uint64_t pol = policy_evict_first();
-  auto issue_tile = [&](int i) {
-    const int slot = i % kDecStages;
-    const uint32_t stage = sbase + L::kRingOff + slot * L::kStageBytes;
-    const int first = i * pages_per_tile;  // within the segment
-    const int np = min(pages_per_tile, pg_end - pg_begin - first);
-    int good = 0;
-    for (int pp = 0; pp < np; ++pp) good += ids_s[(first + pp) % kDecIdRing] >= 0 ? 1 : 0;
-    mbar_arrive_expect_tx(bar(slot), static_cast<uint32_t>(good * 2 * (D / 64) * T * 128));
-    for (int pp = 0; pp < np; ++pp) {
-      const int id = ids_s[(first + pp) % kDecIdRing];
-      if (id < 0) continue;
-      for (int kind = 0; kind < 2; ++kind) {
-        for (int h = 0; h < D / 64; ++h) {
-          const uint32_t dst = stage + kind * L::kKindBytes + (pp * (D / 64) + h) * T * 128;
-          tma_load_3d(dst, &tm_cache, bar(slot), 64 * h, kvh, (id * 2 + kind) * T, pol);
-        }
-      }
-    }
-  };
-
-  // Score mapping: two threads per token row, each owning half of the D columns.
-  const int s_row = tid >> 1, s_half = tid & 1;
-  // P V mapping: one thread per column pair, the tile's 64 tokens split into kTokSplit runs.
-  constexpr int kPairs = D / 2;
-  constexpr int kTokSplit = kDecThreads / kPairs;  // 2 (D = 128) or 4 (D = 64)
-  constexpr int kRun = kDecTile / kTokSplit;
-  const int cp = tid % kPairs, run = tid / kPairs;
-  float2 acc[HC];
+  const int head = lane >> 2;  // query head (row of the products) of this lane's accumulators
+  float m_run = -INFINITY;     // compute warps: running max of head `head`, base-2 domain
+  float l_run = 0.f;           // this lane's part of the running sum
+  float o[D / 8][2];           // O (+)= P V, row `head`, 8 columns per block
 #pragma unroll
-  for (int k = 0; k < HC; ++k) acc[k] = make_float2(0.f, 0.f);
-
-  int issued = 0;  // tiles whose copies thread 0 has started
-  if (tid == 0) {
-    tma_prefetch_map(&tm_cache);
-    for (int i = 0; i < kDecStages - 1 && i < n_tiles; ++i) issue_tile(issued++);
-  }
+  for (int d = 0; d < D / 8; ++d) o[d][0] = o[d][1] = 0.f;
+  // Rows 8-15 of the padded products (P rows of no head, always 0) land in shared
+  // sink registers, four pairs so the products stay in independent chains.
+  float sink[4][2] = {{0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}};
   bool ok = true;
-  for (int i = 0; i < n_tiles && ok; ++i) {
-    // The pages of this tile leave the id window after it; their slots take the pages
-    // kDecIdRing further on.  The load starts now and is stored at the end of the tile.
-    const int refill = i * pages_per_tile + kDecIdRing + tid;  // within the segment
-    const bool refills = tid < pages_per_tile && pg_begin + refill < pg_end;
-    const int refill_id = refills ? table_row[pg_begin + refill] : -1;
-    if (tid == 0 && i + kDecStages - 1 < n_tiles) issue_tile(issued++);
-    const int slot = i % kDecStages;
-    const bool got = wd.wait(bar(slot), static_cast<uint32_t>(i / kDecStages) & 1u);
-    if (!__syncthreads_and(got)) {
-      ok = false;
-      break;
-    }
-    const uint8_t* kt = smem + L::kRingOff + slot * L::kStageBytes;
-    const uint8_t* vt = kt + L::kKindBytes;
-    const int first_page = pg_begin + i * pages_per_tile;
-    const int tok0 = first_page << log2T;  // logical token of tile row 0
-    // Rows that hold a token of this segment on an accepted page; the rest (past the
-    // length, past the segment, or on a rejected page) are empty.
-    uint64_t rows_ok = 0;
-    for (int pp = 0; pp < pages_per_tile && first_page + pp < pg_end; ++pp) {
-      if (ids_s[(first_page - pg_begin + pp) % kDecIdRing] < 0) continue;
-      const int lo = pp << log2T, hi = min((pp + 1) << log2T, len - tok0);
-      if (hi > lo) rows_ok |= (hi - lo == 64 ? ~0ull : ((1ull << (hi - lo)) - 1)) << lo;
-    }
 
-    // scores s = q . k in the base-2 domain: this thread's half row of K, converted once,
-    // against every head of the chunk; the two halves meet through one shuffle.
-    {
-      const bool live = (rows_ok >> s_row) & 1ull;
-      float kf[D / 2];
-      if (live) {
-#pragma unroll
-        for (int c = 0; c < D / 16; ++c) {
-          const uint4 w = *reinterpret_cast<const uint4*>(kt + dec_chunk_offset<D>(s_row, s_half * (D / 16) + c, log2T));
-          const float2 a = to_f32x2<BF16>(w.x), bb = to_f32x2<BF16>(w.y), cc = to_f32x2<BF16>(w.z),
-                       dd = to_f32x2<BF16>(w.w);
-          kf[8 * c + 0] = a.x;
-          kf[8 * c + 1] = a.y;
-          kf[8 * c + 2] = bb.x;
-          kf[8 * c + 3] = bb.y;
-          kf[8 * c + 4] = cc.x;
-          kf[8 * c + 5] = cc.y;
-          kf[8 * c + 6] = dd.x;
-          kf[8 * c + 7] = dd.y;
+  if (warp == kDecWarps) {
+    // ----------------------------------------------------------------- producer
+    if (lane == 0) {
+      tma_prefetch_map(&tm_cache);
+      // Each decode step reads its K/V once: evict-first.
+      const uint64_t pol = policy_evict_first();
+      // The window is refilled with cp.async: after tile i is issued, its slots
+      // receive the page ids kDecIdRing pages further on, which are first needed at
+      // least kDecIdRing / 8 = 8 tiles later; waiting until at most 7 refill groups
+      // are in flight before reading the window keeps the copies off the path.
+      int issued = 0;
+      for (int i = 0; i < n_tiles; ++i) {
+        const int slot = i % kDecStages;
+        if (i >= kDecStages && !wd.wait(empty(slot), static_cast<uint32_t>((i / kDecStages) - 1) & 1u)) {
+          ok = false;
+          break;
         }
-      } else {
+        asm volatile("cp.async.wait_group 7;" ::: "memory");
+        const int first = i * pages_per_tile;  // within the segment
+        const int np = min(pages_per_tile, pg_end - pg_begin - first);
+        const int first_page = pg_begin + first;
+        const int tok0 = first_page << log2T;  // logical token of tile row 0
+        // Rows that hold a token of this segment on an accepted page; the rest (past
+        // the length, past the segment, or on a rejected page) are empty.
+        unsigned long long rows_ok = 0;
+        int good = 0;
+        int ids[8];  // the tile's page ids, range-checked (-1: rejected, not read)
 #pragma unroll
-        for (int e = 0; e < D / 2; ++e) kf[e] = 0.f;
-      }
+        for (int pp = 0; pp < 8; ++pp) ids[pp] = pp < np ? checked_id(ids_s[(first + pp) % kDecIdRing]) : -1;
 #pragma unroll
-      for (int k = 0; k < HC; ++k) {
-        const float4* qq = reinterpret_cast<const float4*>(q_s + k * D + s_half * (D / 2));
-        float2 a2 = make_float2(0.f, 0.f), b2 = make_float2(0.f, 0.f);
-#pragma unroll
-        for (int e = 0; e < D / 8; ++e) {
-          const float4 qv = qq[e];
-          a2 = __ffma2_rn(make_float2(qv.x, qv.y), make_float2(kf[4 * e], kf[4 * e + 1]), a2);
-          b2 = __ffma2_rn(make_float2(qv.z, qv.w), make_float2(kf[4 * e + 2], kf[4 * e + 3]), b2);
+        for (int pp = 0; pp < 8; ++pp) {
+          if (ids[pp] < 0) continue;
+          ++good;
+          const int lo = pp << log2T, hi = min((pp + 1) << log2T, len - tok0);
+          if (hi > lo) rows_ok |= (hi - lo == 64 ? ~0ull : ((1ull << (hi - lo)) - 1)) << lo;
         }
-        float dot = (a2.x + a2.y) + (b2.x + b2.y);
-        dot += __shfl_xor_sync(0xffffffffu, dot, 1);
-        if (s_half == 0) s_s[k * kDecTile + s_row] = live ? dot : -INFINITY;
-      }
-    }
-    __syncthreads();
-
-    // online softmax, one warp per head: m' = max(m, max s), p = 2^(s - m'), l' = l 2^(m - m') + sum p
-    for (int qh = warp; qh < HC; qh += kDecThreads / 32) {
-      const float s0 = s_s[qh * kDecTile + lane], s1 = s_s[qh * kDecTile + lane + 32];
-      float mx = fmaxf(s0, s1);
+        rows_s[slot] = rows_ok;
+        mbar_arrive_expect_tx(full(slot), static_cast<uint32_t>(good * 2 * (D / 64) * T * 128));
+        const uint32_t stage = sbase + L::kRingOff + slot * L::kStageBytes;
 #pragma unroll
-      for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
-      const float m_old = m_s[qh];
-      const float m_new = fmaxf(m_old, mx);
-      const float p0 = m_new == -INFINITY ? 0.f : ex2(s0 - m_new);
-      const float p1 = m_new == -INFINITY ? 0.f : ex2(s1 - m_new);
-      float sum = p0 + p1;
-#pragma unroll
-      for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
-      const float alpha = m_old == -INFINITY ? 0.f : ex2(m_old - m_new);
-      p_s[lane * 8 + qh] = p0;
-      p_s[(lane + 32) * 8 + qh] = p1;
-      __syncwarp();
-      if (lane == 0) {
-        alpha_s[qh] = alpha;
-        m_s[qh] = m_new;
-        l_s[qh] = l_s[qh] * alpha + sum;
-      }
-    }
-    __syncthreads();
-
-    // o = alpha o + sum_r p_r v_r: this thread's column pair over its run of rows.
-    // Empty rows are skipped (their V is never read: its data may not be a number).
-#pragma unroll
-    for (int k = 0; k < HC; ++k) {
-      const float al = alpha_s[k];
-      acc[k] = __fmul2_rn(acc[k], make_float2(al, al));
-    }
-    const int c = (2 * cp) >> 3, within = ((2 * cp) & 7) * 2;  // 16-byte chunk and byte inside it
-    const uint64_t run_mask = (rows_ok >> (run * kRun)) & ((kRun == 64 ? ~0ull : (1ull << kRun) - 1));
-    if (run_mask == (kRun == 64 ? ~0ull : (1ull << kRun) - 1)) {
-#pragma unroll 4
-      for (int j = 0; j < kRun; ++j) {
-        const int r = run * kRun + j;
-        const float2 v = to_f32x2<BF16>(*reinterpret_cast<const uint32_t*>(vt + dec_chunk_offset<D>(r, c, log2T) + within));
-        const float4* pp = reinterpret_cast<const float4*>(p_s + r * 8);
-        const float4 pa = pp[0];
-        const float pr[8] = {pa.x, pa.y, pa.z, pa.w, 0.f, 0.f, 0.f, 0.f};
-        float4 pb = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (HC > 4) pb = pp[1];
-#pragma unroll
-        for (int k = 0; k < HC; ++k) {
-          const float pk = k < 4 ? pr[k] : (k == 4 ? pb.x : (k == 5 ? pb.y : (k == 6 ? pb.z : pb.w)));
-          acc[k] = __ffma2_rn(make_float2(pk, pk), v, acc[k]);
-        }
-      }
-    } else {
-      for (int j = 0; j < kRun; ++j) {
-        if (!((run_mask >> j) & 1ull)) continue;
-        const int r = run * kRun + j;
-        const float2 v = to_f32x2<BF16>(*reinterpret_cast<const uint32_t*>(vt + dec_chunk_offset<D>(r, c, log2T) + within));
-#pragma unroll
-        for (int k = 0; k < HC; ++k) {
-          const float pk = p_s[r * 8 + k];
-          acc[k] = __ffma2_rn(make_float2(pk, pk), v, acc[k]);
-        }
-      }
-    }
-    if (refills) ids_s[refill % kDecIdRing] = checked_id(refill_id);
-    __syncthreads();  // the stage, the scores and p may be overwritten now
-  }
-
-  if (ok) {
-    // the runs' partial outputs meet in shared memory, then O = o / l and
-    // lse = (m + log2 l) ln 2; an empty context gives O = 0 and lse = -inf
-    if (run > 0) {
-#pragma unroll
-      for (int k = 0; k < HC; ++k)
-        *reinterpret_cast<float2*>(red_s + ((run - 1) * 8 + k) * D + 2 * cp) = acc[k];
-    }
-    __syncthreads();
-    if (run == 0) {
-#pragma unroll
-      for (int k = 0; k < HC; ++k) {
-        float2 o = acc[k];
-        for (int rr = 1; rr < kTokSplit; ++rr) {
-          const float2 part = *reinterpret_cast<const float2*>(red_s + ((rr - 1) * 8 + k) * D + 2 * cp);
-          o.x += part.x;
-          o.y += part.y;
-        }
-        const float l = l_s[k];
-        const float inv = l > 0.f ? 1.f / l : 0.f;
-        const size_t row = static_cast<size_t>(b) * p.Hq + qh0 + k;
-        if (p.part_o != nullptr) {
-          *reinterpret_cast<float2*>(p.part_o + (static_cast<size_t>(seg) * p.B * p.Hq + row) * D + 2 * cp) =
-              make_float2(o.x * inv, o.y * inv);
-        } else {
-          *reinterpret_cast<uint32_t*>(static_cast<uint16_t*>(p.out) + row * D + 2 * cp) = pack2<BF16>(o.x * inv, o.y * inv);
-        }
-        if (cp == 0) {
-          const float lse = l > 0.f ? (m_s[k] + log2f(l)) * 0.69314718055994530942f : -INFINITY;
-          if (p.part_o != nullptr) {
-            p.part_lse[static_cast<size_t>(seg) * p.B * p.Hq + row] = lse;
-          } else if (p.lse != nullptr) {
-            p.lse[row] = lse;
+        for (int pp = 0; pp < 8; ++pp) {
+          const int id = ids[pp];
+          if (id < 0) continue;
+          for (int kind = 0; kind < 2; ++kind) {
+            for (int h = 0; h < D / 64; ++h) {
+              const uint32_t dst = stage + kind * L::kKindBytes + (pp * (D / 64) + h) * T * 128;
+              tma_load_3d(dst, &tm_cache, full(slot), 64 * h, kvh, (id * 2 + kind) * T, pol);
+            }
           }
         }
+        ++issued;
+        // This tile's window slots now take the pages kDecIdRing further on.
+        for (int pp = 0; pp < np; ++pp) {
+          const int page = pg_begin + first + pp + kDecIdRing;
+          if (page < pg_end) {
+            asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_u32(ids_s + (first + pp) % kDecIdRing)),
+                         "l"(table_row + page)
+                         : "memory");
+          }
+        }
+        asm volatile("cp.async.commit_group;" ::: "memory");
+      }
+      asm volatile("cp.async.wait_all;" ::: "memory");
+      // let every copy issued here land before the block exits
+      for (int i = (issued > kDecStages ? issued - kDecStages : 0); i < issued; ++i) {
+        wd.drain(full(i % kDecStages), static_cast<uint32_t>(i / kDecStages) & 1u);
       }
     }
+  } else {
+    // ------------------------------------------------------------ compute warps
+    const float c = p.scale_log2e;
+    const int tok_w = 16 * warp;  // this warp's rows of every tile
+    for (int i = 0; i < n_tiles; ++i) {
+      const int slot = i % kDecStages;
+      if (!__all_sync(0xffffffffu, wd.wait(full(slot), static_cast<uint32_t>(i / kDecStages) & 1u))) {
+        ok = false;
+        break;
+      }
+      const unsigned long long rows_ok = rows_s[slot];
+      const uint32_t kt = sbase + L::kRingOff + slot * L::kStageBytes;
+      const uint32_t vt = kt + L::kKindBytes;
+      // S = Q K^T for this warp's two 8-token blocks; ldmatrix row address of lane l:
+      // token block + l % 8, 16-byte chunk (8 dims) 4 kk + l / 8 (two k-steps per load).
+      float sacc[2][4];
+#pragma unroll
+      for (int nb = 0; nb < 2; ++nb) {
+        sacc[nb][0] = sacc[nb][1] = sacc[nb][2] = sacc[nb][3] = 0.f;
+#pragma unroll
+        for (int kk = 0; kk < D / 32; ++kk) {
+          uint32_t kb[4];
+          ldsm_x4(kt + dec_chunk_offset<D>(tok_w + 8 * nb + (lane & 7), 4 * kk + (lane >> 3), log2T), kb);
+          const uint2 qa0 = qfrag_s[(2 * kk) * 32 + lane], qa1 = qfrag_s[(2 * kk + 1) * 32 + lane];
+          mma_16816<BF16>(sacc[nb][0], sacc[nb][1], sacc[nb][2], sacc[nb][3], qa0.x, 0u, qa0.y, 0u, kb[0], kb[1]);
+          mma_16816<BF16>(sacc[nb][0], sacc[nb][1], sacc[nb][2], sacc[nb][3], qa1.x, 0u, qa1.y, 0u, kb[2], kb[3]);
+        }
+      }
+      // This lane holds head `head` at tokens tok_w + 8 nb + 2 (lane % 4) + e.
+      float x[4];
+#pragma unroll
+      for (int nb = 0; nb < 2; ++nb) {
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const int r = tok_w + 8 * nb + 2 * (lane & 3) + e;
+          x[2 * nb + e] = ((rows_ok >> r) & 1ull) ? sacc[nb][e] * c : -INFINITY;
+        }
+      }
+      // online softmax over this warp's tokens: m' = max(m, max s), p = 2^(s - m'),
+      // l' = l 2^(m - m') + sum p (the four lanes of a head share m)
+      float mt = fmaxf(fmaxf(x[0], x[1]), fmaxf(x[2], x[3]));
+      mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, 1));
+      mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, 2));
+      const float m_new = fmaxf(m_run, mt);
+      const float alpha = m_run == -INFINITY ? 0.f : ex2(m_run - m_new);
+      float pe[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) pe[e] = m_new == -INFINITY ? 0.f : ex2(x[e] - m_new);
+      l_run = l_run * alpha + ((pe[0] + pe[1]) + (pe[2] + pe[3]));
+      m_run = m_new;
+#pragma unroll
+      for (int d = 0; d < D / 8; ++d) {
+        o[d][0] *= alpha;
+        o[d][1] *= alpha;
+      }
+      // P as the A fragment of O += P V (rows = heads, k = the warp's 16 tokens)
+      const uint32_t pa0 = pack2<BF16>(pe[0], pe[1]);
+      const uint32_t pa2 = pack2<BF16>(pe[2], pe[3]);
+      // V fragments with ldmatrix.trans; lane l: token tok_w + l % 8 + 8 ((l / 8) % 2),
+      // 16-byte chunk (8 dims) 2 dp + l / 16: dims blocks 2 dp and 2 dp + 1.
+      // Empty rows have p = 0; their V may not be a number, so p 0 x NaN would
+      // poison the sum: skip the tile's products when any of the warp's rows is empty
+      // and zero their V through the mask below instead.
+      const unsigned long long mine = (rows_ok >> tok_w) & 0xffffull;
+      if (mine == 0xffffull) {
+#pragma unroll
+        for (int dp = 0; dp < D / 16; ++dp) {
+          uint32_t vb[4];
+          ldsm_x4_trans(vt + dec_chunk_offset<D>(tok_w + (lane & 7) + 8 * ((lane >> 3) & 1), 2 * dp + (lane >> 4), log2T),
+                        vb);
+          mma_16816<BF16>(o[2 * dp][0], o[2 * dp][1], sink[dp % 4][0], sink[dp % 4][1], pa0, 0u, pa2, 0u, vb[0],
+                          vb[1]);
+          mma_16816<BF16>(o[2 * dp + 1][0], o[2 * dp + 1][1], sink[(dp + 2) % 4][0], sink[(dp + 2) % 4][1], pa0, 0u,
+                          pa2, 0u, vb[2], vb[3]);
+        }
+      } else if (mine != 0) {
+        // Partly empty: the V fragment entries of empty rows are replaced by zero.
+        // Lane l holds, in each fragment register, rows (tokens) 2 (l % 4) and + 1
+        // (b0b1) and the same + 8 (b2b3).
+        const int r0 = 2 * (lane & 3);
+        const uint32_t keep01 = (((mine >> r0) & 1ull) ? 0x0000ffffu : 0u) | (((mine >> (r0 + 1)) & 1ull) ? 0xffff0000u : 0u);
+        const uint32_t keep89 =
+            (((mine >> (r0 + 8)) & 1ull) ? 0x0000ffffu : 0u) | (((mine >> (r0 + 9)) & 1ull) ? 0xffff0000u : 0u);
+#pragma unroll
+        for (int dp = 0; dp < D / 16; ++dp) {
+          uint32_t vb[4];
+          ldsm_x4_trans(vt + dec_chunk_offset<D>(tok_w + (lane & 7) + 8 * ((lane >> 3) & 1), 2 * dp + (lane >> 4), log2T),
+                        vb);
+          mma_16816<BF16>(o[2 * dp][0], o[2 * dp][1], sink[dp % 4][0], sink[dp % 4][1], pa0, 0u, pa2, 0u,
+                          vb[0] & keep01, vb[1] & keep89);
+          mma_16816<BF16>(o[2 * dp + 1][0], o[2 * dp + 1][1], sink[(dp + 2) % 4][0], sink[(dp + 2) % 4][1], pa0,
+                          0u, pa2, 0u, vb[2] & keep01, vb[3] & keep89);
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(empty(slot));
+    }
+    // this warp's state for the merge: the four lanes of a head add their sums
+    l_run += __shfl_xor_sync(0xffffffffu, l_run, 1);
+    l_run += __shfl_xor_sync(0xffffffffu, l_run, 2);
+    if ((lane & 3) == 0) {
+      wm_s[warp * 8 + head] = m_run;
+      wl_s[warp * 8 + head] = l_run;
+    }
   }
-  // let every copy thread 0 issued land before the block exits
-  if (tid == 0) {
-    for (int i = (issued > kDecStages ? issued - kDecStages : 0); i < issued; ++i) {
-      wd.drain(bar(i % kDecStages), static_cast<uint32_t>(i / kDecStages) & 1u);
+  __syncthreads();  // every copy has landed (the producer drained), every warp's state is in
+  // Merge of the warps (section 6.4): M = max m_w, L = sum l_w 2^(m_w - M),
+  // O = sum o_w 2^(m_w - M) / L; each compute warp scales its partial output.
+  if (warp < kDecWarps) {
+    float mx = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < kDecWarps; ++w) mx = fmaxf(mx, wm_s[w * 8 + head]);
+    const float sc = m_run == -INFINITY ? 0.f : ex2(m_run - mx);
+    if (head < HC) {
+#pragma unroll
+      for (int d = 0; d < D / 8; ++d) {
+        *reinterpret_cast<float2*>(red_s + (warp * 8 + head) * D + 8 * d + 2 * (lane & 3)) =
+            make_float2(o[d][0] * sc, o[d][1] * sc);
+      }
     }
   }
   __syncthreads();
+  if (ok && !wd.aborted()) {
+    // O = o / L and lse = (M + log2 L) ln 2; an empty context gives O = 0 and lse = -inf
+    for (int idx = tid; idx < HC * (D / 2); idx += kDecThreads) {
+      const int k = idx / (D / 2), cp = idx % (D / 2);
+      float mx = -INFINITY;
+#pragma unroll
+      for (int w = 0; w < kDecWarps; ++w) mx = fmaxf(mx, wm_s[w * 8 + k]);
+      float l = 0.f;
+      float2 acc = make_float2(0.f, 0.f);
+#pragma unroll
+      for (int w = 0; w < kDecWarps; ++w) {
+        const float mw = wm_s[w * 8 + k];
+        l += mw == -INFINITY ? 0.f : wl_s[w * 8 + k] * ex2(mw - mx);
+        const float2 part = *reinterpret_cast<const float2*>(red_s + (w * 8 + k) * D + 2 * cp);
+        acc.x += part.x;
+        acc.y += part.y;
+      }
+      const float inv = l > 0.f ? 1.f / l : 0.f;
+      const size_t row = static_cast<size_t>(b) * p.Hq + qh0 + k;
+      if (p.part_o != nullptr) {
+        *reinterpret_cast<float2*>(p.part_o + (static_cast<size_t>(seg) * p.B * p.Hq + row) * D + 2 * cp) =
+            make_float2(acc.x * inv, acc.y * inv);
+      } else {
+        *reinterpret_cast<uint32_t*>(static_cast<uint16_t*>(p.out) + row * D + 2 * cp) =
+            pack2<BF16>(acc.x * inv, acc.y * inv);
+      }
+      if (cp == 0) {
+        const float lse = l > 0.f ? (mx + log2f(l)) * 0.69314718055994530942f : -INFINITY;
+        if (p.part_o != nullptr) {
+          p.part_lse[static_cast<size_t>(seg) * p.B * p.Hq + row] = lse;
+        } else if (p.lse != nullptr) {
+          p.lse[row] = lse;
+        }
+      }
+    }
+  }
 }
 
 // Merge of the decode segments (section 6.4 of the page, in log-sum-exp form as in

@@ -183,7 +183,8 @@ int attn_splitkv_default_splits(int B, int H, int N, int D);
  * A request with length 0 gets O = 0 and lse = -inf.  A block-table entry
  * outside [0, num_pages) or a length outside [0, max_pages * page_size] is not
  * followed: the tokens it names are skipped and attn_device_status reports
- * ATTN_ERR_BAD_INDEX.  Probabilities stay fp32 (no 16-bit rounding of P).
+ * ATTN_ERR_BAD_INDEX.  As in attn_fwd, P is rounded to the input's 16-bit type for
+ * the P V product; scores, sums and O accumulate in fp32.
  */
 int attn_decode_paged(const void* q, const void* cache, const int* block_table, const int* lengths,
                       void* out, float* lse, int B, int Hq, int Hkv, int D, int page_size,
