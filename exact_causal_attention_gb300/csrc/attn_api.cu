@@ -39,6 +39,14 @@ __device__ int g_device_status = 0;
 constexpr int kSchedSlots = 64;
 __device__ int g_sched_pool[kSchedSlots * 64] = {};
 
+// Counters of the paged decode's fused segment merge: one per (request, K/V head,
+// head chunk), zero between launches (each group's last segment resets its
+// counter).  Slots are taken in turn so up to 8 launches can run at once; larger
+// launches use the separate merge kernel.
+constexpr int kDecCounterSlots = 8;
+constexpr int kDecCountersPerSlot = 4096;
+__device__ unsigned g_dec_counters[kDecCounterSlots * kDecCountersPerSlot] = {};
+
 using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
                                    const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
                                    const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
@@ -52,6 +60,8 @@ struct DeviceState {
   void* scratch = nullptr;  // address of g_splitkv_scratch on this device, set by its first use
   int* sched_pool = nullptr;  // address of g_sched_pool on this device
   unsigned sched_next = 0;    // slot of the next attention launch
+  unsigned* dec_counters = nullptr;  // address of g_dec_counters on this device
+  unsigned dec_next = 0;             // slot of the next split decode launch
   unsigned configured = 0;  // bitmask of kernel instantiations with smem attribute set
   unsigned configured_decode = 0;
 };
@@ -97,6 +107,8 @@ int device_state(DeviceState** out) {
       st.status = static_cast<int*>(addr);
       if (cudaGetSymbolAddress(&addr, g_sched_pool) != cudaSuccess) return ATTN_ERR_CUDA;
       st.sched_pool = static_cast<int*>(addr);
+      if (cudaGetSymbolAddress(&addr, g_dec_counters) != cudaSuccess) return ATTN_ERR_CUDA;
+      st.dec_counters = static_cast<unsigned*>(addr);
     }
     st.probed = true;
   }
@@ -470,7 +482,7 @@ int launch_decode(const CUtensorMap& tm, eca::DecodeParams& p, const DecodeShape
     case 2: rc = run(eca::paged_decode_kernel<D, BF16, 2>, 1u << (base + 1)); break;
     default: rc = run(eca::paged_decode_kernel<D, BF16, 1>, 1u << base); break;
   }
-  if (rc != ATTN_OK || p.part_o == nullptr) return rc;
+  if (rc != ATTN_OK || p.part_o == nullptr || p.counters != nullptr) return rc;  // merged in the kernel
   const long long rows = static_cast<long long>(p.B) * p.Hq;
   const long long want = (rows + 7) / 8, cap = static_cast<long long>(st->sm_count) * 8;
   eca::paged_decode_combine<D, BF16><<<static_cast<unsigned>(want < cap ? want : cap), 256, 0, stream>>>(p);
@@ -533,6 +545,11 @@ int decode_impl(bool bf16, const void* q, const void* cache, const int* block_ta
   p.wait_limit_ns = kWaitLimitNs;
   p.timeout_code = ATTN_ERR_TIMEOUT;
   p.bad_index_code = ATTN_ERR_BAD_INDEX;
+  p.counters = nullptr;
+  const long long groups = static_cast<long long>(B) * Hkv * sh.head_chunks;
+  if (sh.splits > 1 && groups <= kDecCountersPerSlot) {
+    p.counters = st->dec_counters + static_cast<size_t>(st->dec_next++ % kDecCounterSlots) * kDecCountersPerSlot;
+  }
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   if (D == 128) {
     return bf16 ? launch_decode<128, true>(tm, p, sh, st, s) : launch_decode<128, false>(tm, p, sh, st, s);
@@ -655,8 +672,9 @@ int attn_decode_default_splits(int B, int Hq, int Hkv, int page_size, int max_pa
   const DecodeShape one = decode_shape(Hq, Hkv, page_size, max_pages, 1);
   const long long ctas = static_cast<long long>(B) * Hkv * one.head_chunks;
   const long long tiles = (static_cast<long long>(max_pages) * page_size + eca::kDecTile - 1) / eca::kDecTile;
-  // One wave of the three CTAs an SM holds, at least one segment each.
-  long long s = 3LL * st->sm_count / ctas;
+  // About two CTAs per SM (measured best on the decode page's geometry, contexts
+  // 1K-32K: fewer leave HBM idle, more add per-CTA start and merge costs).
+  long long s = (2LL * st->sm_count + ctas / 2) / ctas;
   if (s > tiles) s = tiles;
   if (s > kMaxSplits) s = kMaxSplits;
   return s < 1 ? 1 : static_cast<int>(s);

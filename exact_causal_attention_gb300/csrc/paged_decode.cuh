@@ -59,6 +59,10 @@ struct DecodeParams {
   float scale_log2e;
   unsigned long long wait_limit_ns;
   int timeout_code, bad_index_code;
+  // Split only: one counter per (request, K/V head, head chunk), zero on entry and
+  // left zero; the last segment to finish merges the group's partial results.
+  // Null: a separate merge kernel does it.
+  unsigned* counters;
 };
 
 template <int D>
@@ -72,7 +76,7 @@ struct DecodeSmem {
   static constexpr int kQFragOff = kIdsOff + kDecIdRing * 4;        // uint32 [D/16][32 lanes][2] query fragments
   static constexpr int kStatOff = kQFragOff + (D / 16) * 32 * 8;     // fp32 [warps][8] m, then [warps][8] l
   static constexpr int kBarOff = kStatOff + 2 * kDecWarps * 8 * 4;  // full[stages], then empty[stages]
-  static constexpr int kMiscOff = kBarOff + 2 * kDecStages * 8;     // abort flag
+  static constexpr int kMiscOff = kBarOff + 2 * kDecStages * 8;     // abort flag, last-segment flag
   static constexpr int kBytes = kMiscOff + 16;
   static constexpr int kDynamicBytes = kBytes + 1024;
   static_assert(kDecWarps * 8 * D * 4 <= kDecStages * kStageBytes, "reduction buffer fits over the ring");
@@ -455,6 +459,51 @@ __global__ void __maxnreg__(128) paged_decode_kernel(const __grid_constant__ CUt
         }
       }
     }
+  }
+  if (p.part_o == nullptr || p.counters == nullptr) return;
+  // Merge of the segments (section 6.4, log-sum-exp form) by the group's last
+  // segment to finish: lse = ln sum_s e^(lse_s), O = sum_s e^(lse_s - lse) O_s.
+  const int valid = min(p.splits, (n_pages + p.seg_pages - 1) / p.seg_pages);  // segments with pages
+  volatile int* last_flag = reinterpret_cast<volatile int*>(smem + L::kMiscOff + 4);
+  const size_t stride = static_cast<size_t>(p.B) * p.Hq;
+  if (seg < valid) {
+    __syncthreads();  // this segment's partial results are written
+    if (tid == 0) {
+      __threadfence();
+      unsigned* counter = p.counters + static_cast<size_t>(blockIdx.x / p.splits);
+      const bool last = atomicAdd(counter, 1u) == static_cast<unsigned>(valid - 1);
+      if (last) {
+        *counter = 0u;  // back to zero for the next launch
+        __threadfence();
+      }
+      *last_flag = last ? 1 : 0;
+    }
+    __syncthreads();
+    if (*last_flag == 0) return;
+  } else if (!(valid == 0 && seg == 0)) {
+    return;  // an empty segment; an empty request is finished by its segment 0
+  }
+  for (int idx = tid; idx < HC * (D / 2); idx += kDecThreads) {
+    const int k = idx / (D / 2), cp = idx % (D / 2);
+    const size_t row = static_cast<size_t>(b) * p.Hq + qh0 + k;
+    float m = -INFINITY;
+    for (int sg = 0; sg < valid; ++sg) m = fmaxf(m, __ldcg(p.part_lse + sg * stride + row));
+    float wsum = 0.f;
+    float2 acc = make_float2(0.f, 0.f);
+    if (m != -INFINITY) {
+      for (int sg = 0; sg < valid; ++sg) {
+        const float lse_s = __ldcg(p.part_lse + sg * stride + row);
+        if (lse_s == -INFINITY) continue;
+        const float wgt = expf(lse_s - m);
+        wsum += wgt;
+        const float2 o_s = __ldcg(reinterpret_cast<const float2*>(p.part_o + (sg * stride + row) * D + 2 * cp));
+        acc.x += wgt * o_s.x;
+        acc.y += wgt * o_s.y;
+      }
+    }
+    const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
+    *reinterpret_cast<uint32_t*>(static_cast<uint16_t*>(p.out) + row * D + 2 * cp) = pack2<BF16>(acc.x * inv, acc.y * inv);
+    if (cp == 0 && p.lse != nullptr) p.lse[row] = wsum > 0.f ? m + logf(wsum) : -INFINITY;
   }
 }
 

@@ -201,9 +201,12 @@ int attn_decode_paged_bf16(const void* q, const void* cache, const int* block_ta
  * the sizes are invalid).  Needs no GPU. */
 size_t attn_decode_workspace_bytes(int B, int Hq, int D, int kv_splits);
 
-/* A context split for the current device: one wave of the three decode CTAs an SM
- * holds, capped by the 64-token tiles of max_pages * page_size and by 64.  Negative attn_status on bad
- * sizes or a non-sm_103 device. */
+/* A context split for the current device: about two decode CTAs per SM (the
+ * measured best at every context length of the page's benchmark geometry),
+ * capped by the 64-token tiles of max_pages * page_size and by 64.  When the split
+ * is used, the segments are merged inside the decode kernel (by each group's last
+ * segment) unless B * Hkv * head chunks exceeds 4096, when a second kernel merges
+ * them.  Negative attn_status on bad sizes or a non-sm_103 device. */
 int attn_decode_default_splits(int B, int Hq, int Hkv, int page_size, int max_pages);
 
 /*
