@@ -216,6 +216,65 @@ def bench_reference(args, w):
     print(json.dumps(line), flush=True)
 
 
+def bench_paged(eca, inputs, dev, stream, flush, contexts):
+    """Paged GQA decode over the decode page's geometry (B=8, Hq=32, Hkv=8, D=128,
+    page size 16): HBM-bound, it must stream 2 B L Hkv D s bytes of K/V per step.
+    Median of 10 calls after 3 per context, L2 flushed before each."""
+    import torch
+
+    paged = {}
+    peaks_pd, _ = measured_peaks()
+    pw = inputs.PAGED_BENCH
+    gen = torch.Generator(device=dev).manual_seed(pw.seed)
+    for ctx in contexts:
+        pages = (ctx + pw.page_size - 1) // pw.page_size
+        P = pw.B * pages
+        cache = torch.randn(P, 2, pw.page_size, pw.Hkv, pw.D, generator=gen, device=dev, dtype=torch.float16)
+        table = torch.randperm(P, generator=gen, device=dev).to(torch.int32).view(pw.B, pages).contiguous()
+        lens = torch.full((pw.B,), ctx, dtype=torch.int32, device=dev)
+        qd = torch.randn(pw.B, pw.Hq, pw.D, generator=gen, device=dev, dtype=torch.float16)
+        outd = torch.empty_like(qd)
+        lsed = torch.empty((pw.B, pw.Hq), dtype=torch.float32, device=dev)
+        splits = eca.load_library().attn_decode_default_splits(pw.B, pw.Hq, pw.Hkv, pw.page_size, pages)
+        need = int(eca.load_library().attn_decode_workspace_bytes(pw.B, pw.Hq, pw.D, splits))
+        ws = torch.empty(need + 256, dtype=torch.uint8, device=dev) if need else None
+        if ws is not None:
+            off = (-ws.data_ptr()) % 256
+            ws = ws[off:off + need]
+        times = []
+        for i in range(13):
+            flush.zero_()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            eca.decode_paged(qd, cache, table, lens, kv_splits=splits, out=outd, lse=lsed, workspace=ws,
+                             stream=stream)
+            b.record(stream)
+            times.append((a, b))
+        torch.cuda.synchronize(dev)
+        ms = sorted(a.elapsed_time(b) for a, b in times[3:])
+        med = ms[len(ms) // 2]
+        kv = 2 * pw.B * ctx * pw.Hkv * pw.D * 2
+        paged[str(ctx)] = {"us": round(med * 1e3, 2), "GB_s": round(kv / (med * 1e-3) / 1e9, 1),
+                           "frac_of_hbm": round(kv / (med * 1e-3) / 1e9 / float(peaks_pd["hbm_gbs"]), 3),
+                           "kv_splits": splits}
+        if ctx == contexts[-1]:
+            newkv = torch.randn(pw.B, 2, pw.Hkv, pw.D, generator=gen, device=dev, dtype=torch.float16)
+            at = []
+            for i in range(13):
+                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a.record(stream)
+                eca.paged_append(newkv, cache, table, lens, stream=stream)
+                b.record(stream)
+                at.append((a, b))
+            torch.cuda.synchronize(dev)
+            ams = sorted(a.elapsed_time(b) for a, b in at[3:])
+            paged["append_us"] = round(ams[len(ams) // 2] * 1e3, 2)
+        del cache, table, lens, qd, outd, lsed, ws
+    span = f"ctx{contexts[0]}" if len(contexts) == 1 else f"ctx{contexts[0]}..{contexts[-1]}"
+    paged["workload"] = pw.name.replace("ctx32768", span)
+    return paged
+
+
 def bench_ours(args, w):
     import torch
     import torch.distributed as dist
@@ -413,58 +472,7 @@ def bench_ours(args, w):
         row_softmax["hbm_peak_gbs"] = float(peaks_rs["hbm_gbs"])
         row_softmax["peak_kind"] = kind_rs
 
-    # Paged GQA decode over the decode page's geometry (B=8, Hq=32, Hkv=8, D=128, page size 16):
-    # HBM-bound, it must stream 2 B L Hkv D s bytes of K/V per step.
-    paged = {}
-    if not args.no_sweep and rank == 0:
-        peaks_pd, _ = measured_peaks()
-        pw = inputs.PAGED_BENCH
-        gen = torch.Generator(device=dev).manual_seed(pw.seed)
-        for ctx in inputs.PAGED_CONTEXTS:
-            pages = (ctx + pw.page_size - 1) // pw.page_size
-            P = pw.B * pages
-            cache = torch.randn(P, 2, pw.page_size, pw.Hkv, pw.D, generator=gen, device=dev, dtype=torch.float16)
-            table = torch.randperm(P, generator=gen, device=dev).to(torch.int32).view(pw.B, pages).contiguous()
-            lens = torch.full((pw.B,), ctx, dtype=torch.int32, device=dev)
-            qd = torch.randn(pw.B, pw.Hq, pw.D, generator=gen, device=dev, dtype=torch.float16)
-            outd = torch.empty_like(qd)
-            lsed = torch.empty((pw.B, pw.Hq), dtype=torch.float32, device=dev)
-            splits = eca.load_library().attn_decode_default_splits(pw.B, pw.Hq, pw.Hkv, pw.page_size, pages)
-            need = int(eca.load_library().attn_decode_workspace_bytes(pw.B, pw.Hq, pw.D, splits))
-            ws = torch.empty(need + 256, dtype=torch.uint8, device=dev) if need else None
-            if ws is not None:
-                off = (-ws.data_ptr()) % 256
-                ws = ws[off:off + need]
-            times = []
-            for i in range(13):
-                flush.zero_()
-                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-                a.record(stream)
-                eca.decode_paged(qd, cache, table, lens, kv_splits=splits, out=outd, lse=lsed, workspace=ws,
-                                 stream=stream)
-                b.record(stream)
-                times.append((a, b))
-            torch.cuda.synchronize(dev)
-            ms = sorted(a.elapsed_time(b) for a, b in times[3:])
-            med = ms[len(ms) // 2]
-            kv = 2 * pw.B * ctx * pw.Hkv * pw.D * 2
-            paged[str(ctx)] = {"us": round(med * 1e3, 2), "GB_s": round(kv / (med * 1e-3) / 1e9, 1),
-                               "frac_of_hbm": round(kv / (med * 1e-3) / 1e9 / float(peaks_pd["hbm_gbs"]), 3),
-                               "kv_splits": splits}
-            if ctx == inputs.PAGED_CONTEXTS[-1]:
-                newkv = torch.randn(pw.B, 2, pw.Hkv, pw.D, generator=gen, device=dev, dtype=torch.float16)
-                at = []
-                for i in range(13):
-                    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-                    a.record(stream)
-                    eca.paged_append(newkv, cache, table, lens, stream=stream)
-                    b.record(stream)
-                    at.append((a, b))
-                torch.cuda.synchronize(dev)
-                ams = sorted(a.elapsed_time(b) for a, b in at[3:])
-                paged["append_us"] = round(ams[len(ams) // 2] * 1e3, 2)
-            del cache, table, lens, qd, outd, lsed, ws
-        paged["workload"] = pw.name.replace("ctx32768", "ctx1024..32768")
+    paged = bench_paged(eca, inputs, dev, stream, flush, inputs.PAGED_CONTEXTS) if (not args.no_sweep and rank == 0) else {}
 
     fp16_peak = None
     if not args.no_peak and rank == 0:
@@ -538,11 +546,25 @@ def main():
     ap.add_argument("--no-peak", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--paged-only", type=int, nargs="*", metavar="CONTEXT",
+                    help="only the paged-decode measurement, at the given contexts (default: all)")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
     from exact_causal_attention_gb300 import inputs
 
     w = inputs.WORKLOADS[WORKLOAD]
+    if args.paged_only is not None:
+        import torch
+
+        import exact_causal_attention_gb300 as eca
+
+        eca.load_library()
+        dev = torch.device("cuda", 0)
+        flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+        contexts = args.paged_only or list(inputs.PAGED_CONTEXTS)
+        paged = bench_paged(eca, inputs, dev, torch.cuda.current_stream(dev), flush, contexts)
+        print(json.dumps({"paged_decode": paged}), flush=True)
+        return
     if args.impl == "reference":
         bench_reference(args, w)
     else:
