@@ -120,11 +120,65 @@ def _check_qkv(q, k, v):
         raise ValueError("q, k, v must be on one device")
 
 
+_raw_stream_fn = None
+
+
+def _raw_stream(device_index: int, stream) -> int:
+    """cudaStream_t of ``stream``, or of torch's current stream on the device, as an int.
+    torch's raw-stream query skips building a Stream object, which costs microseconds."""
+    global _raw_stream_fn
+    if stream is not None:
+        return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+    if _raw_stream_fn is None:
+        import torch
+
+        fn = getattr(torch._C, "_cuda_getCurrentRawStream", None)
+        _raw_stream_fn = fn if fn is not None else (lambda i: torch.cuda.current_stream(i).cuda_stream)
+    return _raw_stream_fn(device_index)
+
+
+def _fwd_fast(q, k, v, o, lse, causal, scale, stream) -> bool:
+    """The common call, checked with few attribute reads: q, k, v, o contiguous CUDA
+    tensors of one shape, 16-bit type and device (the current one), lse None or
+    contiguous fp32 [B, H, N] there.  Returns False, having launched nothing, for
+    anything else, which the checked path then reports."""
+    import torch
+
+    try:
+        shape = q.shape
+        dt = q.dtype
+        dev = q.get_device()
+        if (len(shape) != 4 or dev < 0 or dt not in (torch.float16, torch.bfloat16)
+                or k.shape != shape or v.shape != shape or o.shape != shape
+                or k.dtype != dt or v.dtype != dt or o.dtype != dt
+                or k.get_device() != dev or v.get_device() != dev or o.get_device() != dev
+                or not (q.is_contiguous() and k.is_contiguous() and v.is_contiguous() and o.is_contiguous())):
+            return False
+        if lse is not None and (lse.dtype != torch.float32 or lse.shape != shape[:3] or lse.get_device() != dev
+                                or not lse.is_contiguous()):
+            return False
+        if torch._C._cuda_getDevice() != dev:
+            return False
+    except (AttributeError, TypeError):
+        return False
+    B, H, N, D = shape
+    lib = load_library()
+    fn = lib.attn_fwd_bf16 if dt == torch.bfloat16 else lib.attn_fwd
+    rc = fn(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr() if lse is not None else None,
+            B, H, N, D, 1 if causal else 0, 1.0 / math.sqrt(D) if scale is None else float(scale),
+            _raw_stream(dev, stream))
+    if rc != 0:
+        raise AttnError(rc, "attn_fwd")
+    return True
+
+
 def attn_fwd_into(q, k, v, o, lse, causal: bool = True, scale: float | None = None, stream=None) -> None:
     """Write O into ``o`` ([B,H,N,D], q's dtype) and the natural-log LSE into ``lse``
     ([B,H,N] float32, or None) on ``stream`` (default: torch's current stream)."""
     import torch
 
+    if _fwd_fast(q, k, v, o, lse, causal, scale, stream):
+        return
     _check_qkv(q, k, v)
     B, H, N, D = q.shape
     if o.shape != q.shape or o.dtype != q.dtype or not o.is_contiguous() or o.device != q.device:

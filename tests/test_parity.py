@@ -148,3 +148,29 @@ def test_rejections_on_device(cuda_lib):
     with pytest.raises(eca.AttnError) as e:
         eca.attn_fwd(d96, d96, d96)
     assert e.value.status == -3
+
+
+def test_binding_fast_path_declines_bad_outputs(cuda_lib):
+    """attn_fwd_into's quick check passes anything unusual to the full checks, which
+    raise; a valid call gives the same bytes on the default and an explicit stream."""
+    import exact_causal_attention_gb300 as eca
+
+    g = torch.Generator(device="cuda").manual_seed(5)
+    q, k, v = (torch.randn(1, 2, 256, 64, device="cuda", generator=g).half() for _ in range(3))
+    o = torch.empty_like(q)
+    lse = torch.empty(1, 2, 256, device="cuda")
+    with pytest.raises(ValueError):
+        eca.attn_fwd_into(q, k, v, torch.empty_like(q, dtype=torch.bfloat16), lse)
+    with pytest.raises(ValueError):
+        eca.attn_fwd_into(q, k, v, o, torch.empty(1, 2, 256, device="cuda", dtype=torch.float16))
+    with pytest.raises(ValueError):
+        eca.attn_fwd_into(q, k, v, o, torch.empty(1, 2, 255, device="cuda"))
+    with pytest.raises(TypeError):
+        eca.attn_fwd_into(q, k.float(), v, o, lse)
+    eca.attn_fwd_into(q, k, v, o, lse)
+    s = torch.cuda.Stream()
+    o2, lse2 = torch.full_like(o, float("nan")), torch.full_like(lse, float("nan"))
+    torch.cuda.synchronize()
+    eca.attn_fwd_into(q, k, v, o2, lse2, stream=s)
+    s.synchronize()
+    assert torch.equal(o, o2) and torch.equal(lse, lse2)
