@@ -100,7 +100,8 @@ struct FwdParams {
 // Shared memory: Q of the unit's two query tiles, then a ring of stages.  A ring
 // item is {V_j-1, K_j}: the V tile of step j-1 and the K tile of step j, which
 // one step of each issuer consumes together (the first item of a unit holds K_0
-// alone, the last V_last alone).
+// alone, the last V_last alone).  Each part lands on its own barrier: a step's
+// P V MMAs need only V, so they go in while K is still arriving.
 template <int D>
 struct FwdSmem {
   static constexpr int kSub = D / 64;                      // 64-element column blocks per row
@@ -118,8 +119,9 @@ struct FwdSmem {
   // barrier indices
   static constexpr int kBarQFull = 0;                // + t: Q of tile t loaded
   static constexpr int kBarQFree = 2;                // + t: issuer t's last Q K^T of the unit done
-  static constexpr int kBarFull = 4;
-  static constexpr int kBarEmpty = kBarFull + kStages;  // two arrivals: both issuers
+  static constexpr int kBarFull = 4;                    // + slot: the item's V part landed (or it has none)
+  static constexpr int kBarFullK = kBarFull + kStages;  // + slot: the item's K part landed (or it has none)
+  static constexpr int kBarEmpty = kBarFullK + kStages;  // two arrivals: both issuers
   static constexpr int kBarS = kBarEmpty + kStages;  // + t: S_t computed
   static constexpr int kBarPa = kBarS + 2;           // + t: P_t of keys 0-63 written (and O_t rescaled)
   static constexpr int kBarPb = kBarPa + 2;          // + t: P_t of keys 64-127 written
@@ -241,6 +243,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int s = 0; s < L::kStages; ++s) {
       mbar_init(bar(L::kBarFull + s), 1);
+      mbar_init(bar(L::kBarFullK + s), 1);
       mbar_init(bar(L::kBarEmpty + s), 2);
     }
     for (int t = 0; t < 2; ++t) {
@@ -360,16 +363,23 @@ __global__ void __launch_bounds__(kThreads, 1)
             break;
           }
           const uint32_t stage = sbase + L::kRingOff + slot * L::kStageBytes;
-          const uint32_t full = bar(L::kBarFull + slot);
-          mbar_arrive_expect_tx(full, ((i > 0) + (i < w.n_max)) * L::kTileBytes);
+          // The V and K parts complete on barriers of their own, so the P V MMAs can
+          // start before K has landed; a missing part is a plain arrival.
+          const uint32_t full_v = bar(L::kBarFull + slot), full_k = bar(L::kBarFullK + slot);
           if (i > 0) {
+            mbar_arrive_expect_tx(full_v, L::kTileBytes);
             for (int s = 0; s < L::kSub; ++s)
-              tma_load_3d(stage + s * kSubTileBytes, &tm_v, full, 64 * s, (w.kv0 + i - 1) * kBlockN, w.kvh, pol_kv);
+              tma_load_3d(stage + s * kSubTileBytes, &tm_v, full_v, 64 * s, (w.kv0 + i - 1) * kBlockN, w.kvh, pol_kv);
+          } else {
+            mbar_arrive(full_v);
           }
           if (i < w.n_max) {
+            mbar_arrive_expect_tx(full_k, L::kTileBytes);
             for (int s = 0; s < L::kSub; ++s)
-              tma_load_3d(stage + L::kTileBytes + s * kSubTileBytes, &tm_k, full, 64 * s, (w.kv0 + i) * kBlockN,
+              tma_load_3d(stage + L::kTileBytes + s * kSubTileBytes, &tm_k, full_k, 64 * s, (w.kv0 + i) * kBlockN,
                           w.kvh, pol_kv);
+          } else {
+            mbar_arrive(full_k);
           }
           ++it;
         }
@@ -377,6 +387,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // Let every copy this thread started land before the block can exit.
       for (int x = (it > L::kStages ? it - L::kStages : 0); x < it; ++x) {
         wd.drain(bar(L::kBarFull + x % L::kStages), parity(x / L::kStages));
+        wd.drain(bar(L::kBarFullK + x % L::kStages), parity(x / L::kStages));
       }
     }
   } else if (warp == 11) {
@@ -453,7 +464,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         // Item 0 (K_0).  Every item is waited for and released by both issuers,
         // whether or not this tile uses it, so the ring's two-arrival phases stay aligned.
         if ((n_kv > 0 && !warp_wait(bar(L::kBarQFull + t), parity(q_loads++))) ||
-            !warp_wait(bar(L::kBarFull + it % L::kStages), parity(it / L::kStages))) {
+            !warp_wait(bar(L::kBarFull + it % L::kStages), parity(it / L::kStages)) ||
+            !warp_wait(bar(L::kBarFullK + it % L::kStages), parity(it / L::kStages))) {
           ok = false;
           break;
         }
@@ -499,7 +511,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             tc_fence_after_sync();
             issue_pv<D, BF16>(o_tmem, s_tmem, ring_v_desc + stage_off(it), true, 4, 8);
-            if (j + 1 < n_kv) issue_qk<D, BF16>(s_tmem, q_desc, ring_k_desc + stage_off(it));
+          }
+          if (!warp_wait(bar(L::kBarFullK + it % L::kStages), parity(it / L::kStages))) {
+            ok = false;
+            break;
+          }
+          if (j + 1 < n_kv) {
+            tc_fence_after_sync();
+            issue_qk<D, BF16>(s_tmem, q_desc, ring_k_desc + stage_off(it));
           }
           pass_turn();
           if (j < n_kv) {
