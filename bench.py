@@ -216,6 +216,74 @@ def bench_reference(args, w):
     print(json.dumps(line), flush=True)
 
 
+def bench_split(eca, inputs, dev, stream, flush):
+    """The key split on causal B=1 H=4 N=8192 D=128 fp16 (too few heads to fill the GPU), with the
+    default segment count, against the unsplit kernel; L2 flushed before every call."""
+    import torch
+
+    sw = inputs.Workload("causal_b1_h4_n8192_d128_fp16", 1, 4, 8192, 128, "fp16", True, 5)
+    sq, sk, sv = (x.to(dev) for x in inputs.workload_qkv(sw))
+    so = torch.empty_like(sq)
+    sl = torch.empty((sw.B, sw.H, sw.N), dtype=torch.float32, device=dev)
+    splits = eca.splitkv_default_splits(sw.B, sw.H, sw.N, sw.D)
+    need = eca.splitkv_workspace_bytes(sw.B, sw.H, sw.N, sw.D, splits)
+    ws = torch.empty(need + 256, dtype=torch.uint8, device=dev)
+    off = (-ws.data_ptr()) % 256
+    ws = ws[off:off + need]
+
+    def timed(fn):
+        times = []
+        for i in range(13):
+            flush.zero_()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            fn()
+            b.record(stream)
+            times.append((a, b))
+        torch.cuda.synchronize(dev)
+        ms = sorted(a.elapsed_time(b) for a, b in times[3:])
+        return ms[len(ms) // 2]
+
+    t_plain = timed(lambda: eca.attn_fwd_into(sq, sk, sv, so, sl, causal=True, scale=sw.scale, stream=stream))
+    t_split = timed(lambda: eca.attn_fwd_splitkv(sq, sk, sv, so, sl, kv_splits=splits, workspace=ws,
+                                                 causal=True, scale=sw.scale, stream=stream))
+    return {"workload": sw.name, "kv_splits": splits, "workspace_bytes": need,
+            "unsplit_ms": round(t_plain, 4), "unsplit_tflops": round(sw.flops / (t_plain * 1e-3) / 1e12, 1),
+            "split_ms": round(t_split, 4), "split_tflops": round(sw.flops / (t_split * 1e-3) / 1e12, 1),
+            "launches_per_call": 2}
+
+
+def bench_row_softmax(eca, inputs, dev, stream, flush):
+    """The fp32 online row softmax on the HBM-sized shape (larger than L2) and on the page's shape
+    (L2 flushed before each call); GB/s counts one read and one write per element."""
+    import torch
+
+    peaks_rs, kind_rs = measured_peaks()
+    row_softmax = {}
+    for (M, Ncols, seed), label in ((inputs.SOFTMAX_HBM_SHAPE, "hbm"), (inputs.SOFTMAX_PAGE_SHAPE, "page")):
+        xs = inputs.uniform_matrix(M, Ncols, seed).to(dev)
+        ys = torch.empty_like(xs)
+        times = []
+        for i in range(13):
+            if label == "page":
+                flush.zero_()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            eca.row_softmax(xs, ys, stream=stream)
+            b.record(stream)
+            times.append((a, b))
+        torch.cuda.synchronize(dev)
+        ms = sorted(a.elapsed_time(b) for a, b in times[3:])
+        med = ms[len(ms) // 2]
+        gbs = 8.0 * M * Ncols / (med * 1e-3) / 1e9
+        row_softmax[label] = {"M": M, "N": Ncols, "us": round(med * 1e3, 2), "GB_s": round(gbs, 1),
+                              "frac_of_hbm": round(gbs / float(peaks_rs["hbm_gbs"]), 3)}
+        del xs, ys
+    row_softmax["hbm_peak_gbs"] = float(peaks_rs["hbm_gbs"])
+    row_softmax["peak_kind"] = kind_rs
+    return row_softmax
+
+
 def bench_paged(eca, inputs, dev, stream, flush, contexts):
     """Paged GQA decode over the decode page's geometry (B=8, Hq=32, Hkv=8, D=128,
     page size 16): HBM-bound, it must stream 2 B L Hkv D s bytes of K/V per step.
@@ -436,39 +504,7 @@ def bench_ours(args, w):
             del sq, sk, sv, so, sl
 
     # Key split on a workload too small in B x H to fill the GPU (causal, B=1, H=4, N=8192, D=128).
-    splitkv = {}
-    if not args.no_sweep and rank == 0:
-        sw = inputs.Workload("causal_b1_h4_n8192_d128_fp16", 1, 4, 8192, 128, "fp16", True, 5)
-        sq, sk, sv = (x.to(dev) for x in inputs.workload_qkv(sw))
-        so = torch.empty_like(sq)
-        sl = torch.empty((sw.B, sw.H, sw.N), dtype=torch.float32, device=dev)
-        splits = eca.splitkv_default_splits(sw.B, sw.H, sw.N, sw.D)
-        need = eca.splitkv_workspace_bytes(sw.B, sw.H, sw.N, sw.D, splits)
-        ws = torch.empty(need + 256, dtype=torch.uint8, device=dev)
-        off = (-ws.data_ptr()) % 256
-        ws = ws[off:off + need]
-
-        def timed(fn):
-            times = []
-            for i in range(13):
-                flush.zero_()
-                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-                a.record(stream)
-                fn()
-                b.record(stream)
-                times.append((a, b))
-            torch.cuda.synchronize(dev)
-            ms = sorted(a.elapsed_time(b) for a, b in times[3:])
-            return ms[len(ms) // 2]
-
-        t_plain = timed(lambda: eca.attn_fwd_into(sq, sk, sv, so, sl, causal=True, scale=sw.scale, stream=stream))
-        t_split = timed(lambda: eca.attn_fwd_splitkv(sq, sk, sv, so, sl, kv_splits=splits, workspace=ws,
-                                                     causal=True, scale=sw.scale, stream=stream))
-        splitkv = {"workload": sw.name, "kv_splits": splits, "workspace_bytes": need,
-                   "unsplit_ms": round(t_plain, 4), "unsplit_tflops": round(sw.flops / (t_plain * 1e-3) / 1e12, 1),
-                   "split_ms": round(t_split, 4), "split_tflops": round(sw.flops / (t_split * 1e-3) / 1e12, 1),
-                   "launches_per_call": 2}
-        del sq, sk, sv, so, sl, ws
+    splitkv = bench_split(eca, inputs, dev, stream, flush) if (not args.no_sweep and rank == 0) else {}
 
     # Grouped key/value heads (GQA, 4 query heads per key/value head), causal B=1 H=32 Hkv=8 N=8192 D=128.
     gqa = {}
@@ -494,30 +530,7 @@ def bench_ours(args, w):
         del gq, gk, gv, go, gl
 
     # Online row softmax (fp32): an HBM-bound kernel, one read and one write per element.
-    row_softmax = {}
-    if not args.no_sweep and rank == 0:
-        peaks_rs, kind_rs = measured_peaks()
-        for (M, Ncols, seed), label in ((inputs.SOFTMAX_HBM_SHAPE, "hbm"), (inputs.SOFTMAX_PAGE_SHAPE, "page")):
-            xs = inputs.uniform_matrix(M, Ncols, seed).to(dev)
-            ys = torch.empty_like(xs)
-            times = []
-            for i in range(13):
-                if label == "page":
-                    flush.zero_()
-                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-                a.record(stream)
-                eca.row_softmax(xs, ys, stream=stream)
-                b.record(stream)
-                times.append((a, b))
-            torch.cuda.synchronize(dev)
-            ms = sorted(a.elapsed_time(b) for a, b in times[3:])
-            med = ms[len(ms) // 2]
-            gbs = 8.0 * M * Ncols / (med * 1e-3) / 1e9
-            row_softmax[label] = {"M": M, "N": Ncols, "us": round(med * 1e3, 2), "GB_s": round(gbs, 1),
-                                  "frac_of_hbm": round(gbs / float(peaks_rs["hbm_gbs"]), 3)}
-            del xs, ys
-        row_softmax["hbm_peak_gbs"] = float(peaks_rs["hbm_gbs"])
-        row_softmax["peak_kind"] = kind_rs
+    row_softmax = bench_row_softmax(eca, inputs, dev, stream, flush) if (not args.no_sweep and rank == 0) else {}
 
     paged = bench_paged(eca, inputs, dev, stream, flush, inputs.PAGED_CONTEXTS) if (not args.no_sweep and rank == 0) else {}
 
@@ -610,12 +623,15 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--paged-only", type=int, nargs="*", metavar="CONTEXT",
                     help="only the paged-decode measurement, at the given contexts (default: all)")
+    ap.add_argument("--softmax-only", action="store_true", help="only the row-softmax measurement")
+    ap.add_argument("--split-only", action="store_true", help="only the key-split measurement")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
     from exact_causal_attention_gb300 import inputs
 
     w = inputs.WORKLOADS[WORKLOAD]
-    if args.paged_only is not None:
+    if args.paged_only is not None or args.softmax_only or args.split_only:
+        # One side measurement alone (for profiling its kernels); one JSON line.
         import torch
 
         import exact_causal_attention_gb300 as eca
@@ -623,9 +639,15 @@ def main():
         eca.load_library()
         dev = torch.device("cuda", 0)
         flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
-        contexts = args.paged_only or list(inputs.PAGED_CONTEXTS)
-        paged = bench_paged(eca, inputs, dev, torch.cuda.current_stream(dev), flush, contexts)
-        print(json.dumps({"paged_decode": paged}), flush=True)
+        stream = torch.cuda.current_stream(dev)
+        if args.paged_only is not None:
+            contexts = args.paged_only or list(inputs.PAGED_CONTEXTS)
+            out = {"paged_decode": bench_paged(eca, inputs, dev, stream, flush, contexts)}
+        elif args.softmax_only:
+            out = {"row_softmax": bench_row_softmax(eca, inputs, dev, stream, flush)}
+        else:
+            out = {"splitkv": bench_split(eca, inputs, dev, stream, flush)}
+        print(json.dumps(out), flush=True)
         return
     if args.impl == "reference":
         bench_reference(args, w)
