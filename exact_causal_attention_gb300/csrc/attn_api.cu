@@ -734,6 +734,7 @@ int attn_row_softmax_f32(const float* x, float* y, long long M, int N, attn_stre
 #define ECA_BLOCK_ROWS(ITEMS)                                                                         \
   (vec ? eca::row_softmax_cached<256, ITEMS, true><<<row_blocks, 256, 0, s>>>(x, y, M, N)            \
        : eca::row_softmax_cached<256, ITEMS, false><<<row_blocks, 256, 0, s>>>(x, y, M, N))
+  const unsigned pair_blocks = static_cast<unsigned>((M + 1) / 2);  // 2 rows (128 threads each) per block
   if (N <= 32 * 4) {
     ECA_WARP_ROWS(4);
   } else if (N <= 32 * 8) {
@@ -744,8 +745,13 @@ int attn_row_softmax_f32(const float* x, float* y, long long M, int N, attn_stre
     ECA_WARP_ROWS(32);
   } else if (N <= 32 * 64) {
     ECA_WARP_ROWS(64);
-  } else if (N <= 256 * 16) {
-    ECA_BLOCK_ROWS(16);
+  } else if (N <= 128 * 32) {
+    // 128 threads per row: a short matrix (such as 1024 x 4096) fits in one wave.
+    if (vec) {
+      eca::row_softmax_cached<128, 32, true><<<pair_blocks, 256, 0, s>>>(x, y, M, N);
+    } else {
+      eca::row_softmax_cached<128, 32, false><<<pair_blocks, 256, 0, s>>>(x, y, M, N);
+    }
   } else if (N <= 256 * 32) {
     ECA_BLOCK_ROWS(32);
   } else if (N <= 256 * 64) {

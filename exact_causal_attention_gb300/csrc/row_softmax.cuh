@@ -9,6 +9,8 @@
 //
 // Schedules (rows contiguous, N elements each):
 //   * warp per row (section 4.9's layout), row held in registers: N <= 2048;
+//   * 128 threads per row, two rows per block, row held in registers: N <= 4096
+//     (a short matrix then still fits in one wave of blocks);
 //   * 256-thread block per row, row held in registers: N <= 16384;
 //   * 256-thread block per row, two passes over the row: larger N.
 // Loads and stores are 16-byte vectors when N is a multiple of 4 (rows then
@@ -54,19 +56,21 @@ __device__ __forceinline__ OnlineMD md_warp_reduce(OnlineMD s) {
   return s;
 }
 
-// Whole-block merge (256 threads = 8 warps), result broadcast to every thread.
+// Merge over each group of WPR consecutive warps of a 256-thread block (one row
+// per group), result broadcast to every thread of the group.
+template <int WPR>
 __device__ __forceinline__ OnlineMD md_block_reduce(OnlineMD s, OnlineMD* smem) {
   s = md_warp_reduce(s);
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   __syncthreads();  // smem may still be read from a previous reduction
   if (lane == 0) smem[warp] = s;
   __syncthreads();
-  OnlineMD t = lane < 8 ? smem[lane] : OnlineMD{-INFINITY, 0.f};
+  OnlineMD t = lane < WPR ? smem[warp / WPR * WPR + lane] : OnlineMD{-INFINITY, 0.f};
   t = md_warp_reduce(t);
   return t;
 }
 
-// Register-cached row softmax: TPR threads per row (32 or 256), ITEMS elements per
+// Register-cached row softmax: TPR threads per row (32, 128 or 256), ITEMS elements per
 // thread, VEC = float4 accesses.  Element e of a thread sits at position
 // (k * TPR + tid) * 4 + c for vectors (k = e / 4, c = e % 4), else k * TPR + tid.
 template <int TPR, int ITEMS, bool VEC>
@@ -100,7 +104,7 @@ __global__ void __launch_bounds__(256) row_softmax_cached(const float* x, float*
   }
 #pragma unroll
   for (int e = 0; e < ITEMS; ++e) md_push(s, v[e]);
-  s = TPR == 32 ? md_warp_reduce(s) : md_block_reduce(s, red);
+  s = TPR == 32 ? md_warp_reduce(s) : md_block_reduce<TPR / 32>(s, red);
   if (s.d == 0.f) s.m = 0.f;  // a row of -inf only: written as zeros
   const float inv = s.d > 0.f ? 1.f / s.d : 0.f;
   if (!active) return;
@@ -143,7 +147,7 @@ __global__ void __launch_bounds__(256) row_softmax_stream(const float* x, float*
   } else {
     for (int pos = threadIdx.x; pos < N; pos += 256) md_push(s, xr[pos]);
   }
-  s = md_block_reduce(s, red);
+  s = md_block_reduce<8>(s, red);
   if (s.d == 0.f) s.m = 0.f;  // a row of -inf only: written as zeros
   const float inv = s.d > 0.f ? 1.f / s.d : 0.f;
   if (VEC) {

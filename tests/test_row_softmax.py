@@ -37,7 +37,7 @@ def gpu_softmax(x_cpu, inplace=False, offset=0):
     return y.double().cpu().numpy()
 
 
-SHAPES = [(1024, 4096), (1025, 257), (3, 1), (5, 2048), (7, 2049), (2, 16384), (2, 16385), (1, 100000),
+SHAPES = [(1024, 4096), (3, 4096), (5, 3001), (1, 2052), (1025, 257), (3, 1), (5, 2048), (7, 2049), (2, 16384), (2, 16385), (1, 100000),
           (4, 33), (9, 128), (2, 4100), (300, 1000)]
 
 
