@@ -42,6 +42,7 @@ CASES = [
     (1, 1, 1, 64, "fp16", True, 4),
     (1, 2, 3000, 64, "bf16", False, 64),
     (1, 3, 1536, 128, "fp16", True, 5),
+    (1, 2, 2560, 128, "fp16", True, 20),  # rows see 1 to 20 segments: several merge batches
 ]
 
 
