@@ -253,6 +253,32 @@ def bench_split(eca, inputs, dev, stream, flush):
             "launches_per_call": 2}
 
 
+def bench_gqa(eca, inputs, dev, stream, flush):
+    """Grouped heads, causal B=1 H=32 Hkv=8 N=8192 D=128 fp16 (4 query heads per key/value head);
+    L2 flushed before every call; TFLOP/s counts 2BHN²D."""
+    import torch
+
+    gq, _, _ = inputs.make_qkv(1, 32, 8192, 128, "fp16", seed=6)
+    _, gk, gv = inputs.make_qkv(1, 8, 8192, 128, "fp16", seed=7)
+    gq, gk, gv = gq.to(dev), gk.to(dev), gv.to(dev)
+    go = torch.empty_like(gq)
+    gl = torch.empty((1, 32, 8192), dtype=torch.float32, device=dev)
+    times = []
+    for i in range(13):
+        flush.zero_()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        eca.attn_fwd_gqa(gq, gk, gv, causal=True, o=go, lse=gl, stream=stream)
+        b.record(stream)
+        times.append((a, b))
+    torch.cuda.synchronize(dev)
+    ms = sorted(a.elapsed_time(b) for a, b in times[3:])
+    med = ms[len(ms) // 2]
+    flops = 2.0 * 32 * 8192 * 8192 * 128
+    return {"workload": "causal_b1_h32_hkv8_n8192_d128_fp16", "ms": round(med, 4),
+            "tflops": round(flops / (med * 1e-3) / 1e12, 1)}
+
+
 def bench_row_softmax(eca, inputs, dev, stream, flush):
     """The fp32 online row softmax on the HBM-sized shape (larger than L2) and on the page's shape
     (L2 flushed before each call); GB/s counts one read and one write per element."""
@@ -507,27 +533,7 @@ def bench_ours(args, w):
     splitkv = bench_split(eca, inputs, dev, stream, flush) if (not args.no_sweep and rank == 0) else {}
 
     # Grouped key/value heads (GQA, 4 query heads per key/value head), causal B=1 H=32 Hkv=8 N=8192 D=128.
-    gqa = {}
-    if not args.no_sweep and rank == 0:
-        gq, _, _ = inputs.make_qkv(1, 32, 8192, 128, "fp16", seed=6)
-        _, gk, gv = inputs.make_qkv(1, 8, 8192, 128, "fp16", seed=7)
-        gq, gk, gv = gq.to(dev), gk.to(dev), gv.to(dev)
-        go = torch.empty_like(gq)
-        gl = torch.empty((1, 32, 8192), dtype=torch.float32, device=dev)
-        times = []
-        for i in range(13):
-            flush.zero_()
-            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            a.record(stream)
-            eca.attn_fwd_gqa(gq, gk, gv, causal=True, o=go, lse=gl, stream=stream)
-            b.record(stream)
-            times.append((a, b))
-        torch.cuda.synchronize(dev)
-        ms = sorted(a.elapsed_time(b) for a, b in times[3:])
-        med = ms[len(ms) // 2]
-        gqa = {"workload": "causal_b1_h32_hkv8_n8192_d128_fp16", "ms": round(med, 4),
-               "tflops": round(flops / (med * 1e-3) / 1e12, 1)}
-        del gq, gk, gv, go, gl
+    gqa = bench_gqa(eca, inputs, dev, stream, flush) if (not args.no_sweep and rank == 0) else {}
 
     # Online row softmax (fp32): an HBM-bound kernel, one read and one write per element.
     row_softmax = bench_row_softmax(eca, inputs, dev, stream, flush) if (not args.no_sweep and rank == 0) else {}
@@ -625,12 +631,13 @@ def main():
                     help="only the paged-decode measurement, at the given contexts (default: all)")
     ap.add_argument("--softmax-only", action="store_true", help="only the row-softmax measurement")
     ap.add_argument("--split-only", action="store_true", help="only the key-split measurement")
+    ap.add_argument("--gqa-only", action="store_true", help="only the grouped-head measurement")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
     from exact_causal_attention_gb300 import inputs
 
     w = inputs.WORKLOADS[WORKLOAD]
-    if args.paged_only is not None or args.softmax_only or args.split_only:
+    if args.paged_only is not None or args.softmax_only or args.split_only or args.gqa_only:
         # One side measurement alone (for profiling its kernels); one JSON line.
         import torch
 
@@ -645,6 +652,8 @@ def main():
             out = {"paged_decode": bench_paged(eca, inputs, dev, stream, flush, contexts)}
         elif args.softmax_only:
             out = {"row_softmax": bench_row_softmax(eca, inputs, dev, stream, flush)}
+        elif args.gqa_only:
+            out = {"gqa": bench_gqa(eca, inputs, dev, stream, flush)}
         else:
             out = {"splitkv": bench_split(eca, inputs, dev, stream, flush)}
         print(json.dumps(out), flush=True)
