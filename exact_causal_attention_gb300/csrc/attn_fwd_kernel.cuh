@@ -51,9 +51,12 @@
 //     current reference without first taking the new tile's row max.  No p may
 //     overflow the 16-bit P: a sum of at most 2^15 over keys 0-63 bounds each of
 //     their p, and a max score of keys 64-127 at most 15 above the reference
-//     bounds theirs.  Only the first key tile of a unit and the rare rows that
-//     fail a check take the row max, move the reference (rescaling O and l) and
-//     redo the tile from S, still intact in TMEM.
+//     bounds theirs.  Under the fixed assignment a unit whose first key tile is
+//     unmasked starts from a guessed reference, kept only if the row's sum of p
+//     is also at least 2^-8 (no underflow); otherwise the first key tile, the
+//     diagonal one and the rare rows that fail a check take the row max, move
+//     the reference (rescaling O and l) and redo the tile from S, still intact
+//     in TMEM.
 //   * P reaches the issuer in two halves: the P V MMAs of keys 0-63 run while
 //     the softmax exponentiates keys 64-127 (whose S columns it loaded while
 //     exponentiating keys 0-63).
@@ -71,6 +74,9 @@ constexpr int kSubTileBytes = 128 * 128;  // 128 rows x 64 16-bit elements (one 
 constexpr int kThreads = 384;
 constexpr int kTmemCols = 512;
 constexpr float kMaxRowSum = 32768.0f;  // bound on sum_j p_ij that keeps every p in fp16 range
+constexpr float kGuessRef = 4.0f;       // first reference of a unit (scores times scale log2 e)
+constexpr float kGuessDepth = 8.0f;     // a guess may sit at most this far above the row's max
+constexpr float kMinGuessSum = 1.0f / 256.0f;  // = 2^-kGuessDepth: sum of p accepted under a guess
 constexpr int kUnitQueue = 4;           // depth of the shared-memory queue of unit indices
 constexpr int kUnitReaders = 11;        // warps that read each queue entry: 8 softmax, 2 issuers, Q loader
 
@@ -565,7 +571,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (n_kv == 0) continue;
       const int tile = w.tile0 + t;
       const int row = tile * kBlockM + r_local;
-      float m_ref = -INFINITY;  // reference max, base-2 domain (already multiplied by c)
+      // Reference max, base-2 domain (already multiplied by c).  Under the fixed
+      // assignment a unit starts from a guess: on the first key tile the guess must
+      // also not sit far above the row (its p would underflow), and a rejected guess
+      // is replaced, not kept.  (The dynamic instance starts from the first tile's
+      // max: the guess's extra live values push it past its registers.)
+      constexpr bool kGuessFirst = !kDynamic;
+      float m_ref = kGuessFirst ? kGuessRef : -INFINITY;
       float l = 0.f;
       for (int j = 0; j < n_kv; ++j) {
         if (!warp_wait(bar(L::kBarS + t), parity(s_waits))) {
@@ -631,12 +643,17 @@ __global__ void __launch_bounds__(kThreads, 1)
 
         float alpha = 1.f;
         float row_sum = 0.f;
-        bool move = true;  // the first key tile of a unit has no reference yet
-        if (j > 0) {
+        bool move = true;  // without a guess, the first key tile takes the row max
+        if (kGuessFirst || j > 0) {
           const bool masked = (p.causal && w.kv0 + j == tile) || (ragged_keys && w.kv0 + j == p.n_tiles - 1);
-          if (masked) {
+          if (masked && j == 0) {
+            // A row's own first keys (the diagonal tile): take their max, as a guessed
+            // reference would round a lone key's p in 16 bits where p = 1 is exact.
+            move = true;
+          } else if (masked) {
             load_scores();
             row_sum = exponentiate(-m_ref);
+            move = !(row_sum <= kMaxRowSum);  // (also an inf sum)
           } else {
             // Keys 64-127 load while keys 0-63 are exponentiated.
             tmem_ld_x32(t_s, s[0]);
@@ -662,7 +679,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             // reference must hold for the whole row now: keys 0-63 are safe when
             // their sum of p is at most the bound, keys 64-127 when their max score
             // is at most log2(bound) = 15 above the reference.
-            const bool fast = sum_a <= kMaxRowSum && fmaxf(mx[0], mx[1]) * c - m_ref <= 15.f;
+            const float top_b = fmaxf(mx[0], mx[1]) * c - m_ref;
+            const bool fast = sum_a <= kMaxRowSum && top_b <= 15.f &&
+                              (j > 0 || sum_a >= kMinGuessSum || top_b >= -kGuessDepth);
             if (__all_sync(0xffffffffu, fast)) {
               tmem_st_x32(t_s, pk[0]);
               tmem_wait_st();
@@ -682,8 +701,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             load_scores();
             row_sum = exponentiate(-m_ref);
+            // A guess is kept only if the row's p do not underflow (an inf sum also moves).
+            move = !(row_sum <= kMaxRowSum) || (j == 0 && !(row_sum >= kMinGuessSum));
           }
-          move = !(row_sum <= kMaxRowSum);  // also true for an overflowed (inf) sum
         }
         if (__any_sync(0xffffffffu, move)) {
           load_scores();  // S is still intact in TMEM: P has not been stored yet
@@ -696,8 +716,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 mx[q] = fmax3(mx[q], __uint_as_float(s[q][i]), __uint_as_float(s[q][i + 1]));
             }
             const float m_tile = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * c;
-            const float m_new = fmaxf(m_ref, m_tile);
-            alpha = m_ref == -INFINITY ? 0.f : ex2(m_ref - m_new);
+            const float m_new = j == 0 ? m_tile : fmaxf(m_ref, m_tile);
+            alpha = (j == 0 || m_ref == -INFINITY) ? 0.f : ex2(m_ref - m_new);
             m_ref = m_new;
           }
           row_sum = exponentiate(m_ref == -INFINITY ? 0.f : -m_ref);

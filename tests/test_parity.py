@@ -174,3 +174,26 @@ def test_binding_fast_path_declines_bad_outputs(cuda_lib):
     eca.attn_fwd_into(q, k, v, o2, lse2, stream=s)
     s.synchronize()
     assert torch.equal(o, o2) and torch.equal(lse, lse2)
+
+
+@pytest.mark.parametrize("D", [64, 128])
+@pytest.mark.parametrize("x_row", [-60.0, -6.0, 34.0])
+def test_rows_far_from_the_first_reference(cuda_lib, D, x_row):
+    """Every key equal, so each causal row's scores are one value x_row (in units of
+    scale * log2 e): the output is the running mean of V and lse = s + ln(i + 1).
+    The first key tile's reference then sits 64 above the row (p would underflow
+    in 16 bits unless the tile's own max replaces it), 10 above (kept: p ~ 2^-10),
+    or 30 below (p would overflow, so the max replaces it)."""
+    B, H, N = 1, 2, 384
+    scale = 1.0 / math.sqrt(D)
+    u = torch.ones(D)
+    a = x_row / (scale * D * math.log2(math.e))  # q = a u, k = u: s = a D scale
+    q = (a * u).expand(B, H, N, D).contiguous().half()
+    k = u.expand(B, H, N, D).contiguous().half()
+    g = torch.Generator().manual_seed(9)
+    v = torch.randn(B, H, N, D, generator=g).half()
+    o, lse = run_gpu(q, k, v, True, scale)
+    ro, rl = oracle_full(q, k, v, "fp16", True, scale)
+    compare(o, lse, ro, rl, "fp16")
+    prefix = np.cumsum(v.double().numpy(), axis=2) / np.arange(1, N + 1)[None, None, :, None]
+    assert np.abs(o - prefix).max() <= 4e-3
