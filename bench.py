@@ -43,6 +43,24 @@ def rank_env():
             int(os.environ.get("LOCAL_RANK", "0")))
 
 
+def max_over_ranks(x: float, device="cpu") -> float:
+    """The largest x over the ranks of the default process group (x itself without one)."""
+    import torch
+    import torch.distributed as dist
+
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_tflops(flops_per_step: float, steps: int, world: int, max_ms: float) -> float:
+    """Every rank runs the same workload (independent replicas): all ranks' work over the
+    slowest rank's time."""
+    return flops_per_step * steps * world / (max_ms * 1e-3) / 1e12
+
+
 def host_cores():
     try:
         return len(os.sched_getaffinity(0))
@@ -191,7 +209,7 @@ def bench_reference(args, w):
 
     q, k, v = inputs.workload_qkv(w)
     sampler = OracleSampler(q, k, v, w)
-    per_step = max(0.02, 60.0 / max(1, args.steps + args.warmup))
+    per_step = max(0.02, args.reference_seconds / max(1, args.steps + args.warmup))
     for s in range(args.warmup):
         sampler.timed(per_step, seed=100 + s)
     flops, secs, nrows = 0.0, 0.0, 0
@@ -419,16 +437,12 @@ def bench_ours(args, w):
     barrier()
     clocks = sampler.stop()
     step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
-    total_ms = sum(step_ms)
-    if world > 1:
-        t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(sum(step_ms), dev)
     status = eca.device_status()
     if status != 0:
         raise RuntimeError("a kernel wait timed out in the timed region")
     flops = w.flops
-    value = flops * args.steps * world / (total_ms * 1e-3) / 1e12
+    value = whole_job_tflops(flops, args.steps, world, total_ms)
     kernel_ms = total_ms / args.steps
 
     # End to end through the C ABI: pinned host q, k, v in, o and lse out, every step.
@@ -481,11 +495,7 @@ def bench_ours(args, w):
     s_up.wait_stream(stream)
     e1.record(s_up)
     barrier()
-    e2e_ms = e0.elapsed_time(e1) / e2e_steps
-    if world > 1:
-        t = torch.tensor([e2e_ms], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / e2e_steps, dev)
     if eca.device_status() != 0:
         raise RuntimeError("a kernel wait timed out in the end-to-end loop")
     h2d = sum(x.numel() * x.element_size() for x in (hq, hk, hv))
@@ -627,6 +637,8 @@ def main():
     ap.add_argument("--no-peak", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--reference-seconds", type=float, default=60.0,
+                    help="--impl reference: oracle time over warm-up and timed steps together")
     ap.add_argument("--paged-only", type=int, nargs="*", metavar="CONTEXT",
                     help="only the paged-decode measurement, at the given contexts (default: all)")
     ap.add_argument("--softmax-only", action="store_true", help="only the row-softmax measurement")

@@ -1,0 +1,70 @@
+"""Host side of multi-rank runs, on CPU with two gloo ranks (no GPU).
+
+The path shards with no exchange (every (batch, head) slice is independent), so a
+run on N GPUs is N replicas: bench.py times each rank, takes the slowest rank's
+time and counts all ranks' work.  These tests run that reduction across two real
+processes, and the reference arm under torchrun (rank 0 alone prints its line)."""
+import json
+import os
+import socket
+import subprocess
+import sys
+
+import pytest
+import torch.multiprocessing as mp
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+sys.path.insert(0, ROOT)
+
+import bench  # noqa: E402
+
+
+def _free_port() -> int:
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _rank_main(rank, world, port, out_dir):
+    import torch.distributed as dist
+
+    os.environ["MASTER_ADDR"] = "127.0.0.1"
+    os.environ["MASTER_PORT"] = str(port)
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        ms = 10.0 + 7.5 * rank  # rank 1 is the slower one
+        worst = bench.max_over_ranks(ms, "cpu")
+        value = bench.whole_job_tflops(1.0e12, 4, world, worst)
+        with open(os.path.join(out_dir, f"rank{rank}.json"), "w") as f:
+            json.dump({"worst": worst, "value": value}, f)
+    finally:
+        dist.destroy_process_group()
+
+
+def test_slowest_rank_sets_the_time(tmp_path):
+    world = 2
+    mp.start_processes(_rank_main, args=(world, _free_port(), str(tmp_path)), nprocs=world, join=True,
+                       start_method="spawn")
+    got = [json.load(open(tmp_path / f"rank{r}.json")) for r in range(world)]
+    assert [g["worst"] for g in got] == [17.5, 17.5]
+    # 2 ranks x 4 steps x 1e12 FLOP in 17.5 ms
+    assert all(g["value"] == pytest.approx(8.0e12 / 17.5e-3 / 1e12) for g in got)
+
+
+def test_single_process_needs_no_group():
+    assert bench.max_over_ranks(3.25) == 3.25
+    assert bench.whole_job_tflops(2.0e12, 10, 1, 20.0) == pytest.approx(1000.0)
+
+
+def test_reference_arm_prints_once_under_torchrun():
+    cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", "--nproc-per-node", "2",
+           "--master-addr", "127.0.0.1", "--master-port", str(_free_port()),
+           os.path.join(ROOT, "bench.py"), "--impl", "reference", "--gpus", "2", "--steps", "1",
+           "--warmup", "3", "--reference-seconds", "1"]
+    r = subprocess.run(cmd, cwd=ROOT, capture_output=True, text=True, timeout=600)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [ln for ln in r.stdout.splitlines() if ln.startswith("{")]
+    assert len(lines) == 1, r.stdout
+    line = json.loads(lines[0])
+    assert line["impl"] == "reference" and line["n_gpus"] == 2 and line["value"] > 0
+    assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["cpu_baseline"]["kind"] == "oracle"
