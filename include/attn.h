@@ -20,7 +20,10 @@
  * j <= i).  Arithmetic: fp16/bf16 products accumulated in fp32 on the tensor
  * cores, running max m, sum l and unnormalised output o kept in fp32 (the page's
  * section 2), probabilities rounded to the input type before the P V product,
- * O rounded to nearest even.
+ * O rounded to nearest even.  The kernel's m is a reference that may trail the
+ * row's max (or start from a fixed guess) as long as no probability can leave
+ * the 16-bit range or underflow it; the recurrence gives the same O and lse for
+ * any reference, so this changes only rounding.
  *
  * Ownership: every pointer is device memory owned by the caller; the library
  * allocates nothing per call and keeps no reference after the call returns.
