@@ -647,8 +647,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (kGuessFirst || j > 0) {
           const bool masked = (p.causal && w.kv0 + j == tile) || (ragged_keys && w.kv0 + j == p.n_tiles - 1);
           if (masked && j == 0) {
-            // A row's own first keys (the diagonal tile): take their max, as a guessed
-            // reference would round a lone key's p in 16 bits where p = 1 is exact.
+            // A masked first tile (the diagonal, or the only, ragged, key tile) holds a
+            // row's first keys: take their max, as a guessed reference would round a
+            // lone key's p in 16 bits where p = 1 is exact.
             move = true;
           } else if (masked) {
             load_scores();
