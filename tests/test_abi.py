@@ -87,6 +87,12 @@ def test_binding_rejects_cpu_tensors():
     x = torch.zeros(1, 1, 4, 64, dtype=torch.float16)
     with pytest.raises(TypeError):
         eca.attn_fwd(x, x, x)
+    # attn_fwd_into's quick check declines what it cannot pass and the full checks raise
+    lse = torch.zeros(1, 1, 4)
+    with pytest.raises(TypeError):
+        eca.attn_fwd_into(x, x, x, torch.empty_like(x), lse)
+    with pytest.raises((TypeError, ValueError)):
+        eca.attn_fwd_into(x[0], x[0], x[0], torch.empty_like(x[0]), None)
 
 
 def test_splitkv_workspace_size_without_gpu(lib):
