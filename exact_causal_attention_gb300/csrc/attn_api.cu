@@ -294,16 +294,20 @@ int launch(const void* q, const void* k, const void* v, void* o, float* lse, int
   p.status = st->status;
   p.N = N;
   p.n_tiles = (N + eca::kBlockM - 1) / eca::kBlockM;
-  p.n_pairs = (p.n_tiles + 1) / 2;
+  // Causal grouped heads pair two heads of a key/value group at one query tile:
+  // both tiles then need the same key tiles.
+  p.head_pair = (part_o == nullptr && causal && (H / Hkv) % 2 == 0) ? 1 : 0;
+  p.n_pairs = p.head_pair ? p.n_tiles : (p.n_tiles + 1) / 2;
   p.BH = BH;
   p.H = H;
   p.Hkv = Hkv;
   p.splits = ks.splits;
   p.seg_tiles = ks.seg_tiles;
-  p.n_units = p.n_pairs * BH * ks.splits;
+  p.n_units = p.n_pairs * (BH >> p.head_pair) * ks.splits;
   const unsigned long long kv_bytes = 4ull * static_cast<unsigned long long>(B) * Hkv * N * D;  // K and V, 16-bit
-  p.group_heads = unit_group_heads(BH, H / Hkv, p.n_pairs * ks.splits, st->sm_count, kv_bytes);
-  const bool dynamic = p.group_heads < BH;
+  p.group_heads = unit_group_heads(BH >> p.head_pair, (H / Hkv) >> p.head_pair, p.n_pairs * ks.splits,
+                                   st->sm_count, kv_bytes);
+  const bool dynamic = p.group_heads < (BH >> p.head_pair);
   p.sched = st->sched_pool + 64 * (st->sched_next++ % kSchedSlots);
   p.causal = causal ? 1 : 0;
   p.scale_log2e = scale * 1.4426950408889634f;

@@ -96,6 +96,7 @@ struct FwdParams {
   int seg_tiles;  // key tiles per segment
   int n_units;    // n_pairs * BH * splits
   int group_heads;  // slices per group in the unit order (the last group may be smaller)
+  int head_pair;    // 1: a unit is one query tile of two heads of a key/value group (slices are head pairs)
   int* sched;     // [0]: next unit to hand out, [32]: CTAs finished; both back to 0 at exit
   int causal;
   float scale_log2e;  // scale * log2(e)
@@ -164,27 +165,28 @@ struct Unit {
 // key segment.
 __device__ __forceinline__ void unit_from(int l, const FwdParams& p, Unit& u) {
   const int per_slice = p.n_pairs * p.splits;
-  const int full_groups = p.BH / p.group_heads;
+  const int slices = p.BH >> p.head_pair;
+  const int full_groups = slices / p.group_heads;
   int grp = l / (p.group_heads * per_slice);
   int g = p.group_heads;
   int local = l - grp * (p.group_heads * per_slice);
   if (grp >= full_groups) {  // the smaller last group
     grp = full_groups;
-    g = p.BH - full_groups * p.group_heads;
+    g = slices - full_groups * p.group_heads;
     local = l - full_groups * (p.group_heads * per_slice);
   }
   u.seg = local % p.splits;
   const int r = local / p.splits;
-  u.bh = grp * p.group_heads + r % g;
+  u.bh = (grp * p.group_heads + r % g) << p.head_pair;
   u.kvh = (u.bh / p.H) * p.Hkv + (u.bh % p.H) / (p.H / p.Hkv);
-  const int pair = p.n_pairs - 1 - r / g;
-  u.tile0 = 2 * pair;
+  const int pair = p.n_pairs - 1 - r / g;  // with head pairs, the query tile
+  u.tile0 = p.head_pair ? pair : 2 * pair;
   u.kv0 = u.seg * p.seg_tiles;
   const int kv_end = u.kv0 + p.seg_tiles < p.n_tiles ? u.kv0 + p.seg_tiles : p.n_tiles;
-  const bool has1 = u.tile0 + 1 < p.n_tiles;
+  const bool has1 = p.head_pair || u.tile0 + 1 < p.n_tiles;
   // key tiles each query tile needs in total, then the part inside this segment
   const int need0 = p.causal ? u.tile0 + 1 : p.n_tiles;
-  const int need1 = has1 ? (p.causal ? u.tile0 + 2 : p.n_tiles) : 0;
+  const int need1 = has1 ? (p.causal ? u.tile0 + 2 - p.head_pair : p.n_tiles) : 0;
   const int e0 = need0 < kv_end ? need0 : kv_end;
   const int e1 = need1 < kv_end ? need1 : kv_end;
   u.n_kv0 = e0 > u.kv0 ? e0 - u.kv0 : 0;
@@ -417,7 +419,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           mbar_arrive_expect_tx(bar(L::kBarQFull + t), L::kTileBytes);
           for (int s = 0; s < L::kSub; ++s) {
             tma_load_3d(sbase + L::kQOff + t * L::kTileBytes + s * kSubTileBytes, &tm_q, bar(L::kBarQFull + t),
-                        64 * s, (w.tile0 + t) * kBlockM, w.bh, pol_q);
+                        64 * s, (w.tile0 + (p.head_pair ? 0 : t)) * kBlockM, w.bh + (p.head_pair ? t : 0), pol_q);
           }
           ++loads[t];
         }
@@ -569,7 +571,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       const int n_kv = t ? w.n_kv1 : w.n_kv0;
       if (n_kv == 0) continue;
-      const int tile = w.tile0 + t;
+      const int tile = w.tile0 + (p.head_pair ? 0 : t);
+      const int head = w.bh + (p.head_pair ? t : 0);
       const int row = tile * kBlockM + r_local;
       // Reference max, base-2 domain (already multiplied by c).  Under the fixed
       // assignment a unit starts from a guess: on the first key tile the guess must
@@ -766,7 +769,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float2 il2 = make_float2(inv_l, inv_l);
       const float row_lse = (m_ref + log2f(l)) * 0.69314718055994530942f;
       if (p.part_o != nullptr) {
-        const size_t prow = (static_cast<size_t>(w.seg) * p.BH + w.bh) * p.N + static_cast<size_t>(row);
+        const size_t prow = (static_cast<size_t>(w.seg) * p.BH + head) * p.N + static_cast<size_t>(row);
         float* dst = p.part_o + prow * D;
 #pragma unroll
         for (int c0 = 0; c0 < D; c0 += 32) {
@@ -823,12 +826,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) {
-          tma_store_3d(&tm_o, slab, 64 * c64, tile * kBlockM + wq * 32, w.bh);
+          tma_store_3d(&tm_o, slab, 64 * c64, tile * kBlockM + wq * 32, head);
           bulk_commit_group();
         }
       }
       if (p.lse != nullptr && row < p.N) {
-        p.lse[static_cast<size_t>(w.bh) * p.N + row] = row_lse;
+        p.lse[static_cast<size_t>(head) * p.N + row] = row_lse;
       }
     }
     if (lane == 0) bulk_wait_all();  // every output store has landed before the block exits
