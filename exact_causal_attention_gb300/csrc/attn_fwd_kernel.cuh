@@ -24,8 +24,11 @@
 //     the segment's normalised partial output and log-sum-exp in fp32 for a
 //     separate merge ("CUDA KV Cache：分页存储与长上下文 Decode 极致优化",
 //     section 6.4).  Grouped heads (same page, section 3.3): query head h
-//     reads key/value head h / (H / Hkv) directly, with no copy; the heads of
-//     one group are adjacent in the unit order so their K/V tiles come from L2.
+//     reads key/value head h / (H / Hkv) directly, with no copy.  Causal
+//     unsplit launches with an even group pair two heads of a group at one query
+//     tile instead of two consecutive tiles, so each K/V tile serves both query
+//     heads in the CTA and both need the same key tiles; the heads of a group
+//     are adjacent in the unit order so their K/V tiles come from L2.
 //     384 threads:
 //       warps 0-3  softmax for query tile 0     warps 4-7  softmax for query tile 1
 //       warp 8     takes units; TMA producer of the ring items {V_j, K_j+1}
