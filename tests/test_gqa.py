@@ -40,6 +40,7 @@ CASES = [
     (1, 32, 8, 2048, 128, "fp16", True),
     (1, 6, 3, 129, 64, "fp16", True),
     (2, 4, 4, 257, 128, "bf16", True),
+    (1, 6, 2, 500, 128, "fp16", True),  # three heads per group: consecutive-tile units, not head pairs
 ]
 
 
