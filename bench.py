@@ -61,6 +61,14 @@ def whole_job_tflops(flops_per_step: float, steps: int, world: int, max_ms: floa
     return flops_per_step * steps * world / (max_ms * 1e-3) / 1e12
 
 
+def executed_flops(w) -> float:
+    """MMA FLOPs the kernel executes: every 128 x 128 (query tile, key tile) block it visits,
+    the diagonal and ragged blocks counted in full (Q K^T and P V, 2 * 128 * 128 * D each)."""
+    n = -(-w.N // 128)
+    blocks = n * (n + 1) // 2 if w.causal else n * n
+    return 4.0 * 128 * 128 * w.D * w.B * w.H * blocks
+
+
 def host_cores():
     try:
         return len(os.sched_getaffinity(0))
@@ -600,7 +608,7 @@ def bench_ours(args, w):
         "vs_baseline": value / world / (flops / (PAGE_MS_N8192 * 1e-3) / 1e12),
         "dtype": "fp16", "data": "synthetic",
         "config": {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "D": w.D, "causal": w.causal,
-                   "seed": w.seed, "flops_per_step": flops,
+                   "seed": w.seed, "flops_per_step": flops, "executed_flops_per_step": executed_flops(w),
                    "l2": "flushed between timed steps (256 MiB write, outside the events)",
                    "parallelism": f"replicas x{world}"},
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",

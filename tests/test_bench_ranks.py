@@ -1,4 +1,5 @@
-"""Host side of multi-rank runs, on CPU with two gloo ranks (no GPU).
+"""Host side of bench.py on CPU (no GPU): multi-rank runs with two gloo ranks, and
+the FLOP accounting.
 
 The path shards with no exchange (every (batch, head) slice is independent), so a
 run on N GPUs is N replicas: bench.py times each rank, takes the slowest rank's
@@ -68,3 +69,12 @@ def test_reference_arm_prints_once_under_torchrun():
     line = json.loads(lines[0])
     assert line["impl"] == "reference" and line["n_gpus"] == 2 and line["value"] > 0
     assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["cpu_baseline"]["kind"] == "oracle"
+
+
+def test_executed_flops_exceed_the_algorithmic_count_by_the_diagonal_blocks():
+    from exact_causal_attention_gb300 import inputs
+
+    w = inputs.WORKLOADS["causal_b1_h32_n8192_d128_fp16"]
+    assert bench.executed_flops(w) == pytest.approx(w.flops * 65 / 64)  # (n + 1) / n with n = 64 tiles
+    nc = w.with_causal(False)
+    assert bench.executed_flops(nc) == pytest.approx(nc.flops)  # no diagonal: every block is full work
