@@ -56,10 +56,12 @@
 //     their p, and a max score of keys 64-127 at most 15 above the reference
 //     bounds theirs.  Under the fixed assignment a unit whose first key tile is
 //     unmasked starts from a guessed reference, kept only if the row's sum of p
-//     is also at least 2^-8 (no underflow); otherwise the first key tile, the
-//     diagonal one and the rare rows that fail a check take the row max, move
-//     the reference (rescaling O and l) and redo the tile from S, still intact
-//     in TMEM.
+//     over that tile is at least 1: then l >= 1 from the first tile on, as with
+//     the row max as reference, so a p that lands in fp16's subnormal range
+//     carries no more rounding relative to l than it would there.  Otherwise the
+//     first key tile, the diagonal one and the rare rows that fail a check take
+//     the row max, move the reference (rescaling O and l) and redo the tile from
+//     S, still intact in TMEM.
 //   * P reaches the issuer in two halves: the P V MMAs of keys 0-63 run while
 //     the softmax exponentiates keys 64-127 (whose S columns it loaded while
 //     exponentiating keys 0-63).
@@ -78,8 +80,7 @@ constexpr int kThreads = 384;
 constexpr int kTmemCols = 512;
 constexpr float kMaxRowSum = 32768.0f;  // bound on sum_j p_ij that keeps every p in fp16 range
 constexpr float kGuessRef = 4.0f;       // first reference of a unit (scores times scale log2 e)
-constexpr float kGuessDepth = 8.0f;     // a guess may sit at most this far above the row's max
-constexpr float kMinGuessSum = 1.0f / 256.0f;  // = 2^-kGuessDepth: sum of p accepted under a guess
+constexpr float kMinGuessSum = 1.0f;    // a guess is kept only if the first tile's sum of p reaches this
 constexpr int kUnitQueue = 4;           // depth of the shared-memory queue of unit indices
 constexpr int kUnitReaders = 11;        // warps that read each queue entry: 8 softmax, 2 issuers, Q loader
 
@@ -148,8 +149,10 @@ struct FwdSmem {
   static_assert(kDynamicBytes <= 227 * 1024, "shared memory exceeds the per-block limit");
 };
 
-// One work unit: query tiles 2*pair and 2*pair + 1 of slice bh, against the
-// key tiles kv0 .. kv0 + n_kv - 1 of key segment seg.
+// One work unit, against the key tiles kv0 .. kv0 + n_kv - 1 of key segment seg:
+// query tiles 2*pair and 2*pair + 1 of slice bh; or, with head_pair set, query
+// tile `pair` (tile0 = pair) of the two heads bh and bh + 1, which read the same
+// key/value head.
 struct Unit {
   int bh;
   int kvh;  // key/value slice: query head h of batch b reads head h / (H / Hkv) of batch b
@@ -685,10 +688,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             // Keys 0-63 are handed over before keys 64-127 are exponentiated, so the
             // reference must hold for the whole row now: keys 0-63 are safe when
             // their sum of p is at most the bound, keys 64-127 when their max score
-            // is at most log2(bound) = 15 above the reference.
+            // is at most log2(bound) = 15 above the reference.  A guess (first tile)
+            // also needs the row's sum of p to reach 1, which keys 0-63 show by their
+            // sum and keys 64-127 by a max score at or above the reference (p >= 1).
             const float top_b = fmaxf(mx[0], mx[1]) * c - m_ref;
             const bool fast = sum_a <= kMaxRowSum && top_b <= 15.f &&
-                              (j > 0 || sum_a >= kMinGuessSum || top_b >= -kGuessDepth);
+                              (j > 0 || sum_a >= kMinGuessSum || top_b >= 0.f);
             if (__all_sync(0xffffffffu, fast)) {
               tmem_st_x32(t_s, pk[0]);
               tmem_wait_st();
@@ -708,7 +713,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             load_scores();
             row_sum = exponentiate(-m_ref);
-            // A guess is kept only if the row's p do not underflow (an inf sum also moves).
+            // A guess is kept only if the row's sum of p reaches 1 (an inf sum also moves).
             move = !(row_sum <= kMaxRowSum) || (j == 0 && !(row_sum >= kMinGuessSum));
           }
         }
@@ -837,7 +842,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         p.lse[static_cast<size_t>(head) * p.N + row] = row_lse;
       }
     }
-    if (lane == 0) bulk_wait_all();  // every output store has landed before the block exits
+    // The staging slabs must stay valid until the stores have read them; the
+    // writes themselves complete before the grid does.
+    if (lane == 0) bulk_wait_read_all();
   }
 
   tc_fence_before_sync();
