@@ -126,6 +126,30 @@ def test_splitkv_argument_errors_without_gpu(lib, fn):
     assert c(D=96) == -3
 
 
+def test_noalloc_argument_errors_without_gpu(lib):
+    """attn_fwd_splitkv_noalloc refuses bad split counts, the usual argument errors and
+    a split whose partials need more than its fixed 64 MiB scratch, all before any CUDA
+    call (the addresses here are never dereferenced)."""
+    f = lib.attn_fwd_splitkv_noalloc
+
+    def c(splits=2, **kw):
+        a = dict(q=A, k=A + SZ, v=A + 2 * SZ, o=A + 3 * SZ, lse=None, B=1, H=1, N=512, D=64, causal=1,
+                 scale=0.125)
+        a.update(kw)
+        return f(a["q"], a["k"], a["v"], a["o"], a["lse"], a["B"], a["H"], a["N"], a["D"], a["causal"],
+                 a["scale"], splits, None)
+
+    assert c(splits=0) == -1
+    assert c(splits=65) == -1
+    assert c(q=None) == -1
+    assert c(D=96) == -3
+    assert c(q=A + 2) == -2
+    assert c(o=A + 16) == -1
+    # 4 segments of B*H*N*D fp32 partials: 4 * 8 * 8192 * 128 * 4 B = 128 MiB > 64 MiB
+    big = 8 * 8192 * 128 * 2
+    assert c(splits=4, q=A, k=A + big, v=A + 2 * big, o=A + 3 * big, H=8, N=8192, D=128) == -8
+
+
 def test_splitkv_adjacent_workspace_is_not_overlap(lib):
     # q, k, v, o of 1*1*512*64*2 = 64 KiB each; a workspace starting right after o is legal.
     io = 512 * 64 * 2

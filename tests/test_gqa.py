@@ -50,7 +50,8 @@ def test_gqa_matches_oracle(cuda_lib, B, H, Hkv, N, D, dtype, causal):
     scale = 1.0 / math.sqrt(D)
     o, lse = run(q, k, v, causal, scale)
     ro, rl = oracle_full(q, k, v, dtype, causal, scale)
-    compare(o, lse, ro, rl, dtype, p_rounding_term(q, k, v, dtype, causal, scale))
+    compare(o, lse, ro, rl, dtype, p_rounding_term(q, k, v, dtype, causal, scale),
+            name=f"gqa_b{B}_h{H}_hkv{Hkv}_n{N}_d{D}_{dtype}_{'causal' if causal else 'noncausal'}")
 
 
 def test_gqa_equals_mha_on_expanded_heads(cuda_lib):
@@ -67,10 +68,23 @@ def test_gqa_equals_mha_on_expanded_heads(cuda_lib):
     assert np.array_equal(o, oe) and np.array_equal(lse, lsee)
 
 
+@pytest.mark.parametrize("H,Hkv", [(80, 40), (160, 40), (120, 40)])
+def test_gqa_with_units_taken_dynamically_all_rows(cuda_lib, H, Hkv):
+    # K and V of 84 MB (more than the 64 MiB below which one group is used): units
+    # are grouped by heads (whole groups of query heads sharing a K/V head) and
+    # handed out from a global counter; groups of 2 and 4 heads make head-pair units,
+    # groups of 3 consecutive-tile units.  Every row is compared with the oracle.
+    B, N, D = 2, 2048, 128
+    q, k, v = make(B, H, Hkv, N, D, "fp16", seed=4400 + H)
+    scale = 1.0 / math.sqrt(D)
+    o, lse = run(q, k, v, True, scale)
+    ro, rl = oracle_full(q, k, v, "fp16", True, scale)
+    compare(o, lse, ro, rl, "fp16", name=f"gqa_dynamic_b{B}_h{H}_hkv{Hkv}_n{N}_d{D}_fp16_causal")
+
+
 def test_gqa_with_units_taken_dynamically(cuda_lib):
-    # K and V of 134 MB: units are grouped by heads (whole groups of query heads
-    # sharing a K/V head) and handed out from a global counter.  Every row is
-    # written, sampled rows match the oracle, and a repeat launch is bit-identical.
+    # K and V of 134 MB at a long length: every row is written, sampled rows match
+    # the oracle, and a repeat launch is bit-identical.
     from helpers import oracle_rows, sample_rows
 
     B, H, Hkv, N, D = 2, 32, 8, 16384, 128
@@ -82,6 +96,7 @@ def test_gqa_with_units_taken_dynamically(cuda_lib):
     ro, rl = oracle_rows(q, k, v, "fp16", True, scale, rows)
     bh = np.array([r[0] for r in rows])
     i = np.array([r[1] for r in rows])
-    compare(o.reshape(B * H, N, D)[bh, i], lse.reshape(B * H, N)[bh, i], ro, rl, "fp16")
+    compare(o.reshape(B * H, N, D)[bh, i], lse.reshape(B * H, N)[bh, i], ro, rl, "fp16",
+            name="gqa_dynamic_b2_h32_hkv8_n16384_d128_fp16_causal", rows=len(rows))
     o2, lse2 = run(q, k, v, True, scale)
     assert np.array_equal(o, o2) and np.array_equal(lse, lse2)

@@ -52,7 +52,8 @@ def test_splitkv_matches_oracle(cuda_lib, B, H, N, D, dtype, causal, splits):
     scale = 1.0 / math.sqrt(D)
     o, lse = run_split(q, k, v, causal, scale, splits)
     ro, rl = oracle_full(q, k, v, dtype, causal, scale)
-    compare(o, lse, ro, rl, dtype, p_rounding_term(q, k, v, dtype, causal, scale))
+    compare(o, lse, ro, rl, dtype, p_rounding_term(q, k, v, dtype, causal, scale),
+            name=f"split{splits}_b{B}_h{H}_n{N}_d{D}_{dtype}_{'causal' if causal else 'noncausal'}")
 
 
 def test_splitkv_agrees_with_unsplit_path(cuda_lib):
@@ -78,8 +79,20 @@ def test_splitkv_long_sequence_few_heads_sampled(cuda_lib):
     ro, rl = oracle_rows(q, k, v, "fp16", True, 1.0 / math.sqrt(D), rows)
     bh = np.array([r[0] for r in rows])
     i = np.array([r[1] for r in rows])
-    compare(o.reshape(B * H, N, D)[bh, i], lse.reshape(B * H, N)[bh, i], ro, rl, "fp16")
+    compare(o.reshape(B * H, N, D)[bh, i], lse.reshape(B * H, N)[bh, i], ro, rl, "fp16",
+            name=f"split{splits}_b{B}_h{H}_n{N}_d{D}_fp16_causal", rows=len(rows))
     assert np.isfinite(o).all() and np.isfinite(lse).all()
+
+
+def test_splitkv_with_units_taken_dynamically_all_rows(cuda_lib):
+    # K and V of 84 MB (more than 64 MiB): head-grouped units from the launch's
+    # counter, with a split on top; every row against the oracle.
+    B, H, N, D, splits = 2, 80, 2048, 128, 3
+    q, k, v = inputs.make_qkv(B, H, N, D, "fp16", seed=4243)
+    scale = 1.0 / math.sqrt(D)
+    o, lse = run_split(q, k, v, True, scale, splits)
+    ro, rl = oracle_full(q, k, v, "fp16", True, scale)
+    compare(o, lse, ro, rl, "fp16", name=f"split{splits}_dynamic_b{B}_h{H}_n{N}_d{D}_fp16_causal")
 
 
 def test_splitkv_with_units_taken_dynamically(cuda_lib):
@@ -96,7 +109,8 @@ def test_splitkv_with_units_taken_dynamically(cuda_lib):
     ro, rl = oracle_rows(q, k, v, "fp16", True, scale, rows)
     bh = np.array([r[0] for r in rows])
     i = np.array([r[1] for r in rows])
-    compare(o.reshape(B * H, N, D)[bh, i], lse.reshape(B * H, N)[bh, i], ro, rl, "fp16")
+    compare(o.reshape(B * H, N, D)[bh, i], lse.reshape(B * H, N)[bh, i], ro, rl, "fp16",
+            name="split3_dynamic_b4_h16_n8192_d128_fp16_causal", rows=len(rows))
     o2, lse2 = run_split(q, k, v, True, scale, 3)
     assert np.array_equal(o, o2) and np.array_equal(lse, lse2)
     from helpers import run_gpu

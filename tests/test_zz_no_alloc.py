@@ -5,8 +5,9 @@ belongs to a host framework's pool, or an allocation call is too costly on their
 path): the partial results go to the library's fixed per-device scratch array
 instead of a caller workspace.  Each check calls it through the C ABI and
 compares with attn_fwd_splitkv, the entry point that takes a caller workspace,
-on two calls in a row with different data, so stale scratch contents from the
-first call would show up in the second.  This file is collected last on purpose.
+and with the FP64 oracle, on two calls in a row with different data, so stale
+scratch contents from the first call would show up in the second.  This file is
+collected last on purpose.
 """
 import ctypes
 import math
@@ -16,6 +17,8 @@ import pytest
 import torch
 
 from exact_causal_attention_gb300 import inputs
+
+from helpers import compare, oracle_full
 
 pytestmark = pytest.mark.gpu
 
@@ -33,7 +36,8 @@ def test_noalloc_split_matches_workspace_split_on_two_calls(cuda_lib):
     B, H, N, D, splits = 1, 4, 2304, 128, 4
     scale = 1.0 / math.sqrt(D)
     for call, seed in enumerate((71, 72)):
-        q, k, v = (x.cuda() for x in inputs.make_qkv(B, H, N, D, "fp16", seed=seed, qk_std=1.5))
+        hq, hk, hv = inputs.make_qkv(B, H, N, D, "fp16", seed=seed, qk_std=1.5)
+        q, k, v = hq.cuda(), hk.cuda(), hv.cuda()
         o = torch.full_like(q, float("nan"))
         lse = torch.full((B, H, N), float("nan"), dtype=torch.float32, device="cuda")
         assert _noalloc(lib, q, k, v, o, lse, True, scale, splits) == 0, f"call {call}"
@@ -46,6 +50,9 @@ def test_noalloc_split_matches_workspace_split_on_two_calls(cuda_lib):
         # the tolerances of the parity tests (O 4e-3 max / 5e-4 mean, lse 1e-4)
         assert np.abs(og - rg).max() <= 4e-3 and np.abs(og - rg).mean() <= 5e-4, f"call {call}"
         assert np.abs(lg - rl).max() <= 1e-4, f"call {call}"
+        # and on its own against the FP64 oracle, at the stated tolerances
+        ro, rlo = oracle_full(hq, hk, hv, "fp16", True, scale)
+        compare(og, lg, ro, rlo, "fp16", name=f"noalloc_split{splits}_b{B}_h{H}_n{N}_d{D}_fp16_causal_call{call}")
 
 
 def test_noalloc_rejects_a_split_larger_than_its_scratch(cuda_lib):
