@@ -34,15 +34,18 @@ __device__ int g_device_status = 0;
 
 // Work counters of the attention kernel, one 256-byte slot per launch, taken in
 // turn: a launch hands its units out from slot[0] and counts finished CTAs in
-// slot[32]; its last CTA sets both back to zero.  64 slots let up to 64 launches
-// run at once (on different streams) without sharing one.
+// slot[32]; its last CTA sets both back to zero.  A slot is handed to a new
+// launch only after the launch that last held it has finished: the new launch
+// waits on the GPU for an event recorded after the old one (see SlotGuard), so
+// more than 64 launches in flight at once queue up instead of sharing counters.
 constexpr int kSchedSlots = 64;
 __device__ int g_sched_pool[kSchedSlots * 64] = {};
 
 // Counters of the paged decode's fused segment merge: one per (request, K/V head,
 // head chunk), zero between launches (each group's last segment resets its
-// counter).  Slots are taken in turn so up to 8 launches can run at once; larger
-// launches use the separate merge kernel.
+// counter).  Slots are taken in turn, guarded like the attention kernel's, so up
+// to 8 launches run at once and a ninth waits for the first; larger launches use
+// the separate merge kernel.
 constexpr int kDecCounterSlots = 8;
 constexpr int kDecCountersPerSlot = 4096;
 __device__ unsigned g_dec_counters[kDecCounterSlots * kDecCountersPerSlot] = {};
@@ -52,6 +55,82 @@ using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t
                                    const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
                                    CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
 
+// Order of reuse of a pool of counter slots: before a launch takes a slot, its
+// stream waits for the event recorded after the slot's previous launch (a no-op
+// once that launch has finished), and the event is recorded again after the new
+// launch.  Under stream capture no event is used: the slot is fixed in the
+// graph when captured.
+template <int kSlots>
+struct SlotGuard {
+  cudaEvent_t done[kSlots] = {};
+  bool recorded[kSlots] = {};
+  unsigned next = 0;
+
+  // Takes the next slot for a launch on `stream`; ATTN_ERR_CUDA if an event call fails.
+  int acquire(cudaStream_t stream, unsigned* slot, bool* capturing) {
+    *slot = next++ % kSlots;
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(stream, &cs) != cudaSuccess) return ATTN_ERR_CUDA;
+    *capturing = cs != cudaStreamCaptureStatusNone;
+    if (*capturing || !recorded[*slot]) return ATTN_OK;
+    return cudaStreamWaitEvent(stream, done[*slot], 0) == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+  }
+
+  // Marks the slot busy until the work enqueued so far on `stream` has finished.
+  int release(cudaStream_t stream, unsigned slot, bool capturing) {
+    if (capturing) return ATTN_OK;
+    if (done[slot] == nullptr && cudaEventCreateWithFlags(&done[slot], cudaEventDisableTiming) != cudaSuccess) {
+      return ATTN_ERR_CUDA;
+    }
+    if (cudaEventRecord(done[slot], stream) != cudaSuccess) return ATTN_ERR_CUDA;
+    recorded[slot] = true;
+    return ATTN_OK;
+  }
+};
+
+// Tensor maps already encoded, keyed by everything the encoding reads (address,
+// element type and the [BH, N, D] extents with the box height), so a hit is
+// exactly the map a new encoding would produce, whatever the caller freed or
+// reallocated in between.  Least recently used entries are replaced.
+struct MapCache {
+  struct Entry {
+    const void* ptr;
+    uint64_t shape;  // D, N, BH, box rows, element type packed
+    int BH;
+    unsigned long long last_use;
+    CUtensorMap map;
+  };
+  static constexpr int kEntries = 32;
+  Entry e[kEntries] = {};
+  unsigned long long clock = 0;
+
+  static uint64_t pack(bool bf16, int D, int N, unsigned box_rows) {
+    return (static_cast<uint64_t>(static_cast<uint32_t>(N)) << 32) | (static_cast<uint64_t>(D) << 16) |
+           (static_cast<uint64_t>(box_rows) << 1) | (bf16 ? 1u : 0u);
+  }
+  // The cached map, or nullptr.
+  const CUtensorMap* find(const void* ptr, uint64_t shape, int BH) {
+    for (Entry& x : e) {
+      if (x.last_use != 0 && x.ptr == ptr && x.shape == shape && x.BH == BH) {
+        x.last_use = ++clock;
+        return &x.map;
+      }
+    }
+    return nullptr;
+  }
+  void insert(const void* ptr, uint64_t shape, int BH, const CUtensorMap& map) {
+    Entry* victim = &e[0];
+    for (Entry& x : e) {
+      if (x.last_use < victim->last_use) victim = &x;
+    }
+    victim->ptr = ptr;
+    victim->shape = shape;
+    victim->BH = BH;
+    victim->map = map;
+    victim->last_use = ++clock;
+  }
+};
+
 struct DeviceState {
   bool probed = false;
   bool sm103 = false;
@@ -59,9 +138,10 @@ struct DeviceState {
   int* status = nullptr;    // address of g_device_status on this device
   void* scratch = nullptr;  // address of g_splitkv_scratch on this device, set by its first use
   int* sched_pool = nullptr;  // address of g_sched_pool on this device
-  unsigned sched_next = 0;    // slot of the next attention launch
+  SlotGuard<kSchedSlots> sched_slots;  // slots of the launches that take units from a counter
   unsigned* dec_counters = nullptr;  // address of g_dec_counters on this device
-  unsigned dec_next = 0;             // slot of the next split decode launch
+  SlotGuard<kDecCounterSlots> dec_slots;  // slots of the split decode launches that merge in the kernel
+  MapCache maps;           // q/k/v/o tensor maps of recent attention launches
   unsigned configured = 0;  // bitmask of kernel instantiations with smem attribute set
   unsigned configured_decode = 0;
 };
@@ -133,6 +213,19 @@ int encode_qkv_map(EncodeTiledFn encode, CUtensorMap* map, const void* ptr, bool
              CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? ATTN_OK : ATTN_ERR_INVALID_ARG;
+}
+
+// encode_qkv_map through the device's cache of recent maps.
+int cached_qkv_map(MapCache& cache, EncodeTiledFn encode, CUtensorMap* map, const void* ptr, bool bf16, int D,
+                   int N, int BH, unsigned box_rows = 128) {
+  const uint64_t shape = MapCache::pack(bf16, D, N, box_rows);
+  if (const CUtensorMap* hit = cache.find(ptr, shape, BH)) {
+    *map = *hit;
+    return ATTN_OK;
+  }
+  const int rc = encode_qkv_map(encode, map, ptr, bf16, D, N, BH, box_rows);
+  if (rc == ATTN_OK) cache.insert(ptr, shape, BH, *map);
+  return rc;
 }
 
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
@@ -279,11 +372,11 @@ int launch(const void* q, const void* k, const void* v, void* o, float* lse, int
     st->configured |= 1u << ((D == 128 ? 2 : 0) + (BF16 ? 1 : 0));
   }
   CUtensorMap tq, tk, tv, to;
-  int rc = encode_qkv_map(encode, &tq, q, BF16, D, N, BH);
-  if (rc == ATTN_OK) rc = encode_qkv_map(encode, &tk, k, BF16, D, N, B * Hkv);
-  if (rc == ATTN_OK) rc = encode_qkv_map(encode, &tv, v, BF16, D, N, B * Hkv);
+  int rc = cached_qkv_map(st->maps, encode, &tq, q, BF16, D, N, BH);
+  if (rc == ATTN_OK) rc = cached_qkv_map(st->maps, encode, &tk, k, BF16, D, N, B * Hkv);
+  if (rc == ATTN_OK) rc = cached_qkv_map(st->maps, encode, &tv, v, BF16, D, N, B * Hkv);
   // Output: stored by each softmax warp in 32-row slabs.
-  if (rc == ATTN_OK) rc = encode_qkv_map(encode, &to, o, BF16, D, N, BH, 32);
+  if (rc == ATTN_OK) rc = cached_qkv_map(st->maps, encode, &to, o, BF16, D, N, BH, 32);
   if (rc != ATTN_OK) return rc;
 
   eca::FwdParams p;
@@ -308,7 +401,14 @@ int launch(const void* q, const void* k, const void* v, void* o, float* lse, int
   p.group_heads = unit_group_heads(BH >> p.head_pair, (H / Hkv) >> p.head_pair, p.n_pairs * ks.splits,
                                    st->sm_count, kv_bytes);
   const bool dynamic = p.group_heads < (BH >> p.head_pair);
-  p.sched = st->sched_pool + 64 * (st->sched_next++ % kSchedSlots);
+  // Only the dynamic instance touches its counters.
+  unsigned slot = 0;
+  bool capturing = false;
+  if (dynamic) {
+    const int rc_slot = st->sched_slots.acquire(stream, &slot, &capturing);
+    if (rc_slot != ATTN_OK) return rc_slot;
+  }
+  p.sched = st->sched_pool + 64 * slot;
   p.causal = causal ? 1 : 0;
   p.scale_log2e = scale * 1.4426950408889634f;
   p.wait_limit_ns = kWaitLimitNs;
@@ -321,6 +421,10 @@ int launch(const void* q, const void* k, const void* v, void* o, float* lse, int
     eca::attn_fwd_kernel<D, BF16, false><<<grid, eca::kThreads, L::kDynamicBytes, stream>>>(tq, tk, tv, to, p);
   }
   if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_LAUNCH;
+  if (dynamic) {
+    const int rc_slot = st->sched_slots.release(stream, slot, capturing);
+    if (rc_slot != ATTN_OK) return rc_slot;
+  }
   if (part_o == nullptr) return ATTN_OK;
 
   eca::CombineParams c;
@@ -550,15 +654,22 @@ int decode_impl(bool bf16, const void* q, const void* cache, const int* block_ta
   p.timeout_code = ATTN_ERR_TIMEOUT;
   p.bad_index_code = ATTN_ERR_BAD_INDEX;
   p.counters = nullptr;
-  const long long groups = static_cast<long long>(B) * Hkv * sh.head_chunks;
-  if (sh.splits > 1 && groups <= kDecCountersPerSlot) {
-    p.counters = st->dec_counters + static_cast<size_t>(st->dec_next++ % kDecCounterSlots) * kDecCountersPerSlot;
-  }
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  if (D == 128) {
-    return bf16 ? launch_decode<128, true>(tm, p, sh, st, s) : launch_decode<128, false>(tm, p, sh, st, s);
+  const long long groups = static_cast<long long>(B) * Hkv * sh.head_chunks;
+  unsigned slot = 0;
+  bool capturing = false;
+  if (sh.splits > 1 && groups <= kDecCountersPerSlot) {
+    rc = st->dec_slots.acquire(s, &slot, &capturing);
+    if (rc != ATTN_OK) return rc;
+    p.counters = st->dec_counters + static_cast<size_t>(slot) * kDecCountersPerSlot;
   }
-  return bf16 ? launch_decode<64, true>(tm, p, sh, st, s) : launch_decode<64, false>(tm, p, sh, st, s);
+  if (D == 128) {
+    rc = bf16 ? launch_decode<128, true>(tm, p, sh, st, s) : launch_decode<128, false>(tm, p, sh, st, s);
+  } else {
+    rc = bf16 ? launch_decode<64, true>(tm, p, sh, st, s) : launch_decode<64, false>(tm, p, sh, st, s);
+  }
+  if (rc != ATTN_OK || p.counters == nullptr) return rc;
+  return st->dec_slots.release(s, slot, capturing);
 }
 
 }  // namespace

@@ -21,15 +21,36 @@
  * cores, running max m, sum l and unnormalised output o kept in fp32 (the page's
  * section 2), probabilities rounded to the input type before the P V product,
  * O rounded to nearest even.  The kernel's m is a reference that may trail the
- * row's max (or start from a fixed guess) as long as no probability can leave
- * the 16-bit range or underflow it; the recurrence gives the same O and lse for
- * any reference, so this changes only rounding.
+ * row's max as long as no probability can leave the 16-bit range, or start from
+ * a fixed guess that is kept only when the first key tile's probabilities sum to
+ * at least 1 (so the running sum l stays >= 1, as with the row max); the
+ * recurrence gives the same O and lse for any reference, so this changes only
+ * rounding.
  *
  * Ownership: every pointer is device memory owned by the caller; the library
  * allocates nothing per call and keeps no reference after the call returns.
  * Asynchrony: the call only enqueues work on `stream` (NULL = legacy default
  * stream) and never synchronises; a fault during execution surfaces at the
- * caller's next synchronisation.  Calls may come from several host threads.
+ * caller's next synchronisation.  Calls may come from several host threads (the
+ * host side serialises them on one lock).
+ *
+ * Concurrency limits: launches whose key/value tensors together exceed 64 MiB
+ * hand out their work from a device counter, taken from a pool of 64 per device
+ * in turn; the split paged decode's in-kernel merge uses counters from a pool of
+ * 8.  A counter is handed to a new launch only once the launch that last held
+ * it has finished: the library makes the new launch's stream wait for an event
+ * recorded after the old one, so more launches than the pool holds in flight at
+ * once run one after another where they would share a counter, and are never
+ * corrupted.  Under stream capture no event is used and a launch keeps the
+ * counter it was captured with; two graphs whose captured launches hold the same
+ * counter (captured 64, or 8, such launches apart) must not run at once.
+ *
+ * Bounded waits: every wait inside a kernel gives up after 2 s without progress
+ * (a bug, or a kernel kept off the GPU that long).  The kernel then stops early
+ * and leaves its outputs incomplete; the call that launched it has already
+ * returned ATTN_OK, and only attn_device_status reports ATTN_ERR_TIMEOUT.  Call
+ * attn_device_status after work whose results matter when a stall must not pass
+ * unnoticed.
  *
  * Errors: arguments are checked before anything touches the GPU; an invalid
  * call returns a negative status and launches nothing (section 9 of the page:
