@@ -34,6 +34,14 @@ WORKLOAD = "causal_b1_h32_n8192_d128_fp16"
 # 25.854 ms at B=1, H=32, N=8192, D=128 causal fp16 -> 2BHN^2D / t.
 PAGE_MS_N8192 = 25.854
 L2_FLUSH_BYTES = 256 << 20  # twice the 129 MB L2
+# NVIDIA's published dense FP16/BF16 tensor rate for this part: the HGX B300 specification
+# gives 36 PFLOPS FP16/BF16 per 8 GPUs with 2:4 sparsity, i.e. 2.25 PFLOP/s dense per GPU.
+DATASHEET_DENSE_FP16_TFLOPS = 2250.0
+DATASHEET_SOURCE = "NVIDIA HGX B300 specification: FP16/BF16 tensor 36 PFLOPS per 8 GPUs with sparsity -> 2.25 dense per GPU"
+# Dense fp16 MMA work one SM retires per clock (a 128x128x16 tcgen05.mma every 64 cycles),
+# consistent with the ncu capture of the attention kernel (tensor pipe 76.4% active at
+# 1.797 GHz while executing 1.74 PFLOP/s over 152 SMs).
+MMA_FLOP_PER_CLK_PER_SM = 8192
 PROFILES = os.path.join(ROOT, "profiles")
 
 
@@ -66,6 +74,17 @@ def executed_flops(w) -> float:
     n = -(-w.N // 128)
     blocks = n * (n + 1) // 2 if w.causal else n * n
     return 4.0 * 128 * 128 * w.D * w.B * w.H * blocks
+
+
+def clock_normalised(achieved_tflops, clocks, sm_count):
+    """The achieved rate against the tensor rate at the SM clock the run actually saw (median of
+    the samples taken during the timed region), so kernel changes can be told from clock luck."""
+    mhz = (clocks or {}).get("sm_mhz")
+    if not mhz or not sm_count:
+        return None
+    peak = MMA_FLOP_PER_CLK_PER_SM * sm_count * mhz * 1e6 / 1e12
+    return {"sm_mhz_median": mhz, "sm_count": sm_count, "tflops_per_ghz": achieved_tflops / (mhz / 1000.0),
+            "clock_rate_tensor_peak_tflops": peak, "frac_of_clock_rate_peak": achieved_tflops / peak}
 
 
 def host_cores():
@@ -598,6 +617,7 @@ def bench_ours(args, w):
         dist.destroy_process_group()
     if rank != 0:
         return
+    sm_count = torch.cuda.get_device_properties(dev).multi_processor_count
     peaks, kind = measured_peaks()
     peak = float(peaks["bf16_tflops"])  # fp16 and bf16 share one nominal dense rate (ratio 1.0)
     achieved = flops / (kernel_ms * 1e-3) / 1e12
@@ -628,7 +648,9 @@ def bench_ours(args, w):
         "paged_decode": paged,
         "fp16_matmul_peak_tflops": fp16_peak,
         "frac_of_measured_fp16_matmul": (achieved / fp16_peak) if fp16_peak else None,
-        "frac_of_datasheet_dense_fp16": achieved / 2250.0,
+        "frac_of_datasheet_dense_fp16": achieved / DATASHEET_DENSE_FP16_TFLOPS,
+        "datasheet_source": DATASHEET_SOURCE,
+        "clock_normalised": clock_normalised(achieved, clocks, sm_count),
         "vs_baseline_ref": "page's PyTorch SDPA FLASH on RTX 3060 Laptop (SM86): 25.854 ms",
     }
     print(json.dumps(line), flush=True)

@@ -78,3 +78,15 @@ def test_executed_flops_exceed_the_algorithmic_count_by_the_diagonal_blocks():
     assert bench.executed_flops(w) == pytest.approx(w.flops * 65 / 64)  # (n + 1) / n with n = 64 tiles
     nc = w.with_causal(False)
     assert bench.executed_flops(nc) == pytest.approx(nc.flops)  # no diagonal: every block is full work
+
+
+def test_clock_normalised_rate():
+    import bench
+
+    # 152 SMs at 2070 MHz retire 8192 * 152 * 2.07e9 FLOP/s = 2577.4 TFLOP/s of dense fp16 MMA work.
+    r = bench.clock_normalised(1700.0, {"sm_mhz": 2070.0}, 152)
+    assert r["clock_rate_tensor_peak_tflops"] == pytest.approx(2577.4, rel=1e-4)
+    assert r["frac_of_clock_rate_peak"] == pytest.approx(1700.0 / 2577.4, rel=1e-4)
+    assert r["tflops_per_ghz"] == pytest.approx(1700.0 / 2.07)
+    assert bench.clock_normalised(1700.0, {"sm_mhz": None}, 152) is None
+    assert bench.clock_normalised(1700.0, None, 152) is None
