@@ -261,15 +261,17 @@ def bench_reference(args, w):
 
 
 def bench_split(eca, inputs, dev, stream, flush):
-    """The key split on causal B=1 H=4 N=8192 D=128 fp16 (too few heads to fill the GPU), with the
-    default segment count, against the unsplit kernel; L2 flushed before every call."""
+    """The key split on causal B=1 H=4 N=8192 D=128 fp16 (too few heads to fill the GPU with
+    pair units), with the default segment count (at least 2), against the unsplit kernel (which
+    runs key-halves units here); L2 flushed before every call."""
     import torch
 
     sw = inputs.Workload("causal_b1_h4_n8192_d128_fp16", 1, 4, 8192, 128, "fp16", True, 5)
     sq, sk, sv = (x.to(dev) for x in inputs.workload_qkv(sw))
     so = torch.empty_like(sq)
     sl = torch.empty((sw.B, sw.H, sw.N), dtype=torch.float32, device=dev)
-    splits = eca.splitkv_default_splits(sw.B, sw.H, sw.N, sw.D)
+    default_splits = eca.splitkv_default_splits(sw.B, sw.H, sw.N, sw.D)
+    splits = max(2, default_splits)  # the split path itself, even when the default is not to split
     need = eca.splitkv_workspace_bytes(sw.B, sw.H, sw.N, sw.D, splits)
     ws = torch.empty(need + 256, dtype=torch.uint8, device=dev)
     off = (-ws.data_ptr()) % 256
@@ -291,7 +293,7 @@ def bench_split(eca, inputs, dev, stream, flush):
     t_plain = timed(lambda: eca.attn_fwd_into(sq, sk, sv, so, sl, causal=True, scale=sw.scale, stream=stream))
     t_split = timed(lambda: eca.attn_fwd_splitkv(sq, sk, sv, so, sl, kv_splits=splits, workspace=ws,
                                                  causal=True, scale=sw.scale, stream=stream))
-    return {"workload": sw.name, "kv_splits": splits, "workspace_bytes": need,
+    return {"workload": sw.name, "default_kv_splits": default_splits, "kv_splits": splits, "workspace_bytes": need,
             "unsplit_ms": round(t_plain, 4), "unsplit_tflops": round(sw.flops / (t_plain * 1e-3) / 1e12, 1),
             "split_ms": round(t_split, 4), "split_tflops": round(sw.flops / (t_split * 1e-3) / 1e12, 1),
             "launches_per_call": 2}

@@ -291,8 +291,9 @@ int unit_group_heads(int BH, int q_per_kv, int units_per_slice, int sm_count, un
 
 // Split count with the shortest predicted time, from a replay of the kernel's
 // schedule: units are taken in launch order by whichever CTA is free first, a
-// unit costs the longer of its two tiles' key-tile counts plus a fixed
-// start/end cost, and a split adds the merge kernel's traffic.  The constants
+// unit costs the longer of its two tiles' key-tile counts (of its two halves with
+// key-halves units) plus a fixed start/end cost, and a split adds the merge
+// kernel's traffic.  The constants
 // are rough (a key tile of both query tiles is about 1.2 us on a busy SM, a
 // unit boundary about three of those, the merge about 4 TB/s); only their
 // ratios matter.  Without a shortage of units the answer is 1.
@@ -314,6 +315,20 @@ int predicted_best_splits(int B, int H, int N, int D, int sm_count) {
     std::priority_queue<double, std::vector<double>, std::greater<double>> free_at;
     for (int c = 0; c < sm_count; ++c) free_at.push(0.0);
     double makespan = 0.0;
+    if (ks.splits == 1 && static_cast<long long>(n_pairs) * bh < sm_count) {
+      // Unsplit with fewer pair units than SMs: the kernel runs key-halves units,
+      // one query tile each, its key tiles shared out between the CTA's two slots.
+      for (int tile = n_tiles - 1; tile >= 0; --tile) {
+        for (long long x = 0; x < bh; ++x) {
+          const double t = free_at.top() + (tile + 2) / 2 + kUnitSteps;
+          free_at.pop();
+          free_at.push(t);
+          if (t > makespan) makespan = t;
+        }
+      }
+      best_t = makespan * kStepUs;
+      continue;
+    }
     for (int pair = n_pairs - 1; pair >= 0; --pair) {
       for (long long x = 0; x < bh; ++x) {
         for (int seg = 0; seg < ks.splits; ++seg) {
@@ -362,11 +377,13 @@ int launch(const void* q, const void* k, const void* v, void* o, float* lse, int
   const int BH = B * H;
   using L = eca::FwdSmem<D>;
   if (!(st->configured & (1u << ((D == 128 ? 2 : 0) + (BF16 ? 1 : 0))))) {
-    // Both assignment modes of this instantiation.
-    if (cudaFuncSetAttribute(eca::attn_fwd_kernel<D, BF16, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             L::kDynamicBytes) != cudaSuccess ||
-        cudaFuncSetAttribute(eca::attn_fwd_kernel<D, BF16, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             L::kDynamicBytes) != cudaSuccess) {
+    // The three unit modes of this instantiation.
+    if (cudaFuncSetAttribute(eca::attn_fwd_kernel<D, BF16, eca::kModePairs>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, L::kDynamicBytes) != cudaSuccess ||
+        cudaFuncSetAttribute(eca::attn_fwd_kernel<D, BF16, eca::kModeDynamic>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, L::kDynamicBytes) != cudaSuccess ||
+        cudaFuncSetAttribute(eca::attn_fwd_kernel<D, BF16, eca::kModeHalves>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, L::kDynamicBytes) != cudaSuccess) {
       return ATTN_ERR_CUDA;
     }
     st->configured |= 1u << ((D == 128 ? 2 : 0) + (BF16 ? 1 : 0));
@@ -401,6 +418,17 @@ int launch(const void* q, const void* k, const void* v, void* o, float* lse, int
   p.group_heads = unit_group_heads(BH >> p.head_pair, (H / Hkv) >> p.head_pair, p.n_pairs * ks.splits,
                                    st->sm_count, kv_bytes);
   const bool dynamic = p.group_heads < (BH >> p.head_pair);
+  // Fewer units than SMs (short sequences): a unit becomes one query tile whose key
+  // tiles the CTA's two slots share out in halves, which doubles the units and
+  // halves the longest chain of key steps.
+  bool halves = false;
+  if (part_o == nullptr && !dynamic && p.n_units < st->sm_count) {
+    halves = true;
+    p.head_pair = 0;
+    p.n_pairs = p.n_tiles;
+    p.n_units = p.n_tiles * BH;
+    p.group_heads = BH;
+  }
   // Only the dynamic instance touches its counters.
   unsigned slot = 0;
   bool capturing = false;
@@ -416,9 +444,14 @@ int launch(const void* q, const void* k, const void* v, void* o, float* lse, int
   // Persistent: one CTA per SM (the shared-memory footprint admits only one), never more than the units.
   const unsigned grid = static_cast<unsigned>(p.n_units < st->sm_count ? p.n_units : st->sm_count);
   if (dynamic) {
-    eca::attn_fwd_kernel<D, BF16, true><<<grid, eca::kThreads, L::kDynamicBytes, stream>>>(tq, tk, tv, to, p);
+    eca::attn_fwd_kernel<D, BF16, eca::kModeDynamic><<<grid, eca::kThreads, L::kDynamicBytes, stream>>>(tq, tk, tv,
+                                                                                                      to, p);
+  } else if (halves) {
+    eca::attn_fwd_kernel<D, BF16, eca::kModeHalves><<<grid, eca::kThreads, L::kDynamicBytes, stream>>>(tq, tk, tv,
+                                                                                                     to, p);
   } else {
-    eca::attn_fwd_kernel<D, BF16, false><<<grid, eca::kThreads, L::kDynamicBytes, stream>>>(tq, tk, tv, to, p);
+    eca::attn_fwd_kernel<D, BF16, eca::kModePairs><<<grid, eca::kThreads, L::kDynamicBytes, stream>>>(tq, tk, tv,
+                                                                                                    to, p);
   }
   if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_LAUNCH;
   if (dynamic) {

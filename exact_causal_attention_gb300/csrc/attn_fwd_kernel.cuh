@@ -28,7 +28,13 @@
 //     unsplit launches with an even group pair two heads of a group at one query
 //     tile instead of two consecutive tiles, so each K/V tile serves both query
 //     heads in the CTA and both need the same key tiles; the heads of a group
-//     are adjacent in the unit order so their K/V tiles come from L2.
+//     are adjacent in the unit order so their K/V tiles come from L2.  When a
+//     launch has fewer such units than SMs (short sequences), a unit is one query
+//     tile whose key tiles are split in two halves, one per tile slot of the CTA
+//     (key halves): the two slots run the same recurrence on their halves side by
+//     side, each on ring items of its own, and the epilogue merges their (m, l, O)
+//     with the online-softmax law (section 4's merge, the decode page's section
+//     6.4), so the unit's chain of key steps is half as long.
 //     384 threads:
 //       warps 0-3  softmax for query tile 0     warps 4-7  softmax for query tile 1
 //       warp 8     takes units; TMA producer of the ring items {V_j, K_j+1}
@@ -83,6 +89,11 @@ constexpr float kGuessRef = 4.0f;       // first reference of a unit (scores tim
 constexpr float kMinGuessSum = 1.0f;    // a guess is kept only if the first tile's sum of p reaches this
 constexpr int kUnitQueue = 4;           // depth of the shared-memory queue of unit indices
 constexpr int kUnitReaders = 11;        // warps that read each queue entry: 8 softmax, 2 issuers, Q loader
+
+// How a launch forms and assigns its work units (the kernel's third template argument).
+constexpr int kModePairs = 0;    // two query tiles (or head pairs) per unit, fixed zig-zag assignment
+constexpr int kModeDynamic = 1;  // the same units, taken from the launch's counter in head groups
+constexpr int kModeHalves = 2;   // one query tile per unit, its key tiles in two halves; fixed assignment
 
 struct FwdParams {
   void* o;        // [BH, N, D] 16-bit (unused when part_o is set)
@@ -142,9 +153,12 @@ struct FwdSmem {
   static constexpr int kBarTurn = kBarDrain + 2;    // + t: issuer t may put its next turn into the pipe
   static constexpr int kBarUnitFull = kBarTurn + 2;          // + slot: queue entry written
   static constexpr int kBarUnitFree = kBarUnitFull + kUnitQueue;  // + slot: queue entry read by every reader
-  static constexpr int kNumBars = kBarUnitFree + kUnitQueue;
+  static constexpr int kBarMerge = kBarUnitFree + kUnitQueue;     // key halves: slot 1's m and l published
+  static constexpr int kNumBars = kBarMerge + 1;
   static constexpr int kMiscOff = kBarOff + kNumBars * 8;  // TMEM base, abort flag, unit queue
-  static constexpr int kBytes = kMiscOff + 8 + 4 * kUnitQueue;
+  // Key halves: slot 1's final m and l per row, read by slot 0's epilogue.
+  static constexpr int kMergeOff = (kMiscOff + 8 + 4 * kUnitQueue + 15) & ~15;
+  static constexpr int kBytes = kMergeOff + 2 * kBlockM * 4;
   static constexpr int kDynamicBytes = kBytes + 1024;  // slack for 1024-B alignment
   static_assert(kDynamicBytes <= 227 * 1024, "shared memory exceeds the per-block limit");
 };
@@ -152,14 +166,17 @@ struct FwdSmem {
 // One work unit, against the key tiles kv0 .. kv0 + n_kv - 1 of key segment seg:
 // query tiles 2*pair and 2*pair + 1 of slice bh; or, with head_pair set, query
 // tile `pair` (tile0 = pair) of the two heads bh and bh + 1, which read the same
-// key/value head.
+// key/value head; or, with key halves, query tile `pair` of slice bh in both
+// slots, slot 0 against key tiles kv0 .. kv0 + n_kv0 - 1 and slot 1 against
+// kv1 .. kv1 + n_kv1 - 1.
 struct Unit {
   int bh;
   int kvh;  // key/value slice: query head h of batch b reads head h / (H / Hkv) of batch b
   int tile0;
   int seg;
-  int kv0;           // first key tile of the segment
-  int n_kv0, n_kv1;  // key tiles each query tile takes from the segment (0 = nothing to do)
+  int kv0;           // first key tile of the segment (of slot 0's half with key halves)
+  int kv1;           // first key tile of slot 1 (kv0 unless key halves)
+  int n_kv0, n_kv1;  // key tiles each slot takes (0 = nothing to do)
   int n_max;
 };
 
@@ -169,6 +186,7 @@ struct Unit {
 // query-tile pair first (causal work grows with the tile index, so the light
 // units come last in every group and the launch ends evenly), then slice, then
 // key segment.
+template <bool kHalves>
 __device__ __forceinline__ void unit_from(int l, const FwdParams& p, Unit& u) {
   const int per_slice = p.n_pairs * p.splits;
   const int slices = p.BH >> p.head_pair;
@@ -185,9 +203,18 @@ __device__ __forceinline__ void unit_from(int l, const FwdParams& p, Unit& u) {
   const int r = local / p.splits;
   u.bh = (grp * p.group_heads + r % g) << p.head_pair;
   u.kvh = (u.bh / p.H) * p.Hkv + (u.bh % p.H) / (p.H / p.Hkv);
-  const int pair = p.n_pairs - 1 - r / g;  // with head pairs, the query tile
-  u.tile0 = p.head_pair ? pair : 2 * pair;
+  const int pair = p.n_pairs - 1 - r / g;  // with head pairs or key halves, the query tile
+  u.tile0 = (p.head_pair || kHalves) ? pair : 2 * pair;
   u.kv0 = u.seg * p.seg_tiles;
+  if (kHalves) {  // never with a key split or head pairs: kv0 = 0
+    const int need = p.causal ? u.tile0 + 1 : p.n_tiles;
+    u.n_kv0 = (need + 1) / 2;
+    u.n_kv1 = need - u.n_kv0;
+    u.kv1 = u.n_kv0;
+    u.n_max = u.n_kv0;
+    return;
+  }
+  u.kv1 = u.kv0;
   const int kv_end = u.kv0 + p.seg_tiles < p.n_tiles ? u.kv0 + p.seg_tiles : p.n_tiles;
   const bool has1 = p.head_pair || u.tile0 + 1 < p.n_tiles;
   // key tiles each query tile needs in total, then the part inside this segment
@@ -228,14 +255,17 @@ __device__ __forceinline__ void issue_pv(uint32_t o_tmem, uint32_t p_tmem, uint6
 
 __device__ __forceinline__ uint32_t parity(int count) { return static_cast<uint32_t>(count) & 1u; }
 
-// kDynamic: units taken from the launch's counter and queued to the CTA's warps
-// (grouped head order); otherwise each warp follows the fixed zig-zag waves.
-template <int D, bool BF16, bool kDynamic>
+// kMode: kModeDynamic takes units from the launch's counter and queues them to
+// the CTA's warps (grouped head order); otherwise each warp follows the fixed
+// zig-zag waves, of pair units or (kModeHalves) of key-halves units.
+template <int D, bool BF16, int kMode>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
                     const FwdParams p) {
   using L = FwdSmem<D>;
+  constexpr bool kDynamic = kMode == kModeDynamic;
+  constexpr bool kHalves = kMode == kModeHalves;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_base = smem_u32(smem_raw);
   const uint32_t sbase = (raw_base + 1023u) & ~1023u;
@@ -258,7 +288,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int s = 0; s < L::kStages; ++s) {
       mbar_init(bar(L::kBarFull + s), 1);
       mbar_init(bar(L::kBarFullK + s), 1);
-      mbar_init(bar(L::kBarEmpty + s), 2);
+      mbar_init(bar(L::kBarEmpty + s), kHalves ? 1 : 2);  // the issuers that consume the item
     }
     for (int t = 0; t < 2; ++t) {
       mbar_init(bar(L::kBarS + t), 1);
@@ -273,6 +303,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(bar(L::kBarUnitFull + q), 1);
       mbar_init(bar(L::kBarUnitFree + q), kUnitReaders);
     }
+    mbar_init(bar(L::kBarMerge), 4);
     mbar_arrive(bar(L::kBarTurn + 0));  // issuer 0 takes the first turn
     *abort_flag = 0;
     fence_barrier_init();
@@ -319,14 +350,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       while (true) {
         const int l = fixed_unit(units_fixed++);
         if (l < 0) return 0;
-        unit_from(l, p, w);
+        unit_from<kHalves>(l, p, w);
         if (w.n_max > 0) return 1;
       }
     }
     int l;
     if (!read_unit(l, whole_warp)) return -1;
     if (l < 0) return 0;
-    unit_from(l, p, w);
+    unit_from<kHalves>(l, p, w);
     return 1;
   };
 
@@ -355,7 +386,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int l = atomicAdd(p.sched, 1);
           if (l >= p.n_units) return -1;
           Unit u;
-          unit_from(l, p, u);
+          unit_from<kHalves>(l, p, u);
           if (u.n_max > 0) return l;
         }
       };
@@ -365,37 +396,44 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (kDynamic) {
           const int l = take_unit();
           if (!push_unit(l) || l < 0) break;
-          unit_from(l, p, w);
+          unit_from<kHalves>(l, p, w);
         } else if (next_unit(w, false) != 1) {
           break;
         }
-        // Items i = 0 .. n_max: {V_(i-1) if i > 0, K_i if i < n_max}.
-        for (int i = 0; i <= w.n_max; ++i) {
-          const int slot = it % L::kStages;
-          if (!wd.wait(bar(L::kBarEmpty + slot), parity(it / L::kStages) ^ 1u)) {
-            ok = false;
-            break;
+        // Items i = 0 .. n_max: {V_(b+i-1) if 0 < i <= n, K_(b+i) if i < n}, with
+        // b = kv0 and n = n_max shared by both slots; with key halves, one item of
+        // each slot per i (slot 0 first), with that slot's b and n.
+        const int per_i = kHalves ? 2 : 1;
+        for (int i = 0; ok && i <= w.n_max; ++i) {
+          for (int h = 0; h < per_i; ++h) {
+            const int b = h ? w.kv1 : w.kv0;
+            const int n = kHalves ? (h ? w.n_kv1 : w.n_kv0) : w.n_max;
+            const int slot = it % L::kStages;
+            if (!wd.wait(bar(L::kBarEmpty + slot), parity(it / L::kStages) ^ 1u)) {
+              ok = false;
+              break;
+            }
+            const uint32_t stage = sbase + L::kRingOff + slot * L::kStageBytes;
+            // The V and K parts complete on barriers of their own, so the P V MMAs can
+            // start before K has landed; a missing part is a plain arrival.
+            const uint32_t full_v = bar(L::kBarFull + slot), full_k = bar(L::kBarFullK + slot);
+            if (i > 0 && i <= n) {
+              mbar_arrive_expect_tx(full_v, L::kTileBytes);
+              for (int s = 0; s < L::kSub; ++s)
+                tma_load_3d(stage + s * kSubTileBytes, &tm_v, full_v, 64 * s, (b + i - 1) * kBlockN, w.kvh, pol_kv);
+            } else {
+              mbar_arrive(full_v);
+            }
+            if (i < n) {
+              mbar_arrive_expect_tx(full_k, L::kTileBytes);
+              for (int s = 0; s < L::kSub; ++s)
+                tma_load_3d(stage + L::kTileBytes + s * kSubTileBytes, &tm_k, full_k, 64 * s, (b + i) * kBlockN,
+                            w.kvh, pol_kv);
+            } else {
+              mbar_arrive(full_k);
+            }
+            ++it;
           }
-          const uint32_t stage = sbase + L::kRingOff + slot * L::kStageBytes;
-          // The V and K parts complete on barriers of their own, so the P V MMAs can
-          // start before K has landed; a missing part is a plain arrival.
-          const uint32_t full_v = bar(L::kBarFull + slot), full_k = bar(L::kBarFullK + slot);
-          if (i > 0) {
-            mbar_arrive_expect_tx(full_v, L::kTileBytes);
-            for (int s = 0; s < L::kSub; ++s)
-              tma_load_3d(stage + s * kSubTileBytes, &tm_v, full_v, 64 * s, (w.kv0 + i - 1) * kBlockN, w.kvh, pol_kv);
-          } else {
-            mbar_arrive(full_v);
-          }
-          if (i < w.n_max) {
-            mbar_arrive_expect_tx(full_k, L::kTileBytes);
-            for (int s = 0; s < L::kSub; ++s)
-              tma_load_3d(stage + L::kTileBytes + s * kSubTileBytes, &tm_k, full_k, 64 * s, (w.kv0 + i) * kBlockN,
-                          w.kvh, pol_kv);
-          } else {
-            mbar_arrive(full_k);
-          }
-          ++it;
         }
       }
       // Let every copy this thread started land before the block can exit.
@@ -425,7 +463,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           mbar_arrive_expect_tx(bar(L::kBarQFull + t), L::kTileBytes);
           for (int s = 0; s < L::kSub; ++s) {
             tma_load_3d(sbase + L::kQOff + t * L::kTileBytes + s * kSubTileBytes, &tm_q, bar(L::kBarQFull + t),
-                        64 * s, (w.tile0 + (p.head_pair ? 0 : t)) * kBlockM, w.bh + (p.head_pair ? t : 0), pol_q);
+                        64 * s, (w.tile0 + ((p.head_pair || kHalves) ? 0 : t)) * kBlockM,
+                        w.bh + (p.head_pair ? t : 0), pol_q);
           }
           ++loads[t];
         }
@@ -462,7 +501,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
         if (lane == 0) mbar_arrive(bar(L::kBarTurn + (1 - t)));
       };
-      int it = 0;       // ring items consumed
+      int it = 0;       // ring items of the units done so far (both slots')
       int p_waits = 0;  // P_t handshakes consumed
       int used = 0;     // earlier units in which tile t existed (its O_t is read by an epilogue)
       int q_loads = 0;  // Q loads of tile t consumed
@@ -475,11 +514,17 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
         }
         const int n_kv = t ? w.n_kv1 : w.n_kv0;
-        // Item 0 (K_0).  Every item is waited for and released by both issuers,
-        // whether or not this tile uses it, so the ring's two-arrival phases stay aligned.
+        // Ring item of this issuer's step i: every item of the unit (both slots use
+        // it), or with key halves every other one, starting with its own slot.
+        const int base = it;
+        auto item = [&](int i) { return kHalves ? base + 2 * i + t : base + i; };
+        int x = item(0);
+        // Item 0 (K_0).  Every item this issuer consumes is waited for and released
+        // whether or not its tile uses it, so the ring's phases stay aligned (two
+        // arrivals per item, or one with key halves).
         if ((n_kv > 0 && !warp_wait(bar(L::kBarQFull + t), parity(q_loads++))) ||
-            !warp_wait(bar(L::kBarFull + it % L::kStages), parity(it / L::kStages)) ||
-            !warp_wait(bar(L::kBarFullK + it % L::kStages), parity(it / L::kStages))) {
+            !warp_wait(bar(L::kBarFull + x % L::kStages), parity(x / L::kStages)) ||
+            !warp_wait(bar(L::kBarFullK + x % L::kStages), parity(x / L::kStages))) {
           ok = false;
           break;
         }
@@ -488,14 +533,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           ok = false;
           break;
         }
-        if (n_kv > 0) issue_qk<D, BF16>(s_tmem, q_desc, ring_k_desc + stage_off(it));
+        if (n_kv > 0) issue_qk<D, BF16>(s_tmem, q_desc, ring_k_desc + stage_off(x));
         pass_turn();
         if (n_kv > 0) tc_commit_warp(bar(L::kBarS + t));
         if (n_kv == 1) tc_commit_warp(bar(L::kBarQFree + t));  // this tile's Q K^T are all issued
-        tc_commit_warp(bar(L::kBarEmpty + it % L::kStages));
-        ++it;
-        for (int j = 0; j < w.n_max; ++j, ++it) {
-          if (!warp_wait(bar(L::kBarFull + it % L::kStages), parity(it / L::kStages))) {
+        tc_commit_warp(bar(L::kBarEmpty + x % L::kStages));
+        for (int j = 0; j < w.n_max; ++j) {
+          x = item(j + 1);
+          if (!warp_wait(bar(L::kBarFull + x % L::kStages), parity(x / L::kStages))) {
             ok = false;
             break;
           }
@@ -518,21 +563,21 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           if (j < n_kv) {
             // P V of keys 0-63 goes in while the softmax still works on keys 64-127.
-            issue_pv<D, BF16>(o_tmem, s_tmem, ring_v_desc + stage_off(it), j > 0, 0, 4);
+            issue_pv<D, BF16>(o_tmem, s_tmem, ring_v_desc + stage_off(x), j > 0, 0, 4);
             if (!warp_wait(bar(L::kBarPb + t), parity(p_waits - 1))) {
               ok = false;
               break;
             }
             tc_fence_after_sync();
-            issue_pv<D, BF16>(o_tmem, s_tmem, ring_v_desc + stage_off(it), true, 4, 8);
+            issue_pv<D, BF16>(o_tmem, s_tmem, ring_v_desc + stage_off(x), true, 4, 8);
           }
-          if (!warp_wait(bar(L::kBarFullK + it % L::kStages), parity(it / L::kStages))) {
+          if (!warp_wait(bar(L::kBarFullK + x % L::kStages), parity(x / L::kStages))) {
             ok = false;
             break;
           }
           if (j + 1 < n_kv) {
             tc_fence_after_sync();
-            issue_qk<D, BF16>(s_tmem, q_desc, ring_k_desc + stage_off(it));
+            issue_qk<D, BF16>(s_tmem, q_desc, ring_k_desc + stage_off(x));
           }
           pass_turn();
           if (j < n_kv) {
@@ -543,8 +588,9 @@ __global__ void __launch_bounds__(kThreads, 1)
               tc_commit_warp(bar(L::kBarO + t));
             }
           }
-          tc_commit_warp(bar(L::kBarEmpty + it % L::kStages));
+          tc_commit_warp(bar(L::kBarEmpty + x % L::kStages));
         }
+        it = base + (kHalves ? 2 : 1) * (w.n_max + 1);
         used += n_kv > 0 ? 1 : 0;
       }
       // Every MMA issued above must finish before TMEM is released.
@@ -566,7 +612,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       const bool got = wd.wait(b, ph);
       return __all_sync(0xffffffffu, got) != 0;
     };
+    float* merge_ml = reinterpret_cast<float*>(smem + L::kMergeOff);  // key halves: slot 1's m, then l
     int s_waits = 0, o_waits = 0;
+    int merges = 0;  // slot 0 with key halves: units whose slot 1 had work
     bool ok = true;
     Unit w;
     while (ok) {
@@ -577,14 +625,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       const int n_kv = t ? w.n_kv1 : w.n_kv0;
       if (n_kv == 0) continue;
-      const int tile = w.tile0 + (p.head_pair ? 0 : t);
+      const int kvb = t ? w.kv1 : w.kv0;  // this slot's first key tile
+      const int tile = w.tile0 + ((p.head_pair || kHalves) ? 0 : t);
       const int head = w.bh + (p.head_pair ? t : 0);
       const int row = tile * kBlockM + r_local;
       // Reference max, base-2 domain (already multiplied by c).  Under the fixed
-      // assignment a unit starts from a guess: on the first key tile the guess must
-      // also not sit far above the row (its p would underflow), and a rejected guess
-      // is replaced, not kept.  (The dynamic instance starts from the first tile's
-      // max: the guess's extra live values push it past its registers.)
+      // assignment a unit starts from a guess, kept on the first key tile only if
+      // that tile's sum of p reaches 1 (a rejected guess is replaced, not kept).
+      // (The dynamic instance starts from the first tile's max: the guess's extra
+      // live values push it past its registers.)
       constexpr bool kGuessFirst = !kDynamic;
       float m_ref = kGuessFirst ? kGuessRef : -INFINITY;
       float l = 0.f;
@@ -603,14 +652,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int q = 0; q < 4; ++q) tmem_ld_x32(t_s + 32u * q, s[q]);
 #pragma unroll
           for (int q = 0; q < 4; ++q) tmem_wait_ld_x32(s[q]);
-          if (p.causal && w.kv0 + j == tile) {
+          if (p.causal && kvb + j == tile) {
 #pragma unroll
             for (int q = 0; q < 4; ++q)
 #pragma unroll
               for (int i = 0; i < 32; ++i)
                 if (32 * q + i > r_local) s[q][i] = __float_as_uint(-INFINITY);
-          } else if (ragged_keys && w.kv0 + j == p.n_tiles - 1) {
-            const int valid = p.N - (w.kv0 + j) * kBlockN;
+          } else if (ragged_keys && kvb + j == p.n_tiles - 1) {
+            const int valid = p.N - (kvb + j) * kBlockN;
 #pragma unroll
             for (int q = 0; q < 4; ++q)
 #pragma unroll
@@ -654,7 +703,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         float row_sum = 0.f;
         bool move = true;  // without a guess, the first key tile takes the row max
         if (kGuessFirst || j > 0) {
-          const bool masked = (p.causal && w.kv0 + j == tile) || (ragged_keys && w.kv0 + j == p.n_tiles - 1);
+          const bool masked = (p.causal && kvb + j == tile) || (ragged_keys && kvb + j == p.n_tiles - 1);
           if (masked && j == 0) {
             // A masked first tile (the diagonal, or the only, ragged, key tile) holds a
             // row's first keys: take their max, as a guessed reference would round a
@@ -771,11 +820,40 @@ __global__ void __launch_bounds__(kThreads, 1)
       ++o_waits;
       tc_fence_after_sync();
 
+      if (kHalves && t == 1) {
+        // Key halves: slot 1 hands its m and l to slot 0, whose epilogue merges O_1
+        // in and then releases it for the next unit.
+        merge_ml[r_local] = m_ref;
+        merge_ml[kBlockM + r_local] = l;
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(L::kBarMerge));
+        continue;
+      }
+      // Key halves: merge slot 1's state with the online-softmax law, M = max(m0, m1),
+      // L = l0 2^(m0 - M) + l1 2^(m1 - M), O = (O_0 2^(m0 - M) + O_1 2^(m1 - M)) / L.
+      const bool merge = kHalves && w.n_kv1 > 0;
+      float m_fin = m_ref, l_fin = l, w0 = 1.f, w1 = 0.f;
+      if (merge) {
+        if (!warp_wait(bar(L::kBarMerge), parity(merges)) || !warp_wait(bar(L::kBarO + 1), parity(merges))) {
+          ok = false;
+          break;
+        }
+        ++merges;
+        tc_fence_after_sync();
+        const float m1 = merge_ml[r_local], l1 = merge_ml[kBlockM + r_local];
+        m_fin = fmaxf(m_ref, m1);
+        w0 = m_ref == -INFINITY ? 0.f : ex2(m_ref - m_fin);
+        w1 = m1 == -INFINITY ? 0.f : ex2(m1 - m_fin);
+        l_fin = w0 * l + w1 * l1;
+      }
+      const uint32_t t_o1 = tmem + lane_base + 256u + static_cast<uint32_t>(D);  // O_1, merged in with key halves
+
       // Epilogue: O = o / l rounded to the output type, lse = (m + log2 l) ln 2;
       // with a key split, the segment's O in fp32 and its lse go to the workspace.
-      const float inv_l = 1.f / l;
-      const float2 il2 = make_float2(inv_l, inv_l);
-      const float row_lse = (m_ref + log2f(l)) * 0.69314718055994530942f;
+      const float inv_l = 1.f / l_fin;
+      const float2 il2 = make_float2(w0 * inv_l, w0 * inv_l);
+      const float2 il2b = make_float2(w1 * inv_l, w1 * inv_l);
+      const float row_lse = (m_fin + log2f(l_fin)) * 0.69314718055994530942f;
       if (p.part_o != nullptr) {
         const size_t prow = (static_cast<size_t>(w.seg) * p.BH + head) * p.N + static_cast<size_t>(row);
         float* dst = p.part_o + prow * D;
@@ -812,17 +890,34 @@ __global__ void __launch_bounds__(kThreads, 1)
           uint32_t o[32];
           tmem_ld_x32(t_o + 64 * c64 + 32 * half, o);
           tmem_wait_ld_x32(o);
+          if (merge) {
+            uint32_t o1[32];
+            tmem_ld_x32(t_o1 + 64 * c64 + 32 * half, o1);
+            tmem_wait_ld_x32(o1);
 #pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            const float2 v = __fmul2_rn(make_float2(__uint_as_float(o[2 * i]), __uint_as_float(o[2 * i + 1])), il2);
-            h[16 * half + i] = pack2<BF16>(v.x, v.y);
+            for (int i = 0; i < 16; ++i) {
+              const float2 a = __fmul2_rn(make_float2(__uint_as_float(o[2 * i]), __uint_as_float(o[2 * i + 1])), il2);
+              const float2 v =
+                  __ffma2_rn(make_float2(__uint_as_float(o1[2 * i]), __uint_as_float(o1[2 * i + 1])), il2b, a);
+              h[16 * half + i] = pack2<BF16>(v.x, v.y);
+            }
+          } else {
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              const float2 v = __fmul2_rn(make_float2(__uint_as_float(o[2 * i]), __uint_as_float(o[2 * i + 1])), il2);
+              h[16 * half + i] = pack2<BF16>(v.x, v.y);
+            }
           }
         }
         if (c64 == D / 64 - 1) {
-          // O_t has been read: the next unit's first P V may overwrite it.
+          // O_t (and with key halves O_1) has been read: the next unit's first P V
+          // may overwrite it.
           tc_fence_before_sync();
           __syncwarp();
-          if (lane == 0) mbar_arrive(bar(L::kBarOFree + t));
+          if (lane == 0) {
+            mbar_arrive(bar(L::kBarOFree + t));
+            if (merge) mbar_arrive(bar(L::kBarOFree + 1));
+          }
         }
         if (lane == 0) bulk_wait_read_all();  // the slab's previous contents have been read
         __syncwarp();

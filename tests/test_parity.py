@@ -44,6 +44,22 @@ def test_edge_lengths(cuda_lib, N, causal, D, dtype):
     compare(o, lse, ro, rl, dtype, p_rounding_term(q, k, v, dtype, causal, scale))
 
 
+@pytest.mark.parametrize("dtype", ["fp16", "bf16"])
+@pytest.mark.parametrize("D", [64, 128])
+@pytest.mark.parametrize("causal", [True, False])
+@pytest.mark.parametrize("N", [1, 127, 129, 257, 513, 1000])
+def test_edge_lengths_with_many_heads(cuda_lib, N, causal, D, dtype):
+    """Enough heads that the launch has at least as many pair units as SMs, so the
+    kernel keeps two query tiles per unit (few heads, as in test_edge_lengths, give
+    key-halves units: one query tile whose key tiles the CTA's two slots share)."""
+    B, H = 4, 40
+    q, k, v = inputs.make_qkv(B, H, N, D, dtype, seed=5000 + N + D, qk_std=1.5)
+    scale = 1.0 / math.sqrt(D)
+    o, lse = run_gpu(q, k, v, causal, scale)
+    ro, rl = oracle_full(q, k, v, dtype, causal, scale)
+    compare(o, lse, ro, rl, dtype, p_rounding_term(q, k, v, dtype, causal, scale))
+
+
 @pytest.mark.parametrize("causal", [True, False])
 def test_zero_queries_give_prefix_mean_at_full_size(cuda_lib, causal):
     # Q = 0: every visible score is 0, so O_i is the mean of the visible v_j and
