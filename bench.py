@@ -530,6 +530,7 @@ def bench_ours(args, w):
     d2h = ho[0].numel() * ho[0].element_size() + hl[0].numel() * hl[0].element_size()
 
     sweep = {}
+    sweep_graph = {}
     if not args.no_sweep and rank == 0:
         # The page's timing (section 8): warm-up, then 7 groups of back-to-back calls timed
         # with CUDA events (5-30 calls a group, about 2 ms of work), the median of the group
@@ -565,7 +566,30 @@ def bench_ours(args, w):
             med = means[len(means) // 2]
             sweep[str(n)] = {"ms": round(med, 4), "tflops": round(sw.flops / (med * 1e-3) / 1e12, 1),
                              "calls_per_group": reps}
-            del sq, sk, sv, so, sl
+            # The same groups captured once in a CUDA graph and replayed: the calls are
+            # unchanged, only the launch gaps between them go (short N is launch-bound).
+            gs = torch.cuda.Stream(dev)
+            gs.wait_stream(stream)
+            graph = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(graph, stream=gs):
+                for _ in range(reps):
+                    eca.attn_fwd_into(sq, sk, sv, so, sl, causal=True, scale=sw.scale, stream=gs)
+            graph.replay()
+            torch.cuda.synchronize(dev)
+            groups = []
+            for g in range(7):
+                flush.zero_()
+                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a.record(stream)
+                graph.replay()
+                b.record(stream)
+                groups.append((a, b))
+            torch.cuda.synchronize(dev)
+            means = sorted(a.elapsed_time(b) / reps for a, b in groups)
+            med = means[len(means) // 2]
+            sweep_graph[str(n)] = {"ms": round(med, 4), "tflops": round(sw.flops / (med * 1e-3) / 1e12, 1),
+                                   "calls_per_group": reps}
+            del graph, sq, sk, sv, so, sl
 
     # Key split on a workload too small in B x H to fill the GPU (causal, B=1, H=4, N=8192, D=128).
     splitkv = bench_split(eca, inputs, dev, stream, flush) if (not args.no_sweep and rank == 0) else {}
@@ -644,6 +668,7 @@ def bench_ours(args, w):
         "gpu_launches": args.steps,
         "clocks": clocks,
         "sweep": sweep,
+        "sweep_graph": sweep_graph,
         "splitkv": splitkv,
         "gqa": gqa,
         "row_softmax": row_softmax,

@@ -437,6 +437,9 @@ int launch(const void* q, const void* k, const void* v, void* o, float* lse, int
     if (rc_slot != ATTN_OK) return rc_slot;
   }
   p.sched = st->sched_pool + 64 * slot;
+  // Divisors of the key-halves unit decoding (dividends are unit and slice indices,
+  // below 2^31).
+  const eca::HalvesDivs hd{eca::make_fast_div(BH), eca::make_fast_div(H), eca::make_fast_div(H / Hkv)};
   p.causal = causal ? 1 : 0;
   p.scale_log2e = scale * 1.4426950408889634f;
   p.wait_limit_ns = kWaitLimitNs;
@@ -444,14 +447,14 @@ int launch(const void* q, const void* k, const void* v, void* o, float* lse, int
   // Persistent: one CTA per SM (the shared-memory footprint admits only one), never more than the units.
   const unsigned grid = static_cast<unsigned>(p.n_units < st->sm_count ? p.n_units : st->sm_count);
   if (dynamic) {
-    eca::attn_fwd_kernel<D, BF16, eca::kModeDynamic><<<grid, eca::kThreads, L::kDynamicBytes, stream>>>(tq, tk, tv,
-                                                                                                      to, p);
+    eca::attn_fwd_kernel<D, BF16, eca::kModeDynamic>
+        <<<grid, eca::kThreads, L::kDynamicBytes, stream>>>(tq, tk, tv, to, p, hd);
   } else if (halves) {
-    eca::attn_fwd_kernel<D, BF16, eca::kModeHalves><<<grid, eca::kThreads, L::kDynamicBytes, stream>>>(tq, tk, tv,
-                                                                                                     to, p);
+    eca::attn_fwd_kernel<D, BF16, eca::kModeHalves>
+        <<<grid, eca::kThreads, L::kDynamicBytes, stream>>>(tq, tk, tv, to, p, hd);
   } else {
-    eca::attn_fwd_kernel<D, BF16, eca::kModePairs><<<grid, eca::kThreads, L::kDynamicBytes, stream>>>(tq, tk, tv,
-                                                                                                    to, p);
+    eca::attn_fwd_kernel<D, BF16, eca::kModePairs>
+        <<<grid, eca::kThreads, L::kDynamicBytes, stream>>>(tq, tk, tv, to, p, hd);
   }
   if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_LAUNCH;
   if (dynamic) {

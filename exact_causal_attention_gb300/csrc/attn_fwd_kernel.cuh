@@ -95,6 +95,35 @@ constexpr int kModePairs = 0;    // two query tiles (or head pairs) per unit, fi
 constexpr int kModeDynamic = 1;  // the same units, taken from the launch's counter in head groups
 constexpr int kModeHalves = 2;   // one query tile per unit, its key tiles in two halves; fixed assignment
 
+// Division of an int in [0, 2^31) by a divisor d >= 1 fixed for the launch, as a
+// multiply-high and two shifts: with l = ceil(log2 d) and m = ceil(2^(31 + l) / d)
+// (below 2^32), floor(x / d) = floor(x m / 2^(31 + l)) = mulhi(2 x, m) >> l.  Exact:
+// m d - 2^(31 + l) < d, so x m / 2^(31 + l) exceeds x / d by less than
+// x / 2^(31 + l) < 2^-l <= 1 / d, which cannot carry floor(x / d) over an integer.
+struct FastDiv {
+  uint32_t m;
+  uint32_t l;
+  int d;
+};
+
+__host__ inline FastDiv make_fast_div(int d) {
+  uint32_t l = 0;
+  while ((1ull << l) < static_cast<unsigned long long>(d)) ++l;
+  const unsigned long long two_s = 1ull << (31 + l);
+  return FastDiv{static_cast<uint32_t>((two_s + static_cast<unsigned long long>(d) - 1) /
+                                       static_cast<unsigned long long>(d)),
+                 l, d};
+}
+
+__device__ __forceinline__ int fast_div(int x, const FastDiv& f) {
+  return static_cast<int>(__umulhi(static_cast<uint32_t>(x) << 1, f.m) >> f.l);
+}
+
+// Divisors of the key-halves unit decoding.
+struct HalvesDivs {
+  FastDiv BH, H, q_per_kv;
+};
+
 struct FwdParams {
   void* o;        // [BH, N, D] 16-bit (unused when part_o is set)
   float* lse;     // [BH, N] or null (unused when part_o is set)
@@ -187,7 +216,26 @@ struct Unit {
 // units come last in every group and the launch ends evenly), then slice, then
 // key segment.
 template <bool kHalves>
-__device__ __forceinline__ void unit_from(int l, const FwdParams& p, Unit& u) {
+__device__ __forceinline__ void unit_from(int l, const FwdParams& p, const HalvesDivs& hd, Unit& u) {
+  if constexpr (kHalves) {
+    // One group of all BH slices, no key split, no head pairs: slice l mod BH, query
+    // tile n_tiles - 1 - l / BH (heaviest first).  Decoded at the start of every
+    // unit by every role, so with multiply-high divisions (short launches are
+    // made of such starts).
+    const int rq = fast_div(l, hd.BH);
+    u.bh = l - rq * p.BH;
+    const int b = fast_div(u.bh, hd.H);
+    u.kvh = b * p.Hkv + fast_div(u.bh - b * p.H, hd.q_per_kv);
+    u.seg = 0;
+    u.tile0 = p.n_pairs - 1 - rq;
+    u.kv0 = 0;
+    const int need = p.causal ? u.tile0 + 1 : p.n_tiles;
+    u.n_kv0 = (need + 1) / 2;
+    u.n_kv1 = need - u.n_kv0;
+    u.kv1 = u.n_kv0;
+    u.n_max = u.n_kv0;
+    return;
+  }
   const int per_slice = p.n_pairs * p.splits;
   const int slices = p.BH >> p.head_pair;
   const int full_groups = slices / p.group_heads;
@@ -203,17 +251,9 @@ __device__ __forceinline__ void unit_from(int l, const FwdParams& p, Unit& u) {
   const int r = local / p.splits;
   u.bh = (grp * p.group_heads + r % g) << p.head_pair;
   u.kvh = (u.bh / p.H) * p.Hkv + (u.bh % p.H) / (p.H / p.Hkv);
-  const int pair = p.n_pairs - 1 - r / g;  // with head pairs or key halves, the query tile
-  u.tile0 = (p.head_pair || kHalves) ? pair : 2 * pair;
+  const int pair = p.n_pairs - 1 - r / g;  // with head pairs, the query tile
+  u.tile0 = p.head_pair ? pair : 2 * pair;
   u.kv0 = u.seg * p.seg_tiles;
-  if (kHalves) {  // never with a key split or head pairs: kv0 = 0
-    const int need = p.causal ? u.tile0 + 1 : p.n_tiles;
-    u.n_kv0 = (need + 1) / 2;
-    u.n_kv1 = need - u.n_kv0;
-    u.kv1 = u.n_kv0;
-    u.n_max = u.n_kv0;
-    return;
-  }
   u.kv1 = u.kv0;
   const int kv_end = u.kv0 + p.seg_tiles < p.n_tiles ? u.kv0 + p.seg_tiles : p.n_tiles;
   const bool has1 = p.head_pair || u.tile0 + 1 < p.n_tiles;
@@ -262,7 +302,7 @@ template <int D, bool BF16, int kMode>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
-                    const FwdParams p) {
+                    const FwdParams p, const HalvesDivs hd) {
   using L = FwdSmem<D>;
   constexpr bool kDynamic = kMode == kModeDynamic;
   constexpr bool kHalves = kMode == kModeHalves;
@@ -312,6 +352,23 @@ __global__ void __launch_bounds__(kThreads, 1)
     tmem_alloc(smem_u32(tmem_slot), kTmemCols);
     tmem_relinquish();
   }
+  // The k-th unit of this CTA under the fixed assignment: unit k G + c of wave k,
+  // the waves dealt to the CTAs in alternating directions; -1 past the last.
+  auto fixed_unit = [&](int k) -> int {
+    const int c = static_cast<int>(blockIdx.x), G = static_cast<int>(gridDim.x);
+    const long long l = static_cast<long long>(k) * G + ((k & 1) ? G - 1 - c : c);
+    return l < p.n_units ? static_cast<int>(l) : -1;
+  };
+  // Next unit with work under the fixed assignment: 1 (in w) or 0 (no more).
+  int units_fixed = 0;
+  auto next_fixed = [&](Unit& w) -> int {
+    while (true) {
+      const int l = fixed_unit(units_fixed++);
+      if (l < 0) return 0;
+      unit_from<kHalves>(l, p, hd, w);
+      if (w.n_max > 0) return 1;
+    }
+  };
   tc_fence_before_sync();
   __syncthreads();
   tc_fence_after_sync();
@@ -335,29 +392,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     ++units_read;
     return true;
   };
-  // The k-th unit of this CTA under the fixed assignment: unit k G + c of wave k,
-  // the waves dealt to the CTAs in alternating directions; -1 past the last.
-  auto fixed_unit = [&](int k) -> int {
-    const int c = static_cast<int>(blockIdx.x), G = static_cast<int>(gridDim.x);
-    const long long l = static_cast<long long>(k) * G + ((k & 1) ? G - 1 - c : c);
-    return l < p.n_units ? static_cast<int>(l) : -1;
-  };
   // Next unit with work for a role: from the fixed assignment, or from the queue
   // under dynamic assignment.  1: got one in w; 0: no more; -1: a wait gave up.
-  int units_fixed = 0;
   auto next_unit = [&](Unit& w, bool whole_warp) -> int {
-    if (!kDynamic) {
-      while (true) {
-        const int l = fixed_unit(units_fixed++);
-        if (l < 0) return 0;
-        unit_from<kHalves>(l, p, w);
-        if (w.n_max > 0) return 1;
-      }
-    }
+    if (!kDynamic) return next_fixed(w);
     int l;
     if (!read_unit(l, whole_warp)) return -1;
     if (l < 0) return 0;
-    unit_from<kHalves>(l, p, w);
+    unit_from<kHalves>(l, p, hd, w);
     return 1;
   };
 
@@ -386,7 +428,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int l = atomicAdd(p.sched, 1);
           if (l >= p.n_units) return -1;
           Unit u;
-          unit_from<kHalves>(l, p, u);
+          unit_from<kHalves>(l, p, hd, u);
           if (u.n_max > 0) return l;
         }
       };
@@ -396,7 +438,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (kDynamic) {
           const int l = take_unit();
           if (!push_unit(l) || l < 0) break;
-          unit_from<kHalves>(l, p, w);
+          unit_from<kHalves>(l, p, hd, w);
         } else if (next_unit(w, false) != 1) {
           break;
         }
@@ -881,9 +923,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       // O = o / l rounded to the output type, 64 columns at a time.  Each warp
       // sends its 32 rows through its slab of the staging buffer with TMA stores
       // (rows past N are clipped by the tensor map).
-      const uint32_t slab = sbase + L::kOutOff + t * L::kStageOutBytes + wq * 4096;
+      // With key halves slot 1 stores nothing, so slot 0 sends its two 64-column
+      // blocks through both tiles' staging buffers and need not wait between them.
 #pragma unroll
       for (int c64 = 0; c64 < D / 64; ++c64) {
+        const uint32_t slab = sbase + L::kOutOff + (kHalves ? c64 : t) * L::kStageOutBytes + wq * 4096;
         uint32_t h[32];
 #pragma unroll
         for (int half = 0; half < 2; ++half) {
@@ -919,7 +963,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (merge) mbar_arrive(bar(L::kBarOFree + 1));
           }
         }
-        if (lane == 0) bulk_wait_read_all();  // the slab's previous contents have been read
+        // The slab's previous contents have been read (with key halves, the first
+        // wait covers both slabs).
+        if (lane == 0 && (!kHalves || c64 == 0)) bulk_wait_read_all();
         __syncwarp();
 #pragma unroll
         for (int ch = 0; ch < 8; ++ch) {
