@@ -178,13 +178,21 @@ __global__ void __maxnreg__(128) paged_decode_kernel(const __grid_constant__ CUt
   const int log2T = 31 - __clz(T);
   const int pages_per_tile = kDecTile >> log2T;
 
+  // The segment's first page ids are read together with the length rather than
+  // after it (the table row holds max_pages entries, so the read stays inside it);
+  // ids past the request's last page are read but never followed.
+  const int* table_row = p.block_table + static_cast<size_t>(b) * p.max_pages;
+  const int pg_begin = seg * p.seg_pages;
+  int id_first = -1;
+  if (tid < kDecIdRing && pg_begin + tid < min(p.max_pages, pg_begin + p.seg_pages)) {
+    id_first = table_row[pg_begin + tid];
+  }
   int len = p.lengths[b];
   if (len < 0 || len > p.max_pages * T) {
     if (tid == 0) atomicExch(p.status, p.bad_index_code);
     len = len < 0 ? 0 : p.max_pages * T;
   }
   const int n_pages = (len + T - 1) >> log2T;
-  const int pg_begin = seg * p.seg_pages;
   const int pg_end = min(n_pages, pg_begin + p.seg_pages);
   const int n_tiles = pg_end > pg_begin ? (pg_end - pg_begin + pages_per_tile - 1) / pages_per_tile : 0;
 
@@ -206,8 +214,7 @@ __global__ void __maxnreg__(128) paged_decode_kernel(const __grid_constant__ CUt
     }
     return id;
   };
-  const int* table_row = p.block_table + static_cast<size_t>(b) * p.max_pages;
-  if (tid < kDecIdRing && pg_begin + tid < pg_end) ids_s[tid] = table_row[pg_begin + tid];
+  if (tid < kDecIdRing && pg_begin + tid < pg_end) ids_s[tid] = id_first;
   // Q of the chunk as A fragments of the score products (rows = heads, padded with
   // zeros to 16), the same for every compute warp: entry [k][l] holds, for lane l,
   // dims 16 k + 2 (l % 4) .. + 1 and the same + 8 of head l / 4.
@@ -483,27 +490,40 @@ __global__ void __maxnreg__(128) paged_decode_kernel(const __grid_constant__ CUt
   } else if (!(valid == 0 && seg == 0)) {
     return;  // an empty segment; an empty request is finished by its segment 0
   }
-  for (int idx = tid; idx < HC * (D / 2); idx += kDecThreads) {
-    const int k = idx / (D / 2), cp = idx % (D / 2);
+  // The segments' log-sum-exps of the chunk's heads, all read at once into shared
+  // memory (over the idle ring), then every thread's share of the partial outputs.
+  float* seg_lse = red_s;  // [HC][valid]
+  for (int e = tid; e < HC * valid; e += kDecThreads) {
+    const int k = e / valid, sg = e - k * valid;
+    seg_lse[e] = __ldcg(p.part_lse + sg * stride + static_cast<size_t>(b) * p.Hq + qh0 + k);
+  }
+  __syncthreads();
+  for (int idx = tid; idx < HC * (D / 4); idx += kDecThreads) {
+    const int k = idx / (D / 4), c4 = idx % (D / 4);
     const size_t row = static_cast<size_t>(b) * p.Hq + qh0 + k;
+    const float* ls = seg_lse + k * valid;
     float m = -INFINITY;
-    for (int sg = 0; sg < valid; ++sg) m = fmaxf(m, __ldcg(p.part_lse + sg * stride + row));
+    for (int sg = 0; sg < valid; ++sg) m = fmaxf(m, ls[sg]);
     float wsum = 0.f;
-    float2 acc = make_float2(0.f, 0.f);
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
     if (m != -INFINITY) {
+#pragma unroll 4
       for (int sg = 0; sg < valid; ++sg) {
-        const float lse_s = __ldcg(p.part_lse + sg * stride + row);
-        if (lse_s == -INFINITY) continue;
-        const float wgt = expf(lse_s - m);
+        const float lse_s = ls[sg];
+        const float wgt = lse_s == -INFINITY ? 0.f : expf(lse_s - m);
         wsum += wgt;
-        const float2 o_s = __ldcg(reinterpret_cast<const float2*>(p.part_o + (sg * stride + row) * D + 2 * cp));
+        if (wgt == 0.f) continue;
+        const float4 o_s = __ldcg(reinterpret_cast<const float4*>(p.part_o + (sg * stride + row) * D + 4 * c4));
         acc.x += wgt * o_s.x;
         acc.y += wgt * o_s.y;
+        acc.z += wgt * o_s.z;
+        acc.w += wgt * o_s.w;
       }
     }
     const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
-    *reinterpret_cast<uint32_t*>(static_cast<uint16_t*>(p.out) + row * D + 2 * cp) = pack2<BF16>(acc.x * inv, acc.y * inv);
-    if (cp == 0 && p.lse != nullptr) p.lse[row] = wsum > 0.f ? m + logf(wsum) : -INFINITY;
+    uint2 packed = make_uint2(pack2<BF16>(acc.x * inv, acc.y * inv), pack2<BF16>(acc.z * inv, acc.w * inv));
+    *reinterpret_cast<uint2*>(static_cast<uint16_t*>(p.out) + row * D + 4 * c4) = packed;
+    if (c4 == 0 && p.lse != nullptr) p.lse[row] = wsum > 0.f ? m + logf(wsum) : -INFINITY;
   }
 }
 

@@ -194,7 +194,8 @@ int attn_splitkv_default_splits(int B, int H, int N, int D);
  *   cache       : device, [num_pages, 2, page_size, Hkv, D] fp16 (index 0 = K,
  *                 1 = V), 16-byte aligned, read only.
  *   block_table : device, [B, max_pages] int32; entries past a request's last
- *                 page are never read.
+ *                 page may be read (they lie inside the row) but are never
+ *                 followed, so their values do not matter.
  *   lengths     : device, [B] int32, 0 .. max_pages * page_size.
  *   out         : device, [B, Hq, D] fp16, written in full.
  *   lse         : device, [B, Hq] fp32 natural-log log-sum-exp, or NULL.
