@@ -299,6 +299,59 @@ def bench_split(eca, inputs, dev, stream, flush):
             "launches_per_call": 2}
 
 
+def bench_sweep_point(eca, inputs, dev, stream, flush, n):
+    """One point of the sweep (causal B=1 H=32 D=128 fp16, seed 1): 10 single calls after an L2
+    flush each (median), and 20 back-to-back calls eager and replayed from a CUDA graph."""
+    import torch
+
+    sw = inputs.sweep_workload(n)
+    sq, sk, sv = (x.to(dev) for x in inputs.workload_qkv(sw))
+    so = torch.empty_like(sq)
+    sl = torch.empty((sw.B, sw.H, sw.N), dtype=torch.float32, device=dev)
+
+    def call(s=stream):
+        eca.attn_fwd_into(sq, sk, sv, so, sl, causal=True, scale=sw.scale, stream=s)
+
+    for _ in range(3):
+        call()
+    single = []
+    for i in range(13):
+        flush.zero_()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        call()
+        b.record(stream)
+        single.append((a, b))
+    torch.cuda.synchronize(dev)
+    single_ms = sorted(a.elapsed_time(b) for a, b in single[3:])[5]
+    flush.zero_()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(20):
+        call()
+    b.record(stream)
+    torch.cuda.synchronize(dev)
+    eager_ms = a.elapsed_time(b) / 20
+    gs = torch.cuda.Stream(dev)
+    gs.wait_stream(stream)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=gs):
+        for _ in range(20):
+            call(gs)
+    graph.replay()
+    flush.zero_()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    graph.replay()
+    b.record(stream)
+    torch.cuda.synchronize(dev)
+    graph_ms = a.elapsed_time(b) / 20
+    tf = lambda ms: round(sw.flops / (ms * 1e-3) / 1e12, 1)  # noqa: E731
+    return {"workload": sw.name, "single_ms": round(single_ms, 4), "single_tflops": tf(single_ms),
+            "eager_ms": round(eager_ms, 4), "eager_tflops": tf(eager_ms), "graph_ms": round(graph_ms, 4),
+            "graph_tflops": tf(graph_ms)}
+
+
 def bench_gqa(eca, inputs, dev, stream, flush):
     """Grouped heads, causal B=1 H=32 Hkv=8 N=8192 D=128 fp16 (4 query heads per key/value head);
     L2 flushed before every call; TFLOP/s counts 2BHN²D."""
@@ -700,12 +753,14 @@ def main():
     ap.add_argument("--softmax-only", action="store_true", help="only the row-softmax measurement")
     ap.add_argument("--split-only", action="store_true", help="only the key-split measurement")
     ap.add_argument("--gqa-only", action="store_true", help="only the grouped-head measurement")
+    ap.add_argument("--sweep-only", type=int, metavar="N",
+                    help="only the sweep workload at this N (causal B=1 H=32 D=128 fp16), eager and from a graph")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
     from exact_causal_attention_gb300 import inputs
 
     w = inputs.WORKLOADS[WORKLOAD]
-    if args.paged_only is not None or args.softmax_only or args.split_only or args.gqa_only:
+    if args.paged_only is not None or args.softmax_only or args.split_only or args.gqa_only or args.sweep_only:
         # One side measurement alone (for profiling its kernels); one JSON line.
         import torch
 
@@ -720,6 +775,8 @@ def main():
             out = {"paged_decode": bench_paged(eca, inputs, dev, stream, flush, contexts)}
         elif args.softmax_only:
             out = {"row_softmax": bench_row_softmax(eca, inputs, dev, stream, flush)}
+        elif args.sweep_only:
+            out = {"sweep": bench_sweep_point(eca, inputs, dev, stream, flush, args.sweep_only)}
         elif args.gqa_only:
             out = {"gqa": bench_gqa(eca, inputs, dev, stream, flush)}
         else:
