@@ -1,9 +1,12 @@
-"""attn_fwd captured in a CUDA graph: the calls only enqueue work on the caller's
-stream and allocate nothing, so a captured sequence replays with the same results
-as eager calls (bit for bit: same kernels, same unit order).  Covers the three ways
-the kernel forms its work units: key halves (short sequences), pairs of query tiles,
-and units handed out from a device counter (K and V over 64 MiB), whose counters must
-come back to zero after every replay."""
+"""Launch-level behaviour of attn_fwd.
+
+Captured in a CUDA graph: the calls only enqueue work on the caller's stream and
+allocate nothing, so a captured sequence replays with the same results as eager
+calls (bit for bit: same kernels, same unit order).  Covers the three ways the
+kernel forms its work units: key halves (short sequences), pairs of query tiles,
+and units handed out from a device counter (K and V over 64 MiB), whose counters
+must come back to zero after every replay.  Also: more concurrent counter launches
+than counter slots, and the tensor-map cache across shape changes."""
 import numpy as np
 import pytest
 import torch
@@ -43,3 +46,51 @@ def test_captured_calls_replay_like_eager_calls(cuda_lib, B, H, N, D):
     torch.cuda.synchronize()
     assert torch.equal(o2, o_ref)
     assert np.isfinite(o.float().cpu().numpy()).all()
+
+
+def test_more_concurrent_counter_launches_than_slots(cuda_lib):
+    """Launches that take their units from a device counter (K and V over 64 MiB) use one
+    of 64 counter slots per device, in turn.  66 such launches on 66 streams, none waiting
+    for another, must all give the eager result: the 65th and 66th reuse the first two
+    slots only after those launches have finished (the library orders them on the GPU)."""
+    eca = cuda_lib
+    B, H, N, D = 1, 40, 8192, 128  # K + V = 160 MiB
+    q, k, v = (x.cuda() for x in inputs.make_qkv(B, H, N, D, "fp16", seed=616))
+    o_ref = torch.empty_like(q)
+    eca.attn_fwd_into(q, k, v, o_ref, None, causal=True)
+    torch.cuda.synchronize()
+    outs = [torch.full_like(q, float("nan")) for _ in range(66)]
+    streams = [torch.cuda.Stream() for _ in range(66)]
+    for s in streams:
+        s.wait_stream(torch.cuda.current_stream())
+    for o, s in zip(outs, streams):
+        eca.attn_fwd_into(q, k, v, o, None, causal=True, stream=s)
+    torch.cuda.synchronize()
+    assert eca.device_status() == 0
+    for i, o in enumerate(outs):
+        assert torch.equal(o, o_ref), f"launch {i}"
+
+
+def test_tensor_map_cache_follows_shape_changes(cuda_lib):
+    """The library caches tensor maps by address and shape: calls that reuse the same
+    buffers with other lengths, head counts and types must each be encoded anew."""
+    from helpers import compare, oracle_full, p_rounding_term
+
+    eca = cuda_lib
+    D = 64
+    buf = [torch.zeros(2 * 4 * 1024 * D, dtype=torch.float16, device="cuda") for _ in range(4)]
+    for (B, H, N, dtype) in [(1, 4, 1024, "fp16"), (2, 2, 700, "fp16"), (1, 4, 1024, "fp16"), (1, 8, 333, "bf16")]:
+        hq, hk, hv = inputs.make_qkv(B, H, N, D, dtype, seed=B * 100 + H + N)
+        n = B * H * N * D
+        t = inputs.TORCH_DTYPES[dtype]
+        q, k, v, o = (b.view(torch.int16)[:n].view(t).view(B, H, N, D) for b in buf)
+        q.copy_(hq.cuda())
+        k.copy_(hk.cuda())
+        v.copy_(hv.cuda())
+        o.fill_(float("nan"))
+        lse = torch.full((B, H, N), float("nan"), device="cuda")
+        eca.attn_fwd_into(q, k, v, o, lse, causal=True)
+        torch.cuda.synchronize()
+        ro, rl = oracle_full(hq, hk, hv, dtype, True, 1.0 / D ** 0.5)
+        compare(o.double().cpu().numpy(), lse.double().cpu().numpy(), ro, rl, dtype,
+                p_rounding_term(hq, hk, hv, dtype, True, 1.0 / D ** 0.5))
