@@ -142,30 +142,35 @@ def test_out_of_range_entries_are_rejected_not_read(cuda_lib):
     assert eca.device_status() == 0
 
 
-def test_split_merge_in_kernel_repeats_bit_identically(cuda_lib):
+@pytest.mark.parametrize("splits", [5, 12])
+def test_split_merge_in_kernel_repeats_bit_identically(cuda_lib, splits):
     # The segments of a split are merged by the last one to finish, counted with
-    # device counters that return to zero after every launch: repeated launches
-    # (same slot reused after the pool wraps) give identical results.
+    # device counters that return to zero after every launch: repeated launches (the
+    # same slot reused after the pool wraps) give identical results, with 5 segments
+    # and with 12, and both match the oracle.
     B, Hq, Hkv, D, T = 4, 16, 4, 128, 16
     lengths = [900, 64, 3000, 17]
     q, cache, table, lens = inputs.paged_decode_inputs(B, Hq, Hkv, D, T, lengths, "fp16", seed=91)
     scale = 1.0 / math.sqrt(D)
-    first = run_decode(q, cache, table, lens, scale, 5)
+    first = run_decode(q, cache, table, lens, scale, splits)
     for _ in range(10):
-        again = run_decode(q, cache, table, lens, scale, 5)
+        again = run_decode(q, cache, table, lens, scale, splits)
         assert np.array_equal(first[0], again[0]) and np.array_equal(first[1], again[1])
     ro, rl = oracle_decode(q, cache, table, lens, T, scale, "fp16")
     check(first[0], first[1], ro, rl, "fp16", None, lengths)
 
 
 def test_split_merge_kernel_for_many_groups(cuda_lib):
-    # More (request, K/V head, head chunk) groups than one counter slot holds: the
-    # separate merge kernel runs instead of the in-kernel merge.
-    B, Hq, Hkv, D, T = 600, 8, 8, 64, 8
+    # More (request, K/V head, head chunk) groups than one counter slot holds
+    # (520 x 8 = 4160 > 4096): the separate merge kernel runs.  With 64-token pages a
+    # tile is one page, so requests of up to 10 pages split 10 ways; shorter ones leave
+    # trailing segments empty.
+    B, Hq, Hkv, D, T = 520, 8, 8, 64, 64
     rng = np.random.default_rng(5)
-    lengths = [int(x) for x in rng.integers(0, 40, size=B)]
+    lengths = [int(x) for x in rng.integers(0, 641, size=B)]
+    lengths[0] = 640
     q, cache, table, lens = inputs.paged_decode_inputs(B, Hq, Hkv, D, T, lengths, "fp16", seed=92)
     scale = 1.0 / math.sqrt(D)
-    o, lse = run_decode(q, cache, table, lens, scale, 2)
+    o, lse = run_decode(q, cache, table, lens, scale, 10)
     ro, rl = oracle_decode(q, cache, table, lens, T, scale, "fp16")
     check(o, lse, ro, rl, "fp16", None, lengths)
