@@ -352,6 +352,61 @@ def bench_sweep_point(eca, inputs, dev, stream, flush, n):
             "graph_tflops": tf(graph_ms)}
 
 
+ANATOMY_POINTS = ("entry", "setup_done", "first_k_load_issued", "first_qk_issued", "first_s_ready",
+                  "first_o_ready_tile0", "first_output_issued_tile0", "first_o_ready_tile1", "exit")
+
+
+def bench_anatomy(eca, inputs, dev, stream, flush, n):
+    """Per-CTA milestones of two back-to-back attention launches (the sweep workload at N,
+    after an L2 flush, both queued behind a spinning kernel), from the anatomy build of
+    the library: for each milestone the min / mean / max over CTAs in microseconds after
+    the first CTA of the first launch started, the units per CTA, and the gap between
+    the last CTA of the first launch and the first of the second."""
+    import ctypes
+
+    import torch
+
+    lib = eca.load_library(eca.ANATOMY_LIB_PATH)
+    sw = inputs.sweep_workload(n)
+    sq, sk, sv = (x.to(dev) for x in inputs.workload_qkv(sw))
+    so = torch.empty_like(sq)
+    sl = torch.empty((sw.B, sw.H, sw.N), dtype=torch.float32, device=dev)
+
+    def call():
+        eca.attn_fwd_into(sq, sk, sv, so, sl, causal=True, scale=sw.scale, stream=stream)
+
+    for _ in range(3):
+        call()
+    words = 2 * 160 * 10
+    buf = (ctypes.c_ulonglong * words)()
+    if lib.attn_anatomy_read(buf, words, 1) != 0:
+        raise RuntimeError("attn_anatomy_read failed: not the anatomy build?")
+    flush.zero_()
+    # A spinning kernel of about 0.5 ms ahead of the two calls, so both are queued on
+    # the GPU before the first starts and the gap between them is the GPU's own.
+    torch.cuda._sleep(1_000_000)
+    call()
+    call()
+    torch.cuda.synchronize(dev)
+    if lib.attn_anatomy_read(buf, words, 1) != 0:
+        raise RuntimeError("attn_anatomy_read failed")
+    st = [[[buf[(sl_ * 160 + c) * 10 + i] for i in range(10)] for c in range(160)] for sl_ in range(2)]
+    t0 = min(st[0][c][0] for c in range(160) if st[0][c][0])
+    out = {"workload": sw.name, "launches": []}
+    for slot in range(2):
+        ctas = [c for c in range(160) if st[slot][c][0]]
+        rec = {"ctas": len(ctas), "units_per_cta": sorted({st[slot][c][9] for c in ctas})}
+        for i, name in enumerate(ANATOMY_POINTS):
+            v = [(st[slot][c][i] - t0) / 1000.0 for c in ctas if st[slot][c][i]]
+            if v:
+                rec[name] = {"min": round(min(v), 2), "mean": round(sum(v) / len(v), 2), "max": round(max(v), 2)}
+        out["launches"].append(rec)
+    a, b = out["launches"]
+    if "exit" in a and "entry" in b:
+        out["gap_us_last_exit_to_next_first_entry"] = round(b["entry"]["min"] - a["exit"]["max"], 2)
+    return out
+
+
 def bench_gqa(eca, inputs, dev, stream, flush):
     """Grouped heads, causal B=1 H=32 Hkv=8 N=8192 D=128 fp16 (4 query heads per key/value head);
     L2 flushed before every call; TFLOP/s counts 2BHN²D."""
@@ -753,6 +808,8 @@ def main():
     ap.add_argument("--softmax-only", action="store_true", help="only the row-softmax measurement")
     ap.add_argument("--split-only", action="store_true", help="only the key-split measurement")
     ap.add_argument("--gqa-only", action="store_true", help="only the grouped-head measurement")
+    ap.add_argument("--anatomy", type=int, metavar="N",
+                    help="per-CTA milestones of two back-to-back launches of the sweep workload at N (anatomy build)")
     ap.add_argument("--sweep-only", type=int, metavar="N",
                     help="only the sweep workload at this N (causal B=1 H=32 D=128 fp16), eager and from a graph")
     args = ap.parse_args()
@@ -760,13 +817,15 @@ def main():
     from exact_causal_attention_gb300 import inputs
 
     w = inputs.WORKLOADS[WORKLOAD]
-    if args.paged_only is not None or args.softmax_only or args.split_only or args.gqa_only or args.sweep_only:
+    if (args.paged_only is not None or args.softmax_only or args.split_only or args.gqa_only or args.sweep_only
+            or args.anatomy):
         # One side measurement alone (for profiling its kernels); one JSON line.
         import torch
 
         import exact_causal_attention_gb300 as eca
 
-        eca.load_library()
+        if not args.anatomy:
+            eca.load_library()
         dev = torch.device("cuda", 0)
         flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
         stream = torch.cuda.current_stream(dev)
@@ -775,6 +834,8 @@ def main():
             out = {"paged_decode": bench_paged(eca, inputs, dev, stream, flush, contexts)}
         elif args.softmax_only:
             out = {"row_softmax": bench_row_softmax(eca, inputs, dev, stream, flush)}
+        elif args.anatomy:
+            out = {"anatomy": bench_anatomy(eca, inputs, dev, stream, flush, args.anatomy)}
         elif args.sweep_only:
             out = {"sweep": bench_sweep_point(eca, inputs, dev, stream, flush, args.sweep_only)}
         elif args.gqa_only:

@@ -17,6 +17,8 @@ __all__ = ["attn_fwd", "attn_fwd_into", "attn_fwd_gqa", "attn_fwd_splitkv", "spl
            "STATUS"]
 
 _LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "_build", "libeca_attn.so")
+# The same library with the attention kernel's per-CTA milestone stamps compiled in.
+ANATOMY_LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "_build", "libeca_attn_anatomy.so")
 _lock = threading.Lock()
 _lib = None
 
@@ -54,6 +56,7 @@ SIGNATURES = {
     "attn_paged_append": (_I, [_VP, _VP, _VP, _VP, _I, _I, _I, _I, _I, _I, _VP]),
     "attn_device_status": (_I, [_VP]),
     "attn_watchdog_selftest": (_I, [_U, _VP]),
+    "attn_anatomy_read": (_I, [ctypes.POINTER(ctypes.c_ulonglong), _SZ, _I]),
     "attn_status_string": (ctypes.c_char_p, [_I]),
     "attn_version": (_I, []),
 }

@@ -11,6 +11,9 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(PKG, "_build")
 LIB_NAME = "libeca_attn.so"
 LIB_PATH = os.path.join(BUILD_DIR, LIB_NAME)
+# The same sources with ECA_ANATOMY: the attention kernel records per-CTA milestone
+# stamps (a measurement aid; nothing else changes).
+ANATOMY_LIB_PATH = os.path.join(BUILD_DIR, "libeca_attn_anatomy.so")
 SOURCES = ["attn_api.cu"]
 ARCH_FLAGS = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
@@ -27,22 +30,32 @@ def _deps():
     return files
 
 
-def build(force: bool = False, verbose: bool = False) -> str:
-    """Compile csrc/ into _build/libeca_attn.so unless it is newer than every source."""
-    os.makedirs(BUILD_DIR, exist_ok=True)
-    if not force and os.path.exists(LIB_PATH):
-        newest = max(os.path.getmtime(f) for f in _deps())
-        if os.path.getmtime(LIB_PATH) >= newest:
-            return LIB_PATH
+def _command(out: str, defines, verbose: bool):
     cuda_lib = os.path.join(os.environ.get("CUDA_HOME", "/usr/local/cuda"), "lib64")
-    tmp = LIB_PATH + f".tmp{os.getpid()}"
     cmd = [_nvcc(), *ARCH_FLAGS, "-O3", "-lineinfo", "-std=c++17", "--shared", "-Xcompiler", "-fPIC",
-           "-cudart", "shared", "-I", INCLUDE, "-I", CSRC, "-Xlinker", f"-rpath,{cuda_lib}",
-           "-o", tmp, *[os.path.join(CSRC, s) for s in SOURCES]]
+           "-cudart", "shared", "-I", INCLUDE, "-I", CSRC, "-Xlinker", f"-rpath,{cuda_lib}", *defines,
+           "-o", out, *[os.path.join(CSRC, s) for s in SOURCES]]
     if verbose:
         cmd.insert(1, "-Xptxas=-v")
-    subprocess.run(cmd, check=True)
-    os.replace(tmp, LIB_PATH)
+    return cmd
+
+
+def build(force: bool = False, verbose: bool = False) -> str:
+    """Compile csrc/ into _build/libeca_attn.so (and the anatomy variant beside it, in
+    parallel) unless both are newer than every source.  Returns the main library."""
+    os.makedirs(BUILD_DIR, exist_ok=True)
+    newest = max(os.path.getmtime(f) for f in _deps())
+    todo = [(path, defines) for path, defines in ((LIB_PATH, []), (ANATOMY_LIB_PATH, ["-DECA_ANATOMY"]))
+            if force or not os.path.exists(path) or os.path.getmtime(path) < newest]
+    procs = []
+    for path, defines in todo:
+        tmp = path + f".tmp{os.getpid()}"
+        procs.append((subprocess.Popen(_command(tmp, defines, verbose)), tmp, path))
+    failed = [path for proc, _, path in procs if proc.wait() != 0]
+    if failed:
+        raise subprocess.CalledProcessError(1, f"nvcc for {failed}")
+    for _, tmp, path in procs:
+        os.replace(tmp, path)
     return LIB_PATH
 
 

@@ -941,6 +941,36 @@ int attn_watchdog_selftest(unsigned int timeout_us, attn_stream_t stream) {
   return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_LAUNCH;
 }
 
+int attn_anatomy_read(unsigned long long* out, size_t out_words, int reset) {
+#ifdef ECA_ANATOMY
+  constexpr size_t kWords = 2 * eca::kAnatomyCtas * eca::kAnatomyPoints;
+  if (out == nullptr || out_words < kWords) return ATTN_ERR_INVALID_ARG;
+  std::lock_guard<std::mutex> lock(g_mutex);
+  DeviceState* st = nullptr;
+  const int r = device_state(&st);
+  if (r != ATTN_OK) return r;
+  if (cudaDeviceSynchronize() != cudaSuccess) return ATTN_ERR_CUDA;
+  if (cudaMemcpyFromSymbol(out, eca::g_anatomy, kWords * sizeof(unsigned long long)) != cudaSuccess) {
+    return ATTN_ERR_CUDA;
+  }
+  if (reset) {
+    static const unsigned long long zeros[kWords] = {};
+    const int zero = 0;
+    if (cudaMemcpyToSymbol(eca::g_anatomy, zeros, sizeof(zeros)) != cudaSuccess ||
+        cudaMemcpyToSymbol(eca::g_anatomy_launch, &zero, sizeof(int)) != cudaSuccess ||
+        cudaMemcpyToSymbol(eca::g_anatomy_exited, &zero, sizeof(int)) != cudaSuccess) {
+      return ATTN_ERR_CUDA;
+    }
+  }
+  return ATTN_OK;
+#else
+  (void)out;
+  (void)out_words;
+  (void)reset;
+  return ATTN_ERR_INVALID_ARG;  // not the anatomy build
+#endif
+}
+
 const char* attn_status_string(int status) {
   switch (status) {
     case ATTN_OK: return "ok";

@@ -124,6 +124,26 @@ struct HalvesDivs {
   FastDiv BH, H, q_per_kv;
 };
 
+// Anatomy build (compiled with ECA_ANATOMY, a separate library for measurement):
+// every CTA records globaltimer stamps of its first unit's milestones, in one of two
+// slots chosen by a launch counter, so two launches in a row can be compared.  In
+// the normal build the stamps compile to nothing.
+constexpr int kAnatomyCtas = 160;
+constexpr int kAnatomyPoints = 10;
+#ifdef ECA_ANATOMY
+__device__ unsigned long long g_anatomy[2][kAnatomyCtas][kAnatomyPoints];
+__device__ int g_anatomy_launch;
+__device__ int g_anatomy_exited;
+#define ECA_STAMP(slot, i)                                                                       \
+  do {                                                                                           \
+    if (blockIdx.x < kAnatomyCtas) g_anatomy[(slot)][blockIdx.x][(i)] = global_timer_ns();        \
+  } while (0)
+#else
+#define ECA_STAMP(slot, i) \
+  do {                     \
+  } while (0)
+#endif
+
 struct FwdParams {
   void* o;        // [BH, N, D] 16-bit (unused when part_o is set)
   float* lse;     // [BH, N] or null (unused when part_o is set)
@@ -319,6 +339,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   // below) as warp-uniform.
   const int warp = __shfl_sync(0xffffffffu, static_cast<int>(threadIdx.x / 32), 0);
   const int lane = threadIdx.x % 32;
+#ifdef ECA_ANATOMY
+  const int an_slot = *reinterpret_cast<volatile int*>(&g_anatomy_launch) & 1;
+  if (threadIdx.x == 0) ECA_STAMP(an_slot, 0);  // entry
+#endif
 
   if (threadIdx.x == 0) {
     for (int t = 0; t < 2; ++t) {
@@ -373,6 +397,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after_sync();
   const uint32_t tmem = __shfl_sync(0xffffffffu, *tmem_slot, 0);
+#ifdef ECA_ANATOMY
+  if (threadIdx.x == 0) ECA_STAMP(an_slot, 1);  // set-up done
+  int an_units = 0;
+#endif
   const Watchdog wd{abort_flag, p.status, p.wait_limit_ns, p.timeout_code};
   // Readers of the unit queue: entry n holds the n-th unit this CTA works on,
   // or -1 after the last.  `read_unit` is called by a whole warp (lane 0 alone
@@ -474,6 +502,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             } else {
               mbar_arrive(full_k);
             }
+#ifdef ECA_ANATOMY
+            if (it == 0) ECA_STAMP(an_slot, 2);  // first K load issued
+#endif
             ++it;
           }
         }
@@ -491,6 +522,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // waiting for the other.
     if (lane == 0) {
       tma_prefetch_map(&tm_q);
+      tma_prefetch_map(&tm_o);  // for the epilogue's first store, well before it
       const uint64_t pol_q = policy_evict_first();
       int loads[2] = {0, 0};
       bool ok = true;
@@ -576,6 +608,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
         }
         if (n_kv > 0) issue_qk<D, BF16>(s_tmem, q_desc, ring_k_desc + stage_off(x));
+#ifdef ECA_ANATOMY
+        if (t == 0 && base == 0 && lane == 0) ECA_STAMP(an_slot, 3);  // first Q K^T issued
+        if (t == 0 && lane == 0) ++an_units;
+#endif
         pass_turn();
         if (n_kv > 0) tc_commit_warp(bar(L::kBarS + t));
         if (n_kv == 1) tc_commit_warp(bar(L::kBarQFree + t));  // this tile's Q K^T are all issued
@@ -685,6 +721,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
         }
         ++s_waits;
+#ifdef ECA_ANATOMY
+        if (t == 0 && s_waits == 1 && wq == 0 && lane == 0) ECA_STAMP(an_slot, 4);  // first S ready
+#endif
         tc_fence_after_sync();
         uint32_t s[4][32];
         // S of this key tile, masked: the diagonal tile (causal) or the ragged
@@ -860,6 +899,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         break;
       }
       ++o_waits;
+#ifdef ECA_ANATOMY
+      if (o_waits == 1 && wq == 0 && lane == 0) ECA_STAMP(an_slot, t == 0 ? 5 : 7);  // first unit's O ready
+#endif
       tc_fence_after_sync();
 
       if (kHalves && t == 1) {
@@ -982,6 +1024,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (p.lse != nullptr && row < p.N) {
         p.lse[static_cast<size_t>(head) * p.N + row] = row_lse;
       }
+#ifdef ECA_ANATOMY
+      if (t == 0 && o_waits == 1 && wq == 0 && lane == 0) ECA_STAMP(an_slot, 6);  // first unit's output issued
+#endif
     }
     // The staging slabs must stay valid until the stores have read them; the
     // writes themselves complete before the grid does.
@@ -1002,6 +1047,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
     tc_fence_after_sync();
     tmem_dealloc(tmem, kTmemCols);
+#ifdef ECA_ANATOMY
+    if (lane == 0) {
+      ECA_STAMP(an_slot, 8);  // exit
+      if (blockIdx.x < kAnatomyCtas) g_anatomy[an_slot][blockIdx.x][9] = static_cast<unsigned long long>(an_units);
+      __threadfence();
+      if (atomicAdd(&g_anatomy_exited, 1) == static_cast<int>(gridDim.x) - 1) {
+        g_anatomy_exited = 0;
+        __threadfence();
+        atomicAdd(&g_anatomy_launch, 1);
+      }
+    }
+#endif
   }
 }
 

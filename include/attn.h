@@ -283,6 +283,21 @@ int attn_device_status(attn_stream_t stream);
  */
 int attn_watchdog_selftest(unsigned int timeout_us, attn_stream_t stream);
 
+/*
+ * attn_anatomy_read -- measurement aid, no counterpart on the pages.  The library
+ * also builds as libeca_attn_anatomy.so (compiled with ECA_ANATOMY), whose attention
+ * kernel records, in every CTA, globaltimer stamps (ns) of its first unit's
+ * milestones; two launches in a row land in two slots.  This call synchronises the
+ * device and copies them to `out`: [2 slots][160 CTAs][10 words], words 0-8 the
+ * stamps (entry, set-up done, first K load issued, first Q K^T issued, first S
+ * ready, first unit's O ready for tile 0, its output issued, the same O for tile 1,
+ * exit; 0 where a CTA has none) and word 9 the units the CTA processed; the slot
+ * of a launch is the parity of the launches since the last reset.  reset != 0 then
+ * zeroes the stamps and the launch count.  out_words must be at least 3200.
+ * Returns ATTN_ERR_INVALID_ARG in the normal build.
+ */
+int attn_anatomy_read(unsigned long long* out, size_t out_words, int reset);
+
 /* Text for a status code (static storage, never NULL). */
 const char* attn_status_string(int status);
 

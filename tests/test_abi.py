@@ -35,6 +35,19 @@ def test_every_declared_symbol_is_exported(lib):
         assert hasattr(lib, name), name
 
 
+def test_anatomy_build_exports_the_same_symbols(lib):
+    """The measurement variant (stamps compiled in) exports every declared function too;
+    in the normal build its read-out call refuses."""
+    lib2 = ctypes.CDLL(eca.ANATOMY_LIB_PATH)
+    for name in declared_functions():
+        assert hasattr(lib2, name), name
+
+
+def test_anatomy_read_refused_in_the_normal_build(lib):
+    buf = (ctypes.c_ulonglong * 3200)()
+    assert lib.attn_anatomy_read(buf, 3200, 0) == -1
+
+
 def test_version_and_status_strings(lib):
     assert lib.attn_version() >= 100
     for code, name in eca.STATUS.items():
