@@ -115,8 +115,13 @@ __host__ inline FastDiv make_fast_div(int d) {
                  l, d};
 }
 
-__device__ __forceinline__ int fast_div(int x, const FastDiv& f) {
+__host__ __device__ __forceinline__ int fast_div(int x, const FastDiv& f) {
+#ifdef __CUDA_ARCH__
   return static_cast<int>(__umulhi(static_cast<uint32_t>(x) << 1, f.m) >> f.l);
+#else  // the same value on the host, for the host-side check of the divisors
+  const unsigned long long hi = (static_cast<unsigned long long>(static_cast<uint32_t>(x) << 1) * f.m) >> 32;
+  return static_cast<int>(static_cast<uint32_t>(hi) >> f.l);
+#endif
 }
 
 // Divisors of the key-halves unit decoding.
