@@ -9,6 +9,7 @@
 #include <functional>
 #include <mutex>
 #include <queue>
+#include <utility>
 #include <vector>
 
 #include "attn.h"
@@ -362,6 +363,27 @@ int predicted_best_splits(int B, int H, int N, int D, int sm_count) {
 
 uint64_t align256(uint64_t x) { return (x + 255) & ~static_cast<uint64_t>(255); }
 
+// Launch with programmatic stream serialisation: the grid may be scheduled before
+// the grid ahead of it on the stream has finished.  Only kernels that call
+// grid_dependency_wait before touching global memory are launched this way.
+// Between two back-to-back attention launches the second then starts as soon as
+// the first completes, instead of after the full stream-ordered launch latency.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), unsigned grid, unsigned block, size_t smem, cudaStream_t stream,
+                       Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(block);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
+
 // Workspace of a key split: fp32 partial outputs [splits, BH, N, D], then fp32
 // partial log-sum-exp [splits, BH, N] at the next 256-byte boundary.
 uint64_t splitkv_bytes(uint64_t bh, uint64_t N, uint64_t D, uint64_t splits, uint64_t* lse_offset) {
@@ -446,17 +468,17 @@ int launch(const void* q, const void* k, const void* v, void* o, float* lse, int
   p.timeout_code = ATTN_ERR_TIMEOUT;
   // Persistent: one CTA per SM (the shared-memory footprint admits only one), never more than the units.
   const unsigned grid = static_cast<unsigned>(p.n_units < st->sm_count ? p.n_units : st->sm_count);
-  if (dynamic) {
-    eca::attn_fwd_kernel<D, BF16, eca::kModeDynamic>
-        <<<grid, eca::kThreads, L::kDynamicBytes, stream>>>(tq, tk, tv, to, p, hd);
-  } else if (halves) {
-    eca::attn_fwd_kernel<D, BF16, eca::kModeHalves>
-        <<<grid, eca::kThreads, L::kDynamicBytes, stream>>>(tq, tk, tv, to, p, hd);
-  } else {
-    eca::attn_fwd_kernel<D, BF16, eca::kModePairs>
-        <<<grid, eca::kThreads, L::kDynamicBytes, stream>>>(tq, tk, tv, to, p, hd);
+  const cudaError_t launched =
+      dynamic ? launch_pdl(eca::attn_fwd_kernel<D, BF16, eca::kModeDynamic>, grid, eca::kThreads, L::kDynamicBytes,
+                           stream, tq, tk, tv, to, p, hd)
+      : halves ? launch_pdl(eca::attn_fwd_kernel<D, BF16, eca::kModeHalves>, grid, eca::kThreads, L::kDynamicBytes,
+                            stream, tq, tk, tv, to, p, hd)
+               : launch_pdl(eca::attn_fwd_kernel<D, BF16, eca::kModePairs>, grid, eca::kThreads, L::kDynamicBytes,
+                            stream, tq, tk, tv, to, p, hd);
+  if (launched != cudaSuccess) {
+    cudaGetLastError();  // clear the error the failed launch recorded
+    return ATTN_ERR_LAUNCH;
   }
-  if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_LAUNCH;
   if (dynamic) {
     const int rc_slot = st->sched_slots.release(stream, slot, capturing);
     if (rc_slot != ATTN_OK) return rc_slot;
@@ -477,8 +499,12 @@ int launch(const void* q, const void* k, const void* v, void* o, float* lse, int
   const long long rows = static_cast<long long>(BH) * N;
   const long long want = (rows + 7) / 8;  // 8 rows (warps) per 256-thread block
   const long long cap = static_cast<long long>(st->sm_count) * 8;
-  eca::splitkv_combine_kernel<D, BF16><<<static_cast<unsigned>(want < cap ? want : cap), 256, 0, stream>>>(c);
-  return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_LAUNCH;
+  if (launch_pdl(eca::splitkv_combine_kernel<D, BF16>, static_cast<unsigned>(want < cap ? want : cap), 256, 0, stream,
+                 c) != cudaSuccess) {
+    cudaGetLastError();
+    return ATTN_ERR_LAUNCH;
+  }
+  return ATTN_OK;
 }
 
 int attn_fwd_impl(bool bf16, const void* q, const void* k, const void* v, void* o, float* lse, int B,
@@ -615,8 +641,11 @@ int launch_decode(const CUtensorMap& tm, eca::DecodeParams& p, const DecodeShape
       }
       st->configured_decode |= bit;
     }
-    kernel<<<grid, eca::kDecThreads, L::kDynamicBytes, stream>>>(tm, p);
-    return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_LAUNCH;
+    if (launch_pdl(kernel, grid, eca::kDecThreads, L::kDynamicBytes, stream, tm, p) != cudaSuccess) {
+      cudaGetLastError();
+      return ATTN_ERR_LAUNCH;
+    }
+    return ATTN_OK;
   };
   const unsigned base = (D == 128 ? 0u : 8u) + (BF16 ? 4u : 0u);
   int rc;
@@ -629,8 +658,12 @@ int launch_decode(const CUtensorMap& tm, eca::DecodeParams& p, const DecodeShape
   if (rc != ATTN_OK || p.part_o == nullptr || p.counters != nullptr) return rc;  // merged in the kernel
   const long long rows = static_cast<long long>(p.B) * p.Hq;
   const long long want = (rows + 7) / 8, cap = static_cast<long long>(st->sm_count) * 8;
-  eca::paged_decode_combine<D, BF16><<<static_cast<unsigned>(want < cap ? want : cap), 256, 0, stream>>>(p);
-  return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_LAUNCH;
+  if (launch_pdl(eca::paged_decode_combine<D, BF16>, static_cast<unsigned>(want < cap ? want : cap), 256, 0, stream,
+                 p) != cudaSuccess) {
+    cudaGetLastError();
+    return ATTN_ERR_LAUNCH;
+  }
+  return ATTN_OK;
 }
 
 int decode_impl(bool bf16, const void* q, const void* cache, const int* block_table, const int* lengths, void* out,
@@ -858,9 +891,12 @@ int attn_paged_append(const void* new_kv, void* cache, const int* block_table, c
   p.bad_index_code = ATTN_ERR_BAD_INDEX;
   const long long rows = static_cast<long long>(B) * 2 * Hkv;
   const long long want = (rows + 7) / 8, cap = static_cast<long long>(st->sm_count) * 8;
-  eca::paged_append_kernel<<<static_cast<unsigned>(want < cap ? want : cap), 256, 0,
-                             reinterpret_cast<cudaStream_t>(stream)>>>(p);
-  return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_LAUNCH;
+  if (launch_pdl(eca::paged_append_kernel, static_cast<unsigned>(want < cap ? want : cap), 256, 0,
+                 reinterpret_cast<cudaStream_t>(stream), p) != cudaSuccess) {
+    cudaGetLastError();
+    return ATTN_ERR_LAUNCH;
+  }
+  return ATTN_OK;
 }
 
 int attn_row_softmax_f32(const float* x, float* y, long long M, int N, attn_stream_t stream) {

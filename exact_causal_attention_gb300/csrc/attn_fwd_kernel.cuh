@@ -345,8 +345,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int warp = __shfl_sync(0xffffffffu, static_cast<int>(threadIdx.x / 32), 0);
   const int lane = threadIdx.x % 32;
 #ifdef ECA_ANATOMY
-  const int an_slot = *reinterpret_cast<volatile int*>(&g_anatomy_launch) & 1;
-  if (threadIdx.x == 0) ECA_STAMP(an_slot, 0);  // entry
+  const unsigned long long an_entry = global_timer_ns();
 #endif
 
   if (threadIdx.x == 0) {
@@ -401,9 +400,18 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_before_sync();
   __syncthreads();
   tc_fence_after_sync();
+  // Set-up done.  The launch is made with programmatic stream serialisation: the
+  // next launch on the stream may now start its own set-up on SMs this grid leaves
+  // free, and nothing below touches global memory before the grid ahead of this
+  // one has finished (every thread waits here, so no bounded wait starts its clock
+  // earlier).
+  grid_launch_dependents();
+  grid_dependency_wait();
   const uint32_t tmem = __shfl_sync(0xffffffffu, *tmem_slot, 0);
 #ifdef ECA_ANATOMY
-  if (threadIdx.x == 0) ECA_STAMP(an_slot, 1);  // set-up done
+  const int an_slot = *reinterpret_cast<volatile int*>(&g_anatomy_launch) & 1;
+  if (threadIdx.x == 0 && blockIdx.x < kAnatomyCtas) g_anatomy[an_slot][blockIdx.x][0] = an_entry;  // entry
+  if (threadIdx.x == 0) ECA_STAMP(an_slot, 1);  // set-up done and the grid ahead finished
   int an_units = 0;
 #endif
   const Watchdog wd{abort_flag, p.status, p.wait_limit_ns, p.timeout_code};

@@ -163,6 +163,10 @@ __global__ void __maxnreg__(128) paged_decode_kernel(const __grid_constant__ CUt
   auto full = [&](int s) -> uint32_t { return sbase + L::kBarOff + 8u * static_cast<uint32_t>(s); };
   auto empty = [&](int s) -> uint32_t { return sbase + L::kBarOff + 8u * static_cast<uint32_t>(kDecStages + s); };
 
+  // Launched with programmatic serialisation: the next launch may be scheduled at
+  // once, and no global memory is read before the grid ahead of this one finished.
+  grid_launch_dependents();
+  grid_dependency_wait();
   const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
   // unit: (b, kv head, head chunk, segment), segment fastest
   int u = blockIdx.x;
@@ -532,6 +536,7 @@ __global__ void __maxnreg__(128) paged_decode_kernel(const __grid_constant__ CUt
 // first logical page is below the request's page count.
 template <int D, bool BF16>
 __global__ void __launch_bounds__(256) paged_decode_combine(const DecodeParams p) {
+  grid_dependency_wait();  // the partials come from the decode grid just ahead
   const int lane = threadIdx.x % 32;
   const long long rows = static_cast<long long>(p.B) * p.Hq;
   for (long long r = static_cast<long long>(blockIdx.x) * 8 + threadIdx.x / 32; r < rows; r += gridDim.x * 8LL) {
@@ -580,6 +585,8 @@ struct AppendParams {
 };
 
 __global__ void __launch_bounds__(256) paged_append_kernel(const AppendParams p) {
+  grid_launch_dependents();
+  grid_dependency_wait();
   const long long rows = static_cast<long long>(p.B) * 2 * p.Hkv;
   const int lane = threadIdx.x % 32;
   const int vecs = p.D / 8;  // 16-byte vectors per row

@@ -60,6 +60,18 @@ __device__ __forceinline__ uint64_t global_timer_ns() {
   return t;
 }
 
+// Programmatic dependent launch.  A grid launched with programmatic stream
+// serialisation may start while the grid ahead of it on the stream still runs;
+// `grid_dependency_wait` returns once that grid has completed and its memory
+// writes are visible (at once for a grid launched without the attribute), so no
+// global memory may be touched before it.  `grid_launch_dependents` lets the next
+// such grid be launched once every CTA of this one has issued it or exited.
+__device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+__device__ __forceinline__ void grid_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // Every wait in the kernels is bounded.  When a wait gives up it raises the
 // block's shared abort flag (so the other roles stop waiting at once) and
 // records `timeout_code` in the device status word; the caller then leaves its

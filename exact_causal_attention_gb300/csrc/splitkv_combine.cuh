@@ -28,6 +28,9 @@ struct CombineParams {
 template <int D, bool BF16>
 __global__ void __launch_bounds__(256) splitkv_combine_kernel(const CombineParams p) {
   constexpr int kPer = D / 32;  // columns per lane: 4 (D = 128) or 2 (D = 64)
+  // Launched with programmatic serialisation right behind the attention kernel
+  // that writes the partials: read none before that grid has finished.
+  grid_dependency_wait();
   const int lane = threadIdx.x % 32;
   const long long rows = static_cast<long long>(p.BH) * p.N;
   const long long warps = static_cast<long long>(gridDim.x) * (blockDim.x / 32);
