@@ -347,9 +347,16 @@ def bench_sweep_point(eca, inputs, dev, stream, flush, n):
     torch.cuda.synchronize(dev)
     graph_ms = a.elapsed_time(b) / 20
     tf = lambda ms: round(sw.flops / (ms * 1e-3) / 1e12, 1)  # noqa: E731
-    return {"workload": sw.name, "single_ms": round(single_ms, 4), "single_tflops": tf(single_ms),
-            "eager_ms": round(eager_ms, 4), "eager_tflops": tf(eager_ms), "graph_ms": round(graph_ms, 4),
-            "graph_tflops": tf(graph_ms)}
+    return {"workload": sw.name, "launch_order": launch_order(), "single_ms": round(single_ms, 4),
+            "single_tflops": tf(single_ms), "eager_ms": round(eager_ms, 4), "eager_tflops": tf(eager_ms),
+            "graph_ms": round(graph_ms, 4), "graph_tflops": tf(graph_ms)}
+
+
+def launch_order() -> str:
+    """How the library launches its kernels in this process: programmatic dependent launch
+    (the default), or plain stream order with ECA_PDL=0."""
+    return "stream" if os.environ.get("ECA_PDL") == "0" else "programmatic"
+
 
 
 ANATOMY_POINTS = ("entry", "setup_done", "first_k_load_issued", "first_qk_issued", "first_s_ready",
@@ -774,6 +781,7 @@ def bench_ours(args, w):
                 "schedule": "pinned host buffers; two device buffer sets; upload, kernel and download on three "
                             "streams, the upload of step i + 1 and download of step i - 1 overlapping kernel i"},
         "gpu_launches": args.steps,
+        "launch_order": launch_order(),
         "clocks": clocks,
         "sweep": sweep,
         "sweep_graph": sweep_graph,
@@ -789,6 +797,20 @@ def bench_ours(args, w):
         "vs_baseline_ref": "page's PyTorch SDPA FLASH on RTX 3060 Laptop (SM86): 25.854 ms",
     }
     print(json.dumps(line), flush=True)
+
+
+def bench_launch_cost():
+    """Builds and runs csrc/launch_cost_probe.cu: microseconds per launch of empty one-CTA-per-SM
+    kernels, 200 back to back, for the launch boundaries that set the floor of a short call."""
+    from exact_causal_attention_gb300 import build as cuda_build
+
+    src = os.path.join(cuda_build.CSRC, "launch_cost_probe.cu")
+    exe = os.path.join(cuda_build.BUILD_DIR, "launch_cost_probe")
+    os.makedirs(cuda_build.BUILD_DIR, exist_ok=True)
+    if not os.path.exists(exe) or os.path.getmtime(exe) < os.path.getmtime(src):
+        subprocess.run([cuda_build._nvcc(), *cuda_build.ARCH_FLAGS, "-O2", "-std=c++17", "-o", exe, src], check=True)
+    out = subprocess.run([exe], check=True, capture_output=True, text=True, timeout=300).stdout
+    return json.loads(out)
 
 
 def main():
@@ -812,8 +834,14 @@ def main():
                     help="per-CTA milestones of two back-to-back launches of the sweep workload at N (anatomy build)")
     ap.add_argument("--sweep-only", type=int, metavar="N",
                     help="only the sweep workload at this N (causal B=1 H=32 D=128 fp16), eager and from a graph")
+    ap.add_argument("--launch-cost", action="store_true",
+                    help="time per launch of empty kernels (with and without global stores and tensor memory) in "
+                         "stream order, with programmatic dependent launch and from a CUDA graph")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
+    if args.launch_cost:
+        print(json.dumps({"launch_cost": bench_launch_cost()}), flush=True)
+        return
     from exact_causal_attention_gb300 import inputs
 
     w = inputs.WORKLOADS[WORKLOAD]

@@ -5,6 +5,7 @@
 
 #include <cmath>
 #include <cstdint>
+#include <cstdlib>
 #include <cstring>
 #include <functional>
 #include <mutex>
@@ -368,6 +369,16 @@ uint64_t align256(uint64_t x) { return (x + 255) & ~static_cast<uint64_t>(255); 
 // grid_dependency_wait before touching global memory are launched this way.
 // Between two back-to-back attention launches the second then starts as soon as
 // the first completes, instead of after the full stream-ordered launch latency.
+// ECA_PDL=0 in the environment (read once per process) launches in plain stream
+// order instead, with the same results; it exists to measure the difference.
+bool programmatic_launch_enabled() {
+  static const bool enabled = [] {
+    const char* v = std::getenv("ECA_PDL");
+    return !(v != nullptr && v[0] == '0' && v[1] == '\0');
+  }();
+  return enabled;
+}
+
 template <typename... KArgs, typename... Args>
 cudaError_t launch_pdl(void (*kernel)(KArgs...), unsigned grid, unsigned block, size_t smem, cudaStream_t stream,
                        Args&&... args) {
@@ -380,7 +391,7 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), unsigned grid, unsigned block, 
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = programmatic_launch_enabled() ? 1 : 0;
   return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
 }
 

@@ -380,6 +380,21 @@ __global__ void __launch_bounds__(kThreads, 1)
     tmem_alloc(smem_u32(tmem_slot), kTmemCols);
     tmem_relinquish();
   }
+  // Work that reads only the launch's own parameters, done before the wait for the
+  // grid ahead: the tensor maps into the TMA unit's descriptor cache, and the
+  // parameters the unit decoding reads into the constant cache (a decode of unit
+  // 0 whose result goes to a queue entry that is written again before it is read).
+  if (warp == 8 && lane == 0) {
+    tma_prefetch_map(&tm_k);
+    tma_prefetch_map(&tm_v);
+  } else if (warp == 11 && lane == 0) {
+    tma_prefetch_map(&tm_q);
+    tma_prefetch_map(&tm_o);  // for the epilogue's first store, well before it
+  } else if (warp == 10 && lane == 0) {
+    Unit u;
+    unit_from<kHalves>(0, p, hd, u);
+    unit_queue[kUnitQueue - 1] = u.bh + u.kvh + u.tile0 + u.kv1 + u.n_max + p.N + p.causal;
+  }
   // The k-th unit of this CTA under the fixed assignment: unit k G + c of wave k,
   // the waves dealt to the CTAs in alternating directions; -1 past the last.
   auto fixed_unit = [&](int k) -> int {
@@ -447,8 +462,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 8) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
-      tma_prefetch_map(&tm_k);
-      tma_prefetch_map(&tm_v);
       const uint64_t pol_kv = policy_evict_last();
       int it = 0;      // ring items issued
       int pushed = 0;  // unit queue entries written
@@ -534,8 +547,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     // unit is done, so a tile that finishes first starts its next unit without
     // waiting for the other.
     if (lane == 0) {
-      tma_prefetch_map(&tm_q);
-      tma_prefetch_map(&tm_o);  // for the epilogue's first store, well before it
       const uint64_t pol_q = policy_evict_first();
       int loads[2] = {0, 0};
       bool ok = true;

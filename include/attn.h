@@ -34,6 +34,18 @@
  * caller's next synchronisation.  Calls may come from several host threads (the
  * host side serialises them on one lock).
  *
+ * Launch order: kernels are launched with programmatic stream serialisation
+ * (programmatic dependent launch).  Stream order is kept for memory: a kernel's
+ * CTAs may be scheduled while the work ahead of it on the stream still runs, but
+ * they touch no global memory before it has completed.  The attention and
+ * decode kernels also let the next such launch on the stream be scheduled once
+ * their set-up is done, so back-to-back calls lose less time between launches.
+ * A kernel of the caller's that is launched with the same attribute right after
+ * one of these calls must likewise wait for the grid ahead of it
+ * (griddepcontrol.wait / cudaGridDependencySynchronize) before reading its
+ * outputs.  ECA_PDL=0 in the environment, read once per process, launches in
+ * plain stream order instead.
+ *
  * Concurrency limits: launches whose key/value tensors together exceed 64 MiB
  * hand out their work from a device counter, taken from a pool of 64 per device
  * in turn; the split paged decode's in-kernel merge uses counters from a pool of

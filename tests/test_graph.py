@@ -94,3 +94,45 @@ def test_tensor_map_cache_follows_shape_changes(cuda_lib):
         ro, rl = oracle_full(hq, hk, hv, dtype, True, 1.0 / D ** 0.5)
         compare(o.double().cpu().numpy(), lse.double().cpu().numpy(), ro, rl, dtype,
                 p_rounding_term(hq, hk, hv, dtype, True, 1.0 / D ** 0.5))
+
+
+def test_stream_order_launch_gives_the_same_results(cuda_lib, tmp_path):
+    """The library launches with programmatic dependent launch by default; ECA_PDL=0
+    launches in plain stream order.  Both orders must give bit-identical results for
+    back-to-back calls of every unit mode (a second process, since the switch is read
+    once per process)."""
+    import os
+    import subprocess
+    import sys
+
+    eca = cuda_lib
+    shapes = [(1, 32, 512, 128), (1, 40, 8192, 128), (2, 6, 1000, 64)]
+    script = r'''
+import sys, numpy as np, torch
+sys.path.insert(0, sys.argv[1])
+import exact_causal_attention_gb300 as eca
+from exact_causal_attention_gb300 import inputs
+for i, (B, H, N, D) in enumerate(%r):
+    q, k, v = (x.cuda() for x in inputs.make_qkv(B, H, N, D, "fp16", seed=700 + N))
+    o = torch.empty_like(q)
+    lse = torch.empty(B, H, N, device="cuda")
+    for _ in range(3):
+        eca.attn_fwd_into(q, k, v, o, lse, causal=True)
+    torch.cuda.synchronize()
+    assert eca.device_status() == 0
+    np.save(sys.argv[2] + f"/o{i}.npy", o.view(torch.int16).cpu().numpy())
+    np.save(sys.argv[2] + f"/l{i}.npy", lse.cpu().numpy())
+''' % (shapes,)
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    env = dict(os.environ, ECA_PDL="0")
+    subprocess.run([sys.executable, "-c", script, root, str(tmp_path)], env=env, check=True, timeout=600)
+    for i, (B, H, N, D) in enumerate(shapes):
+        q, k, v = (x.cuda() for x in inputs.make_qkv(B, H, N, D, "fp16", seed=700 + N))
+        o = torch.empty_like(q)
+        lse = torch.empty(B, H, N, device="cuda")
+        for _ in range(3):
+            eca.attn_fwd_into(q, k, v, o, lse, causal=True)
+        torch.cuda.synchronize()
+        assert eca.device_status() == 0
+        assert np.array_equal(o.view(torch.int16).cpu().numpy(), np.load(tmp_path / f"o{i}.npy")), (B, H, N, D)
+        assert np.array_equal(lse.cpu().numpy(), np.load(tmp_path / f"l{i}.npy")), (B, H, N, D)
