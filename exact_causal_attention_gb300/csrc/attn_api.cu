@@ -419,6 +419,17 @@ int launch(const void* q, const void* k, const void* v, void* o, float* lse, int
                              cudaFuncAttributeMaxDynamicSharedMemorySize, L::kDynamicBytes) != cudaSuccess) {
       return ATTN_ERR_CUDA;
     }
+    // The fixed-assignment instances move registers between their warpgroups
+    // (setmaxnreg); the counts they ask for must fit in what each block is launched
+    // with, or a warpgroup would wait for registers forever.  Refuse a build where
+    // they do not.
+    const void* instances[2] = {reinterpret_cast<const void*>(eca::attn_fwd_kernel<D, BF16, eca::kModePairs>),
+                                reinterpret_cast<const void*>(eca::attn_fwd_kernel<D, BF16, eca::kModeHalves>)};
+    for (const void* fn : instances) {
+      cudaFuncAttributes fa;
+      if (cudaFuncGetAttributes(&fa, fn) != cudaSuccess) return ATTN_ERR_CUDA;
+      if (fa.numRegs * eca::kThreads < 256 * eca::kRegsSoftmax + 128 * eca::kRegsControl) return ATTN_ERR_LAUNCH;
+    }
     st->configured |= 1u << ((D == 128 ? 2 : 0) + (BF16 ? 1 : 0));
   }
   CUtensorMap tq, tk, tv, to;

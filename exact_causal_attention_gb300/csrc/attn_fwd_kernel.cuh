@@ -89,6 +89,14 @@ constexpr float kGuessRef = 4.0f;       // first reference of a unit (scores tim
 constexpr float kMinGuessSum = 1.0f;    // a guess is kept only if the first tile's sum of p reaches this
 constexpr int kUnitQueue = 4;           // depth of the shared-memory queue of unit indices
 constexpr int kUnitReaders = 11;        // warps that read each queue entry: 8 softmax, 2 issuers, Q loader
+// Per-thread registers after the split (setmaxnreg): 256 softmax threads and 128
+// control threads within what the block is launched with, kLaunchRegs per thread
+// (the host checks the compiled count before the first launch).
+constexpr int kLaunchRegs = 168;
+constexpr int kRegsSoftmax = 208;
+constexpr int kRegsControl = 80;
+static_assert(256 * kRegsSoftmax + 128 * kRegsControl <= kThreads * kLaunchRegs,
+              "the register split must fit in the registers the block is launched with");
 
 // How a launch forms and assigns its work units (the kernel's third template argument).
 constexpr int kModePairs = 0;    // two query tiles (or head pairs) per unit, fixed zig-zag assignment
@@ -331,6 +339,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   using L = FwdSmem<D>;
   constexpr bool kDynamic = kMode == kModeDynamic;
   constexpr bool kHalves = kMode == kModeHalves;
+  // The fixed-assignment instances move registers from the control warpgroup to the
+  // softmax warpgroups (which then read O for the epilogue with fewer waits); the
+  // dynamic instance measured about 1% slower at N = 8192 with the same split and
+  // keeps one count for all warps.
+  constexpr bool kSplitRegs = !kDynamic;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_base = smem_u32(smem_raw);
   const uint32_t sbase = (raw_base + 1023u) & ~1023u;
@@ -459,247 +472,252 @@ __global__ void __launch_bounds__(kThreads, 1)
     return 1;
   };
 
-  if (warp == 8) {
-    // ------------------------------------------------------------ TMA producer
-    if (lane == 0) {
-      const uint64_t pol_kv = policy_evict_last();
-      int it = 0;      // ring items issued
-      int pushed = 0;  // unit queue entries written
-      auto push_unit = [&](int l) -> bool {
-        const int q = pushed % kUnitQueue;
-        if (!wd.wait(bar(L::kBarUnitFree + q), parity(pushed / kUnitQueue) ^ 1u)) return false;
-        unit_queue[q] = l;
-        mbar_arrive(bar(L::kBarUnitFull + q));
-        ++pushed;
-        return true;
-      };
-      // Under dynamic assignment this warp takes the CTA's units from the launch's
-      // counter (skipping key segments past a pair's last key tile, which have no
-      // work) when it is about to load their items, and queues them for the other
-      // warps; so a unit goes to the CTA that is free first.
-      auto take_unit = [&]() -> int {
-        while (true) {
-          const int l = atomicAdd(p.sched, 1);
-          if (l >= p.n_units) return -1;
-          Unit u;
-          unit_from<kHalves>(l, p, hd, u);
-          if (u.n_max > 0) return l;
+  if (warp >= 8) {
+    // Control warpgroup (producer, issuers, Q loader): gives registers to the softmax warps.
+    if constexpr (kSplitRegs) setmaxnreg_dec<kRegsControl>();
+    if (warp == 8) {
+      // ------------------------------------------------------------ TMA producer
+      if (lane == 0) {
+        const uint64_t pol_kv = policy_evict_last();
+        int it = 0;      // ring items issued
+        int pushed = 0;  // unit queue entries written
+        auto push_unit = [&](int l) -> bool {
+          const int q = pushed % kUnitQueue;
+          if (!wd.wait(bar(L::kBarUnitFree + q), parity(pushed / kUnitQueue) ^ 1u)) return false;
+          unit_queue[q] = l;
+          mbar_arrive(bar(L::kBarUnitFull + q));
+          ++pushed;
+          return true;
+        };
+        // Under dynamic assignment this warp takes the CTA's units from the launch's
+        // counter (skipping key segments past a pair's last key tile, which have no
+        // work) when it is about to load their items, and queues them for the other
+        // warps; so a unit goes to the CTA that is free first.
+        auto take_unit = [&]() -> int {
+          while (true) {
+            const int l = atomicAdd(p.sched, 1);
+            if (l >= p.n_units) return -1;
+            Unit u;
+            unit_from<kHalves>(l, p, hd, u);
+            if (u.n_max > 0) return l;
+          }
+        };
+        bool ok = true;
+        Unit w;
+        while (ok) {
+          if (kDynamic) {
+            const int l = take_unit();
+            if (!push_unit(l) || l < 0) break;
+            unit_from<kHalves>(l, p, hd, w);
+          } else if (next_unit(w, false) != 1) {
+            break;
+          }
+          // Items i = 0 .. n_max: {V_(b+i-1) if 0 < i <= n, K_(b+i) if i < n}, with
+          // b = kv0 and n = n_max shared by both slots; with key halves, one item of
+          // each slot per i (slot 0 first), with that slot's b and n.
+          const int per_i = kHalves ? 2 : 1;
+          for (int i = 0; ok && i <= w.n_max; ++i) {
+            for (int h = 0; h < per_i; ++h) {
+              const int b = h ? w.kv1 : w.kv0;
+              const int n = kHalves ? (h ? w.n_kv1 : w.n_kv0) : w.n_max;
+              const int slot = it % L::kStages;
+              if (!wd.wait(bar(L::kBarEmpty + slot), parity(it / L::kStages) ^ 1u)) {
+                ok = false;
+                break;
+              }
+              const uint32_t stage = sbase + L::kRingOff + slot * L::kStageBytes;
+              // The V and K parts complete on barriers of their own, so the P V MMAs can
+              // start before K has landed; a missing part is a plain arrival.
+              const uint32_t full_v = bar(L::kBarFull + slot), full_k = bar(L::kBarFullK + slot);
+              if (i > 0 && i <= n) {
+                mbar_arrive_expect_tx(full_v, L::kTileBytes);
+                for (int s = 0; s < L::kSub; ++s)
+                  tma_load_3d(stage + s * kSubTileBytes, &tm_v, full_v, 64 * s, (b + i - 1) * kBlockN, w.kvh, pol_kv);
+              } else {
+                mbar_arrive(full_v);
+              }
+              if (i < n) {
+                mbar_arrive_expect_tx(full_k, L::kTileBytes);
+                for (int s = 0; s < L::kSub; ++s)
+                  tma_load_3d(stage + L::kTileBytes + s * kSubTileBytes, &tm_k, full_k, 64 * s, (b + i) * kBlockN,
+                              w.kvh, pol_kv);
+              } else {
+                mbar_arrive(full_k);
+              }
+  #ifdef ECA_ANATOMY
+              if (it == 0) ECA_STAMP(an_slot, 2);  // first K load issued
+  #endif
+              ++it;
+            }
+          }
         }
-      };
-      bool ok = true;
-      Unit w;
-      while (ok) {
-        if (kDynamic) {
-          const int l = take_unit();
-          if (!push_unit(l) || l < 0) break;
-          unit_from<kHalves>(l, p, hd, w);
-        } else if (next_unit(w, false) != 1) {
-          break;
+        // Let every copy this thread started land before the block can exit.
+        for (int x = (it > L::kStages ? it - L::kStages : 0); x < it; ++x) {
+          wd.drain(bar(L::kBarFull + x % L::kStages), parity(x / L::kStages));
+          wd.drain(bar(L::kBarFullK + x % L::kStages), parity(x / L::kStages));
         }
-        // Items i = 0 .. n_max: {V_(b+i-1) if 0 < i <= n, K_(b+i) if i < n}, with
-        // b = kv0 and n = n_max shared by both slots; with key halves, one item of
-        // each slot per i (slot 0 first), with that slot's b and n.
-        const int per_i = kHalves ? 2 : 1;
-        for (int i = 0; ok && i <= w.n_max; ++i) {
-          for (int h = 0; h < per_i; ++h) {
-            const int b = h ? w.kv1 : w.kv0;
-            const int n = kHalves ? (h ? w.n_kv1 : w.n_kv0) : w.n_max;
-            const int slot = it % L::kStages;
-            if (!wd.wait(bar(L::kBarEmpty + slot), parity(it / L::kStages) ^ 1u)) {
+      }
+    } else if (warp == 11) {
+      // ------------------------------------------------------ Q loader, per query tile
+      // Each tile's Q buffer is refilled as soon as that tile's last Q K^T of the
+      // unit is done, so a tile that finishes first starts its next unit without
+      // waiting for the other.
+      if (lane == 0) {
+        const uint64_t pol_q = policy_evict_first();
+        int loads[2] = {0, 0};
+        bool ok = true;
+        Unit w;
+        while (ok && next_unit(w, false) == 1) {
+          for (int t = 0; t < 2; ++t) {
+            if ((t ? w.n_kv1 : w.n_kv0) == 0) continue;
+            if (loads[t] > 0 && !wd.wait(bar(L::kBarQFree + t), parity(loads[t] - 1))) {
               ok = false;
               break;
             }
-            const uint32_t stage = sbase + L::kRingOff + slot * L::kStageBytes;
-            // The V and K parts complete on barriers of their own, so the P V MMAs can
-            // start before K has landed; a missing part is a plain arrival.
-            const uint32_t full_v = bar(L::kBarFull + slot), full_k = bar(L::kBarFullK + slot);
-            if (i > 0 && i <= n) {
-              mbar_arrive_expect_tx(full_v, L::kTileBytes);
-              for (int s = 0; s < L::kSub; ++s)
-                tma_load_3d(stage + s * kSubTileBytes, &tm_v, full_v, 64 * s, (b + i - 1) * kBlockN, w.kvh, pol_kv);
-            } else {
-              mbar_arrive(full_v);
+            mbar_arrive_expect_tx(bar(L::kBarQFull + t), L::kTileBytes);
+            for (int s = 0; s < L::kSub; ++s) {
+              tma_load_3d(sbase + L::kQOff + t * L::kTileBytes + s * kSubTileBytes, &tm_q, bar(L::kBarQFull + t),
+                          64 * s, (w.tile0 + ((p.head_pair || kHalves) ? 0 : t)) * kBlockM,
+                          w.bh + (p.head_pair ? t : 0), pol_q);
             }
-            if (i < n) {
-              mbar_arrive_expect_tx(full_k, L::kTileBytes);
-              for (int s = 0; s < L::kSub; ++s)
-                tma_load_3d(stage + L::kTileBytes + s * kSubTileBytes, &tm_k, full_k, 64 * s, (b + i) * kBlockN,
-                            w.kvh, pol_kv);
-            } else {
-              mbar_arrive(full_k);
-            }
-#ifdef ECA_ANATOMY
-            if (it == 0) ECA_STAMP(an_slot, 2);  // first K load issued
-#endif
-            ++it;
+            ++loads[t];
           }
         }
-      }
-      // Let every copy this thread started land before the block can exit.
-      for (int x = (it > L::kStages ? it - L::kStages : 0); x < it; ++x) {
-        wd.drain(bar(L::kBarFull + x % L::kStages), parity(x / L::kStages));
-        wd.drain(bar(L::kBarFullK + x % L::kStages), parity(x / L::kStages));
-      }
-    }
-  } else if (warp == 11) {
-    // ------------------------------------------------------ Q loader, per query tile
-    // Each tile's Q buffer is refilled as soon as that tile's last Q K^T of the
-    // unit is done, so a tile that finishes first starts its next unit without
-    // waiting for the other.
-    if (lane == 0) {
-      const uint64_t pol_q = policy_evict_first();
-      int loads[2] = {0, 0};
-      bool ok = true;
-      Unit w;
-      while (ok && next_unit(w, false) == 1) {
+        // Let every copy this thread started land before the block can exit.
         for (int t = 0; t < 2; ++t) {
-          if ((t ? w.n_kv1 : w.n_kv0) == 0) continue;
-          if (loads[t] > 0 && !wd.wait(bar(L::kBarQFree + t), parity(loads[t] - 1))) {
+          if (loads[t] > 0) wd.drain(bar(L::kBarQFull + t), parity(loads[t] - 1));
+        }
+      }
+    } else {
+      // ------------------------------------------------- MMA issuer of query tile t
+      // The whole warp runs this loop: waits are taken by every lane and decided by
+      // a vote, descriptors are warp-uniform, and one elected lane issues each MMA
+      // and commit.
+      {
+        const int t = warp - 9;
+        const uint32_t s_tmem = tmem + 128u * t;                           // S_t, and P_t over it
+        const uint32_t o_tmem = tmem + 256u + static_cast<uint32_t>(D) * t;  // O_t
+        const uint64_t q_desc = smem_desc_sw128(sbase + L::kQOff + t * L::kTileBytes, 16, 1024);
+        const uint64_t ring_v_desc = smem_desc_sw128(sbase + L::kRingOff, kSubTileBytes, 1024);
+        const uint64_t ring_k_desc = smem_desc_sw128(sbase + L::kRingOff + L::kTileBytes, 16, 1024);
+        auto stage_off = [&](int item) {  // stage offset in the descriptors' >>4 address field
+          return static_cast<uint64_t>((item % L::kStages) * (L::kStageBytes >> 4));
+        };
+        auto warp_wait = [&](uint32_t b, uint32_t ph) -> bool {
+          return __all_sync(0xffffffffu, wd.wait(b, ph)) != 0;
+        };
+        // The issuers take turns, one per ring item each, tile 0 first: a turn's
+        // MMAs stay contiguous in the pipe, so one tile's MMAs run while the other
+        // tile's softmax works.
+        int turns = 0;
+        auto take_turn = [&]() -> bool { return warp_wait(bar(L::kBarTurn + t), parity(turns++)); };
+        auto pass_turn = [&]() {
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bar(L::kBarTurn + (1 - t)));
+        };
+        int it = 0;       // ring items of the units done so far (both slots')
+        int p_waits = 0;  // P_t handshakes consumed
+        int used = 0;     // earlier units in which tile t existed (its O_t is read by an epilogue)
+        int q_loads = 0;  // Q loads of tile t consumed
+        bool ok = true;
+        Unit w;
+        while (ok) {
+          const int got = next_unit(w, true);
+          if (got != 1) {
+            ok = got == 0;
+            break;
+          }
+          const int n_kv = t ? w.n_kv1 : w.n_kv0;
+          // Ring item of this issuer's step i: every item of the unit (both slots use
+          // it), or with key halves every other one, starting with its own slot.
+          const int base = it;
+          auto item = [&](int i) { return kHalves ? base + 2 * i + t : base + i; };
+          int x = item(0);
+          // Item 0 (K_0).  Every item this issuer consumes is waited for and released
+          // whether or not its tile uses it, so the ring's phases stay aligned (two
+          // arrivals per item, or one with key halves).
+          if ((n_kv > 0 && !warp_wait(bar(L::kBarQFull + t), parity(q_loads++))) ||
+              !warp_wait(bar(L::kBarFull + x % L::kStages), parity(x / L::kStages)) ||
+              !warp_wait(bar(L::kBarFullK + x % L::kStages), parity(x / L::kStages))) {
             ok = false;
             break;
           }
-          mbar_arrive_expect_tx(bar(L::kBarQFull + t), L::kTileBytes);
-          for (int s = 0; s < L::kSub; ++s) {
-            tma_load_3d(sbase + L::kQOff + t * L::kTileBytes + s * kSubTileBytes, &tm_q, bar(L::kBarQFull + t),
-                        64 * s, (w.tile0 + ((p.head_pair || kHalves) ? 0 : t)) * kBlockM,
-                        w.bh + (p.head_pair ? t : 0), pol_q);
-          }
-          ++loads[t];
-        }
-      }
-      // Let every copy this thread started land before the block can exit.
-      for (int t = 0; t < 2; ++t) {
-        if (loads[t] > 0) wd.drain(bar(L::kBarQFull + t), parity(loads[t] - 1));
-      }
-    }
-  } else if (warp >= 9) {
-    // ------------------------------------------------- MMA issuer of query tile t
-    // The whole warp runs this loop: waits are taken by every lane and decided by
-    // a vote, descriptors are warp-uniform, and one elected lane issues each MMA
-    // and commit.
-    {
-      const int t = warp - 9;
-      const uint32_t s_tmem = tmem + 128u * t;                           // S_t, and P_t over it
-      const uint32_t o_tmem = tmem + 256u + static_cast<uint32_t>(D) * t;  // O_t
-      const uint64_t q_desc = smem_desc_sw128(sbase + L::kQOff + t * L::kTileBytes, 16, 1024);
-      const uint64_t ring_v_desc = smem_desc_sw128(sbase + L::kRingOff, kSubTileBytes, 1024);
-      const uint64_t ring_k_desc = smem_desc_sw128(sbase + L::kRingOff + L::kTileBytes, 16, 1024);
-      auto stage_off = [&](int item) {  // stage offset in the descriptors' >>4 address field
-        return static_cast<uint64_t>((item % L::kStages) * (L::kStageBytes >> 4));
-      };
-      auto warp_wait = [&](uint32_t b, uint32_t ph) -> bool {
-        return __all_sync(0xffffffffu, wd.wait(b, ph)) != 0;
-      };
-      // The issuers take turns, one per ring item each, tile 0 first: a turn's
-      // MMAs stay contiguous in the pipe, so one tile's MMAs run while the other
-      // tile's softmax works.
-      int turns = 0;
-      auto take_turn = [&]() -> bool { return warp_wait(bar(L::kBarTurn + t), parity(turns++)); };
-      auto pass_turn = [&]() {
-        __syncwarp();
-        if (lane == 0) mbar_arrive(bar(L::kBarTurn + (1 - t)));
-      };
-      int it = 0;       // ring items of the units done so far (both slots')
-      int p_waits = 0;  // P_t handshakes consumed
-      int used = 0;     // earlier units in which tile t existed (its O_t is read by an epilogue)
-      int q_loads = 0;  // Q loads of tile t consumed
-      bool ok = true;
-      Unit w;
-      while (ok) {
-        const int got = next_unit(w, true);
-        if (got != 1) {
-          ok = got == 0;
-          break;
-        }
-        const int n_kv = t ? w.n_kv1 : w.n_kv0;
-        // Ring item of this issuer's step i: every item of the unit (both slots use
-        // it), or with key halves every other one, starting with its own slot.
-        const int base = it;
-        auto item = [&](int i) { return kHalves ? base + 2 * i + t : base + i; };
-        int x = item(0);
-        // Item 0 (K_0).  Every item this issuer consumes is waited for and released
-        // whether or not its tile uses it, so the ring's phases stay aligned (two
-        // arrivals per item, or one with key halves).
-        if ((n_kv > 0 && !warp_wait(bar(L::kBarQFull + t), parity(q_loads++))) ||
-            !warp_wait(bar(L::kBarFull + x % L::kStages), parity(x / L::kStages)) ||
-            !warp_wait(bar(L::kBarFullK + x % L::kStages), parity(x / L::kStages))) {
-          ok = false;
-          break;
-        }
-        tc_fence_after_sync();
-        if (!take_turn()) {
-          ok = false;
-          break;
-        }
-        if (n_kv > 0) issue_qk<D, BF16>(s_tmem, q_desc, ring_k_desc + stage_off(x));
-#ifdef ECA_ANATOMY
-        if (t == 0 && base == 0 && lane == 0) ECA_STAMP(an_slot, 3);  // first Q K^T issued
-        if (t == 0 && lane == 0) ++an_units;
-#endif
-        pass_turn();
-        if (n_kv > 0) tc_commit_warp(bar(L::kBarS + t));
-        if (n_kv == 1) tc_commit_warp(bar(L::kBarQFree + t));  // this tile's Q K^T are all issued
-        tc_commit_warp(bar(L::kBarEmpty + x % L::kStages));
-        for (int j = 0; j < w.n_max; ++j) {
-          x = item(j + 1);
-          if (!warp_wait(bar(L::kBarFull + x % L::kStages), parity(x / L::kStages))) {
-            ok = false;
-            break;
-          }
-          if (j < n_kv) {
-            // O_t is overwritten by the first P V of a unit: the previous epilogue must have read it.
-            if (j == 0 && used > 0 && !warp_wait(bar(L::kBarOFree + t), parity(used - 1))) {
-              ok = false;
-              break;
-            }
-            if (!warp_wait(bar(L::kBarPa + t), parity(p_waits))) {
-              ok = false;
-              break;
-            }
-            ++p_waits;
-            tc_fence_after_sync();
-          }
+          tc_fence_after_sync();
           if (!take_turn()) {
             ok = false;
             break;
           }
-          if (j < n_kv) {
-            // P V of keys 0-63 goes in while the softmax still works on keys 64-127.
-            issue_pv<D, BF16>(o_tmem, s_tmem, ring_v_desc + stage_off(x), j > 0, 0, 4);
-            if (!warp_wait(bar(L::kBarPb + t), parity(p_waits - 1))) {
+          if (n_kv > 0) issue_qk<D, BF16>(s_tmem, q_desc, ring_k_desc + stage_off(x));
+  #ifdef ECA_ANATOMY
+          if (t == 0 && base == 0 && lane == 0) ECA_STAMP(an_slot, 3);  // first Q K^T issued
+          if (t == 0 && lane == 0) ++an_units;
+  #endif
+          pass_turn();
+          if (n_kv > 0) tc_commit_warp(bar(L::kBarS + t));
+          if (n_kv == 1) tc_commit_warp(bar(L::kBarQFree + t));  // this tile's Q K^T are all issued
+          tc_commit_warp(bar(L::kBarEmpty + x % L::kStages));
+          for (int j = 0; j < w.n_max; ++j) {
+            x = item(j + 1);
+            if (!warp_wait(bar(L::kBarFull + x % L::kStages), parity(x / L::kStages))) {
               ok = false;
               break;
             }
-            tc_fence_after_sync();
-            issue_pv<D, BF16>(o_tmem, s_tmem, ring_v_desc + stage_off(x), true, 4, 8);
-          }
-          if (!warp_wait(bar(L::kBarFullK + x % L::kStages), parity(x / L::kStages))) {
-            ok = false;
-            break;
-          }
-          if (j + 1 < n_kv) {
-            tc_fence_after_sync();
-            issue_qk<D, BF16>(s_tmem, q_desc, ring_k_desc + stage_off(x));
-          }
-          pass_turn();
-          if (j < n_kv) {
-            if (j + 1 < n_kv) {
-              tc_commit_warp(bar(L::kBarS + t));
-              if (j + 2 == n_kv) tc_commit_warp(bar(L::kBarQFree + t));
-            } else {
-              tc_commit_warp(bar(L::kBarO + t));
+            if (j < n_kv) {
+              // O_t is overwritten by the first P V of a unit: the previous epilogue must have read it.
+              if (j == 0 && used > 0 && !warp_wait(bar(L::kBarOFree + t), parity(used - 1))) {
+                ok = false;
+                break;
+              }
+              if (!warp_wait(bar(L::kBarPa + t), parity(p_waits))) {
+                ok = false;
+                break;
+              }
+              ++p_waits;
+              tc_fence_after_sync();
             }
+            if (!take_turn()) {
+              ok = false;
+              break;
+            }
+            if (j < n_kv) {
+              // P V of keys 0-63 goes in while the softmax still works on keys 64-127.
+              issue_pv<D, BF16>(o_tmem, s_tmem, ring_v_desc + stage_off(x), j > 0, 0, 4);
+              if (!warp_wait(bar(L::kBarPb + t), parity(p_waits - 1))) {
+                ok = false;
+                break;
+              }
+              tc_fence_after_sync();
+              issue_pv<D, BF16>(o_tmem, s_tmem, ring_v_desc + stage_off(x), true, 4, 8);
+            }
+            if (!warp_wait(bar(L::kBarFullK + x % L::kStages), parity(x / L::kStages))) {
+              ok = false;
+              break;
+            }
+            if (j + 1 < n_kv) {
+              tc_fence_after_sync();
+              issue_qk<D, BF16>(s_tmem, q_desc, ring_k_desc + stage_off(x));
+            }
+            pass_turn();
+            if (j < n_kv) {
+              if (j + 1 < n_kv) {
+                tc_commit_warp(bar(L::kBarS + t));
+                if (j + 2 == n_kv) tc_commit_warp(bar(L::kBarQFree + t));
+              } else {
+                tc_commit_warp(bar(L::kBarO + t));
+              }
+            }
+            tc_commit_warp(bar(L::kBarEmpty + x % L::kStages));
           }
-          tc_commit_warp(bar(L::kBarEmpty + x % L::kStages));
+          it = base + (kHalves ? 2 : 1) * (w.n_max + 1);
+          used += n_kv > 0 ? 1 : 0;
         }
-        it = base + (kHalves ? 2 : 1) * (w.n_max + 1);
-        used += n_kv > 0 ? 1 : 0;
+        // Every MMA issued above must finish before TMEM is released.
+        tc_commit_warp(bar(L::kBarDrain + t));
+        wd.drain(bar(L::kBarDrain + t), 0);
       }
-      // Every MMA issued above must finish before TMEM is released.
-      tc_commit_warp(bar(L::kBarDrain + t));
-      wd.drain(bar(L::kBarDrain + t), 0);
     }
   } else {
+    if constexpr (kSplitRegs) setmaxnreg_inc<kRegsSoftmax>();
     // ------------------------------------------------------------------ softmax
     const int t = warp / 4;
     const int wq = warp % 4;
@@ -734,8 +752,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       // Reference max, base-2 domain (already multiplied by c).  Under the fixed
       // assignment a unit starts from a guess, kept on the first key tile only if
       // that tile's sum of p reaches 1 (a rejected guess is replaced, not kept).
-      // (The dynamic instance starts from the first tile's max: the guess's extra
-      // live values push it past its registers.)
+      // (The dynamic instance starts from the first tile's max: with the guess it
+      // measured 0.5-1% slower at N = 8192.)
       constexpr bool kGuessFirst = !kDynamic;
       float m_ref = kGuessFirst ? kGuessRef : -INFINITY;
       float l = 0.f;
@@ -994,24 +1012,52 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int c64 = 0; c64 < D / 64; ++c64) {
         const uint32_t slab = sbase + L::kOutOff + (kHalves ? c64 : t) * L::kStageOutBytes + wq * 4096;
+        // With the register split, the block's 64 columns (and with key halves O_1's)
+        // are loaded with one wait.
         uint32_t h[32];
+        if (merge) {
+          uint32_t o[2][32], o1[2][32];
 #pragma unroll
-        for (int half = 0; half < 2; ++half) {
-          uint32_t o[32];
-          tmem_ld_x32(t_o + 64 * c64 + 32 * half, o);
-          tmem_wait_ld_x32(o);
-          if (merge) {
-            uint32_t o1[32];
-            tmem_ld_x32(t_o1 + 64 * c64 + 32 * half, o1);
-            tmem_wait_ld_x32(o1);
+          for (int half = 0; half < 2; ++half) {
+            tmem_ld_x32(t_o + 64 * c64 + 32 * half, o[half]);
+            tmem_ld_x32(t_o1 + 64 * c64 + 32 * half, o1[half]);
+          }
+          tmem_wait_ld_x32(o[0]);
+          tmem_tie_x32(o[1]);
+          tmem_tie_x32(o1[0]);
+          tmem_tie_x32(o1[1]);
+#pragma unroll
+          for (int half = 0; half < 2; ++half) {
 #pragma unroll
             for (int i = 0; i < 16; ++i) {
-              const float2 a = __fmul2_rn(make_float2(__uint_as_float(o[2 * i]), __uint_as_float(o[2 * i + 1])), il2);
-              const float2 v =
-                  __ffma2_rn(make_float2(__uint_as_float(o1[2 * i]), __uint_as_float(o1[2 * i + 1])), il2b, a);
+              const float2 a = __fmul2_rn(
+                  make_float2(__uint_as_float(o[half][2 * i]), __uint_as_float(o[half][2 * i + 1])), il2);
+              const float2 v = __ffma2_rn(
+                  make_float2(__uint_as_float(o1[half][2 * i]), __uint_as_float(o1[half][2 * i + 1])), il2b, a);
               h[16 * half + i] = pack2<BF16>(v.x, v.y);
             }
-          } else {
+          }
+        } else if constexpr (kSplitRegs) {
+          uint32_t o[2][32];
+          tmem_ld_x32(t_o + 64 * c64, o[0]);
+          tmem_ld_x32(t_o + 64 * c64 + 32, o[1]);
+          tmem_wait_ld_x32(o[0]);
+          tmem_tie_x32(o[1]);
+#pragma unroll
+          for (int half = 0; half < 2; ++half) {
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              const float2 v = __fmul2_rn(
+                  make_float2(__uint_as_float(o[half][2 * i]), __uint_as_float(o[half][2 * i + 1])), il2);
+              h[16 * half + i] = pack2<BF16>(v.x, v.y);
+            }
+          }
+        } else {
+#pragma unroll
+          for (int half = 0; half < 2; ++half) {
+            uint32_t o[32];
+            tmem_ld_x32(t_o + 64 * c64 + 32 * half, o);
+            tmem_wait_ld_x32(o);
 #pragma unroll
             for (int i = 0; i < 16; ++i) {
               const float2 v = __fmul2_rn(make_float2(__uint_as_float(o[2 * i]), __uint_as_float(o[2 * i + 1])), il2);

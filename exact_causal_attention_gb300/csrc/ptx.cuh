@@ -68,6 +68,19 @@ __device__ __forceinline__ uint64_t global_timer_ns() {
 // such grid be launched once every CTA of this one has issued it or exited.
 __device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
+// Per-thread register count of the calling warpgroup: every warp of the warpgroup
+// executes the same call.  `inc` waits until the registers are free in the block's
+// pool (released by another warpgroup's `dec`), so the counts must add up within
+// the registers the block was launched with.
+template <int kRegs>
+__device__ __forceinline__ void setmaxnreg_inc() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegs));
+}
+template <int kRegs>
+__device__ __forceinline__ void setmaxnreg_dec() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegs));
+}
+
 __device__ __forceinline__ void grid_launch_dependents() {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
