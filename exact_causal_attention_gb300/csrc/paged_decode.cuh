@@ -494,35 +494,49 @@ __global__ void __maxnreg__(128) paged_decode_kernel(const __grid_constant__ CUt
   } else if (!(valid == 0 && seg == 0)) {
     return;  // an empty segment; an empty request is finished by its segment 0
   }
-  // The segments' log-sum-exps of the chunk's heads, all read at once into shared
-  // memory (over the idle ring), then every thread's share of the partial outputs.
-  float* seg_lse = red_s;  // [HC][valid]
-  for (int e = tid; e < HC * valid; e += kDecThreads) {
-    const int k = e / valid, sg = e - k * valid;
-    seg_lse[e] = __ldcg(p.part_lse + sg * stride + static_cast<size_t>(b) * p.Hq + qh0 + k);
-  }
-  __syncthreads();
+  // Every thread takes one (head, four columns) share and reads, six segments at a
+  // time, their log-sum-exps and partial outputs in one round trip, folding each
+  // group in with the online law (running max m, sums rescaled by e^(m_old - m)).
   for (int idx = tid; idx < HC * (D / 4); idx += kDecThreads) {
     const int k = idx / (D / 4), c4 = idx % (D / 4);
     const size_t row = static_cast<size_t>(b) * p.Hq + qh0 + k;
-    const float* ls = seg_lse + k * valid;
     float m = -INFINITY;
-    for (int sg = 0; sg < valid; ++sg) m = fmaxf(m, ls[sg]);
     float wsum = 0.f;
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (m != -INFINITY) {
-#pragma unroll 4
-      for (int sg = 0; sg < valid; ++sg) {
-        const float lse_s = ls[sg];
-        const float wgt = lse_s == -INFINITY ? 0.f : expf(lse_s - m);
-        wsum += wgt;
-        if (wgt == 0.f) continue;
-        const float4 o_s = __ldcg(reinterpret_cast<const float4*>(p.part_o + (sg * stride + row) * D + 4 * c4));
-        acc.x += wgt * o_s.x;
-        acc.y += wgt * o_s.y;
-        acc.z += wgt * o_s.z;
-        acc.w += wgt * o_s.w;
+    for (int s0 = 0; s0 < valid; s0 += 6) {
+      float ls[6];
+      float4 os[6];
+#pragma unroll
+      for (int i = 0; i < 6; ++i) {
+        ls[i] = -INFINITY;
+        os[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (s0 + i < valid) {
+          const size_t r_s = static_cast<size_t>(s0 + i) * stride + row;
+          ls[i] = __ldcg(p.part_lse + r_s);
+          os[i] = __ldcg(reinterpret_cast<const float4*>(p.part_o + r_s * D + 4 * c4));
+        }
       }
+      float mc = m;
+#pragma unroll
+      for (int i = 0; i < 6; ++i) mc = fmaxf(mc, ls[i]);
+      if (mc == -INFINITY) continue;
+      const float sc = m == -INFINITY ? 0.f : expf(m - mc);
+      wsum *= sc;
+      acc.x *= sc;
+      acc.y *= sc;
+      acc.z *= sc;
+      acc.w *= sc;
+#pragma unroll
+      for (int i = 0; i < 6; ++i) {
+        const float wgt = ls[i] == -INFINITY ? 0.f : expf(ls[i] - mc);
+        if (wgt == 0.f) continue;  // (an unwritten partial is never read into the sums)
+        wsum += wgt;
+        acc.x += wgt * os[i].x;
+        acc.y += wgt * os[i].y;
+        acc.z += wgt * os[i].z;
+        acc.w += wgt * os[i].w;
+      }
+      m = mc;
     }
     const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
     uint2 packed = make_uint2(pack2<BF16>(acc.x * inv, acc.y * inv), pack2<BF16>(acc.z * inv, acc.w * inv));
