@@ -364,7 +364,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     for (int t = 0; t < 2; ++t) {
       mbar_init(bar(L::kBarQFull + t), 1);
-      mbar_init(bar(L::kBarQFree + t), 1);
+      // With key halves both slots read Q from buffer 0, which is free again once
+      // both issuers have finished their Q K^T of the unit.
+      mbar_init(bar(L::kBarQFree + t), (kHalves && t == 0) ? 2 : 1);
     }
     for (int s = 0; s < L::kStages; ++s) {
       mbar_init(bar(L::kBarFull + s), 1);
@@ -544,9 +546,9 @@ __global__ void __launch_bounds__(kThreads, 1)
               } else {
                 mbar_arrive(full_k);
               }
-  #ifdef ECA_ANATOMY
+#ifdef ECA_ANATOMY
               if (it == 0) ECA_STAMP(an_slot, 2);  // first K load issued
-  #endif
+#endif
               ++it;
             }
           }
@@ -568,7 +570,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         bool ok = true;
         Unit w;
         while (ok && next_unit(w, false) == 1) {
-          for (int t = 0; t < 2; ++t) {
+          // With key halves one Q tile serves both slots (slot 0 always has work).
+          for (int t = 0; t < (kHalves ? 1 : 2); ++t) {
             if ((t ? w.n_kv1 : w.n_kv0) == 0) continue;
             if (loads[t] > 0 && !wd.wait(bar(L::kBarQFree + t), parity(loads[t] - 1))) {
               ok = false;
@@ -597,7 +600,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int t = warp - 9;
         const uint32_t s_tmem = tmem + 128u * t;                           // S_t, and P_t over it
         const uint32_t o_tmem = tmem + 256u + static_cast<uint32_t>(D) * t;  // O_t
-        const uint64_t q_desc = smem_desc_sw128(sbase + L::kQOff + t * L::kTileBytes, 16, 1024);
+        const int qb = kHalves ? 0 : t;  // Q buffer (and its barriers) of this issuer
+        const uint64_t q_desc = smem_desc_sw128(sbase + L::kQOff + qb * L::kTileBytes, 16, 1024);
         const uint64_t ring_v_desc = smem_desc_sw128(sbase + L::kRingOff, kSubTileBytes, 1024);
         const uint64_t ring_k_desc = smem_desc_sw128(sbase + L::kRingOff + L::kTileBytes, 16, 1024);
         auto stage_off = [&](int item) {  // stage offset in the descriptors' >>4 address field
@@ -636,8 +640,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           // Item 0 (K_0).  Every item this issuer consumes is waited for and released
           // whether or not its tile uses it, so the ring's phases stay aligned (two
           // arrivals per item, or one with key halves).
-          if ((n_kv > 0 && !warp_wait(bar(L::kBarQFull + t), parity(q_loads++))) ||
-              !warp_wait(bar(L::kBarFull + x % L::kStages), parity(x / L::kStages)) ||
+          // With key halves Q is loaded once per unit, so both issuers count every load.
+          const bool q_wait = n_kv > 0 && !warp_wait(bar(L::kBarQFull + qb), parity(q_loads));
+          if (n_kv > 0 || kHalves) ++q_loads;
+          if (q_wait || !warp_wait(bar(L::kBarFull + x % L::kStages), parity(x / L::kStages)) ||
               !warp_wait(bar(L::kBarFullK + x % L::kStages), parity(x / L::kStages))) {
             ok = false;
             break;
@@ -648,13 +654,20 @@ __global__ void __launch_bounds__(kThreads, 1)
             break;
           }
           if (n_kv > 0) issue_qk<D, BF16>(s_tmem, q_desc, ring_k_desc + stage_off(x));
-  #ifdef ECA_ANATOMY
+#ifdef ECA_ANATOMY
           if (t == 0 && base == 0 && lane == 0) ECA_STAMP(an_slot, 3);  // first Q K^T issued
           if (t == 0 && lane == 0) ++an_units;
-  #endif
+#endif
           pass_turn();
           if (n_kv > 0) tc_commit_warp(bar(L::kBarS + t));
-          if (n_kv == 1) tc_commit_warp(bar(L::kBarQFree + t));  // this tile's Q K^T are all issued
+          if (n_kv == 1) tc_commit_warp(bar(L::kBarQFree + qb));  // this tile's Q K^T are all issued
+          // A key-halves slot with no keys releases the shared Q buffer at once: this
+          // turn comes after the other issuer's first Q K^T of the unit, so the
+          // buffer's previous phase is complete.
+          if (kHalves && n_kv == 0) {
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(L::kBarQFree + qb));
+          }
           tc_commit_warp(bar(L::kBarEmpty + x % L::kStages));
           for (int j = 0; j < w.n_max; ++j) {
             x = item(j + 1);
@@ -701,7 +714,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (j < n_kv) {
               if (j + 1 < n_kv) {
                 tc_commit_warp(bar(L::kBarS + t));
-                if (j + 2 == n_kv) tc_commit_warp(bar(L::kBarQFree + t));
+                if (j + 2 == n_kv) tc_commit_warp(bar(L::kBarQFree + qb));
               } else {
                 tc_commit_warp(bar(L::kBarO + t));
               }

@@ -166,6 +166,9 @@ __global__ void __maxnreg__(128) paged_decode_kernel(const __grid_constant__ CUt
   // Launched with programmatic serialisation: the next launch may be scheduled at
   // once, and no global memory is read before the grid ahead of this one finished.
   grid_launch_dependents();
+  // The cache's tensor map comes from the launch's own parameters: its descriptor
+  // fetch starts before the wait and overlaps the page-id and length reads.
+  if (threadIdx.x == kDecWarps * 32) tma_prefetch_map(&tm_cache);
   grid_dependency_wait();
   const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
   // unit: (b, kv head, head chunk, segment), segment fastest
@@ -248,7 +251,6 @@ __global__ void __maxnreg__(128) paged_decode_kernel(const __grid_constant__ CUt
   if (warp == kDecWarps) {
     // ----------------------------------------------------------------- producer
     if (lane == 0) {
-      tma_prefetch_map(&tm_cache);
       // Each decode step reads its K/V once: evict-first.
       const uint64_t pol = policy_evict_first();
       // The window is refilled with cp.async: after tile i is issued, its slots
