@@ -352,6 +352,42 @@ def bench_sweep_point(eca, inputs, dev, stream, flush, n):
             "graph_ms": round(graph_ms, 4), "graph_tflops": tf(graph_ms)}
 
 
+def measure_host_link(hq, hk, hv, ho, hl, dq, dk, dv, do, dl, s, dev, h2d, d2h, kernel_ms):
+    """The host link's own rates for one step's buffers (the upload alone, the download alone, both at
+    once; median of 5 each) and the step time they allow with the kernel overlapped: the floor the
+    end-to-end number is measured against."""
+    import torch
+
+    s2 = torch.cuda.Stream(dev)
+
+    def timed(up, down):
+        ts = []
+        for _ in range(5):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(s)
+            s2.wait_event(a)
+            with torch.cuda.stream(s):
+                if up:
+                    dq.copy_(hq, non_blocking=True)
+                    dk.copy_(hk, non_blocking=True)
+                    dv.copy_(hv, non_blocking=True)
+            with torch.cuda.stream(s2):
+                if down:
+                    ho.copy_(do, non_blocking=True)
+                    hl.copy_(dl, non_blocking=True)
+            s.wait_stream(s2)
+            b.record(s)
+            ts.append((a, b))
+        torch.cuda.synchronize(dev)
+        return sorted(a.elapsed_time(b) for a, b in ts)[2]
+
+    up_ms, down_ms, both_ms = timed(True, False), timed(False, True), timed(True, True)
+    floor_ms = max(up_ms, down_ms, both_ms, kernel_ms)
+    return {"h2d_gbs": round(h2d / (up_ms * 1e-3) / 1e9, 1), "d2h_gbs": round(d2h / (down_ms * 1e-3) / 1e9, 1),
+            "both_ms": round(both_ms, 4), "floor_ms_per_step": round(floor_ms, 4),
+            "note": "floor = the slowest of the upload alone, the download alone, both at once, and the kernel"}
+
+
 def launch_order() -> str:
     """How the library launches its kernels in this process: programmatic dependent launch
     (the default), or plain stream order with ECA_PDL=0."""
@@ -643,6 +679,9 @@ def bench_ours(args, w):
         raise RuntimeError("a kernel wait timed out in the end-to-end loop")
     h2d = sum(x.numel() * x.element_size() for x in (hq, hk, hv))
     d2h = ho[0].numel() * ho[0].element_size() + hl[0].numel() * hl[0].element_size()
+    host_link = measure_host_link(hq, hk, hv, ho[0], hl[0], bq[1], bk[1], bv[1], bo[1], bl[1], s_up, dev,
+                                  h2d, d2h, kernel_ms)
+    host_link["e2e_frac_of_floor"] = round(host_link["floor_ms_per_step"] / e2e_ms, 3)
 
     sweep = {}
     sweep_graph = {}
@@ -779,7 +818,8 @@ def bench_ours(args, w):
         "e2e": {"value": flops / (e2e_ms * 1e-3) / 1e12 * world, "unit": "TFLOP/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
                 "schedule": "pinned host buffers; two device buffer sets; upload, kernel and download on three "
-                            "streams, the upload of step i + 1 and download of step i - 1 overlapping kernel i"},
+                            "streams, the upload of step i + 1 and download of step i - 1 overlapping kernel i",
+                "host_link": host_link},
         "gpu_launches": args.steps,
         "launch_order": launch_order(),
         "clocks": clocks,

@@ -136,3 +136,40 @@ for i, (B, H, N, D) in enumerate(%r):
         assert eca.device_status() == 0
         assert np.array_equal(o.view(torch.int16).cpu().numpy(), np.load(tmp_path / f"o{i}.npy")), (B, H, N, D)
         assert np.array_equal(lse.cpu().numpy(), np.load(tmp_path / f"l{i}.npy")), (B, H, N, D)
+
+
+@pytest.mark.parametrize("B,H,N,D", [(1, 32, 512, 128), (2, 6, 1000, 64), (1, 40, 4096, 128)])
+def test_chained_calls_read_the_previous_output(cuda_lib, B, H, N, D):
+    """Back-to-back calls on one stream where each call reads the previous call's output
+    as its query and writes its own output over the previous call's query, with a copy
+    kernel of torch's rewriting the next input after every second call: under
+    programmatic launch a call's CTAs may start while the kernel ahead still runs, so
+    this checks that nothing is read or written before that kernel has finished.  The
+    same chain with a synchronisation after every operation is the reference."""
+    eca = cuda_lib
+    q0, k, v = (x.cuda() for x in inputs.make_qkv(B, H, N, D, "fp16", seed=900 + N))
+    fresh = (q0 * 0.5).contiguous()
+
+    def chain(sync):
+        bufs = [q0.clone(), torch.empty_like(q0)]
+        outs, src = [], 0
+        for i in range(6):
+            q, o = bufs[src], bufs[1 - src]
+            eca.attn_fwd_into(q, k, v, o, None, causal=True)
+            if sync:
+                torch.cuda.synchronize()
+            outs.append(o.clone())
+            if i % 2 == 1:
+                o.copy_(fresh)  # the next call's input, rewritten right behind this call
+                if sync:
+                    torch.cuda.synchronize()
+            src = 1 - src
+        torch.cuda.synchronize()
+        return outs
+
+    ref = chain(True)
+    for _ in range(2):
+        got = chain(False)
+        assert eca.device_status() == 0
+        for a, b in zip(ref, got):
+            assert torch.equal(a, b)

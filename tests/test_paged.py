@@ -123,6 +123,43 @@ def test_append_then_decode(cuda_lib):
     check(o, lse, ro, rl, "fp16", None, lengths)
 
 
+@pytest.mark.parametrize("splits", [1, 3])
+def test_decode_right_behind_append_sees_the_new_token(cuda_lib, splits):
+    """The append and the decode are launched back to back on one stream with no
+    synchronisation between them (under programmatic launch the decode's CTAs may start
+    while the append still runs): the decode must see every appended token.  Repeated
+    so that a race would show."""
+    import exact_causal_attention_gb300 as eca
+
+    B, Hq, Hkv, D, T = 4, 8, 2, 128, 16
+    lengths = [17, 48, 1, 300]
+    q, cache, table, lens = inputs.paged_decode_inputs(B, Hq, Hkv, D, T, lengths, "fp16", seed=81)
+    new = torch.randn(B, 2, Hkv, D, generator=torch.Generator().manual_seed(82), dtype=torch.float64).to(torch.float16)
+    expect = cache.clone()
+    for b, L in enumerate(lengths):
+        t = L - 1
+        expect[int(table[b, t // T]), :, t % T] = new[b]
+    scale = 1.0 / math.sqrt(D)
+    ro, rl = oracle_decode(q, expect, table, lens, T, scale, "fp16")
+    dq, dt, dl, dnew = q.cuda(), table.cuda(), lens.cuda(), new.cuda()
+    for _ in range(3):
+        dc = cache.cuda()
+        torch.cuda.synchronize()
+        out = torch.full_like(dq, float("nan"))
+        lse = torch.full(q.shape[:2], float("nan"), dtype=torch.float32, device="cuda")
+        ws = None
+        if splits > 1:
+            need = int(eca.load_library().attn_decode_workspace_bytes(B, Hq, D, splits))
+            ws = torch.empty(need + 256, dtype=torch.uint8, device="cuda")
+            off = (-ws.data_ptr()) % 256
+            ws = ws[off:off + need]
+        eca.paged_append(dnew, dc, dt, dl)
+        eca.decode_paged(dq, dc, dt, dl, scale=scale, kv_splits=splits, out=out, lse=lse, workspace=ws)
+        torch.cuda.synchronize()
+        assert eca.device_status() == 0
+        check(out.double().cpu().numpy(), lse.double().cpu().numpy(), ro, rl, "fp16", None, lengths)
+
+
 def test_out_of_range_entries_are_rejected_not_read(cuda_lib):
     import exact_causal_attention_gb300 as eca
 
