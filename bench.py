@@ -839,18 +839,30 @@ def bench_ours(args, w):
     print(json.dumps(line), flush=True)
 
 
-def bench_launch_cost():
-    """Builds and runs csrc/launch_cost_probe.cu: microseconds per launch of empty one-CTA-per-SM
-    kernels, 200 back to back, for the launch boundaries that set the floor of a short call."""
+def run_probe(name):
+    """Builds (if stale) and runs the measurement probe csrc/<name>.cu; returns its JSON output."""
     from exact_causal_attention_gb300 import build as cuda_build
 
-    src = os.path.join(cuda_build.CSRC, "launch_cost_probe.cu")
-    exe = os.path.join(cuda_build.BUILD_DIR, "launch_cost_probe")
+    src = os.path.join(cuda_build.CSRC, name + ".cu")
+    exe = os.path.join(cuda_build.BUILD_DIR, name)
     os.makedirs(cuda_build.BUILD_DIR, exist_ok=True)
     if not os.path.exists(exe) or os.path.getmtime(exe) < os.path.getmtime(src):
         subprocess.run([cuda_build._nvcc(), *cuda_build.ARCH_FLAGS, "-O2", "-std=c++17", "-o", exe, src], check=True)
     out = subprocess.run([exe], check=True, capture_output=True, text=True, timeout=300).stdout
     return json.loads(out)
+
+
+def bench_launch_cost():
+    """csrc/launch_cost_probe.cu: microseconds per launch of empty one-CTA-per-SM kernels, 200 back to
+    back, for the launch boundaries that set the floor of a short call."""
+    return run_probe("launch_cost_probe")
+
+
+def bench_ingress():
+    """csrc/ingress_probe.cu: the rate at which bulk copies fill one SM's shared memory, from HBM and
+    from L2, with 16, 64 and all SMs streaming: the ceiling on the K/V tile fills of the attention
+    kernel."""
+    return run_probe("ingress_probe")
 
 
 def main():
@@ -877,10 +889,15 @@ def main():
     ap.add_argument("--launch-cost", action="store_true",
                     help="time per launch of empty kernels (with and without global stores and tensor memory) in "
                          "stream order, with programmatic dependent launch and from a CUDA graph")
+    ap.add_argument("--ingress", action="store_true",
+                    help="shared-memory fill rate per SM by bulk copies, from HBM and from L2")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
     if args.launch_cost:
         print(json.dumps({"launch_cost": bench_launch_cost()}), flush=True)
+        return
+    if args.ingress:
+        print(json.dumps({"ingress": bench_ingress()}), flush=True)
         return
     from exact_causal_attention_gb300 import inputs
 
