@@ -495,9 +495,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         // counter (skipping key segments past a pair's last key tile, which have no
         // work) when it is about to load their items, and queues them for the other
         // warps; so a unit goes to the CTA that is free first.
+        // A CTA's first unit is its own index (the grid never exceeds the units), so
+        // the launch does not start with every CTA contending for the counter at once;
+        // the counter then hands out units from the grid size on.
+        bool first_claim = true;
         auto take_unit = [&]() -> int {
           while (true) {
-            const int l = atomicAdd(p.sched, 1);
+            const int l = first_claim ? static_cast<int>(blockIdx.x) : atomicAdd(p.sched, 1) + static_cast<int>(gridDim.x);
+            first_claim = false;
             if (l >= p.n_units) return -1;
             Unit u;
             unit_from<kHalves>(l, p, hd, u);
