@@ -87,7 +87,9 @@ enum attn_status {
   ATTN_ERR_UNALIGNED = -2,      /* a tensor pointer is not 16-byte aligned */
   ATTN_ERR_UNSUPPORTED_D = -3,  /* D is not 64 or 128 */
   ATTN_ERR_ARCH = -4,           /* the current device is not an sm_103 part */
-  ATTN_ERR_LAUNCH = -5,         /* the CUDA runtime refused the launch (cudaGetLastError) */
+  ATTN_ERR_LAUNCH = -5,         /* the CUDA runtime refused the launch, or the library was built with
+                                   fewer registers per thread than its attention kernel's warpgroups
+                                   move between them (checked before the first launch) */
   ATTN_ERR_TIMEOUT = -6,        /* a kernel's bounded wait expired (reported by attn_device_status) */
   ATTN_ERR_CUDA = -7,           /* another CUDA runtime/driver call failed */
   ATTN_ERR_SCRATCH_LIMIT = -8,  /* attn_fwd_splitkv_noalloc: the split needs more than its fixed scratch */
