@@ -252,3 +252,18 @@ def test_guessed_reference_with_subnormal_probabilities(cuda_lib, D, first):
     stats = compare(o, lse, ro, rl, "fp16")
     record(f"guessed_reference_{first}_d{D}", {**stats, "excess_over_output_rounding": excess})
     assert excess <= 1e-3, {**stats, "excess_over_output_rounding": excess}
+
+
+@pytest.mark.parametrize("causal,dtype", [(False, "fp16"), (True, "bf16"), (False, "bf16")])
+def test_counter_units_other_masks_and_types(cuda_lib, causal, dtype):
+    """Launches whose K and V exceed 64 MiB take their units from the launch's counter in
+    head groups.  The workloads cover that path causal and in fp16 only; here it runs
+    non-causal and in bf16 too (B=2 H=32 N=4096 D=128: K and V 128 MiB), every row
+    against the oracle."""
+    B, H, N, D = 2, 32, 4096, 128
+    q, k, v = inputs.make_qkv(B, H, N, D, dtype, seed=7100 + int(causal) + (dtype == "bf16") * 2)
+    scale = 1.0 / math.sqrt(D)
+    o, lse = run_gpu(q, k, v, causal, scale)
+    ro, rl = oracle_full(q, k, v, dtype, causal, scale)
+    compare(o, lse, ro, rl, dtype, p_rounding_term(q, k, v, dtype, causal, scale),
+            name=f"counter_units_b2_h32_n4096_d128_{dtype}_{'causal' if causal else 'noncausal'}")
