@@ -267,3 +267,16 @@ def test_counter_units_other_masks_and_types(cuda_lib, causal, dtype):
     ro, rl = oracle_full(q, k, v, dtype, causal, scale)
     compare(o, lse, ro, rl, dtype, p_rounding_term(q, k, v, dtype, causal, scale),
             name=f"counter_units_b2_h32_n4096_d128_{dtype}_{'causal' if causal else 'noncausal'}")
+
+
+@pytest.mark.parametrize("causal", [True, False])
+def test_counter_units_d64_ragged(cuda_lib, causal):
+    """The counter path with D = 64 and a ragged length (B=4 H=32 N=4000: K and V
+    131 MB), every row against the oracle."""
+    B, H, N, D = 4, 32, 4000, 64
+    q, k, v = inputs.make_qkv(B, H, N, D, "fp16", seed=7200 + int(causal))
+    scale = 1.0 / math.sqrt(D)
+    o, lse = run_gpu(q, k, v, causal, scale)
+    ro, rl = oracle_full(q, k, v, "fp16", causal, scale)
+    compare(o, lse, ro, rl, "fp16", None,
+            name=f"counter_units_b4_h32_n4000_d64_fp16_{'causal' if causal else 'noncausal'}")
