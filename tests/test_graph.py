@@ -173,3 +173,36 @@ def test_chained_calls_read_the_previous_output(cuda_lib, B, H, N, D):
         assert eca.device_status() == 0
         for a, b in zip(ref, got):
             assert torch.equal(a, b)
+
+
+def test_chained_split_calls_read_the_previous_output(cuda_lib):
+    """The same chain through the key split (an attention launch and a merge launch per
+    call, both launched programmatically): each call reads the previous call's output."""
+    eca = cuda_lib
+    B, H, N, D, splits = 1, 4, 2048, 128, 3
+    q0, k, v = (x.cuda() for x in inputs.make_qkv(B, H, N, D, "fp16", seed=950))
+    need = eca.splitkv_workspace_bytes(B, H, N, D, splits)
+    raw = torch.empty(need + 256, dtype=torch.uint8, device="cuda")
+    off = (-raw.data_ptr()) % 256
+    ws = raw[off:off + need]
+
+    def chain(sync):
+        bufs = [q0.clone(), torch.empty_like(q0)]
+        outs, src = [], 0
+        for _ in range(4):
+            q, o = bufs[src], bufs[1 - src]
+            lse = torch.empty(B, H, N, device="cuda")
+            eca.attn_fwd_splitkv(q, k, v, o, lse, kv_splits=splits, workspace=ws, causal=True)
+            if sync:
+                torch.cuda.synchronize()
+            outs.append((o.clone(), lse))
+            src = 1 - src
+        torch.cuda.synchronize()
+        return outs
+
+    ref = chain(True)
+    for _ in range(2):
+        got = chain(False)
+        assert eca.device_status() == 0
+        for (a, la), (b, lb) in zip(ref, got):
+            assert torch.equal(a, b) and torch.equal(la, lb)
