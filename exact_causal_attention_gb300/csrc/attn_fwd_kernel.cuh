@@ -58,9 +58,10 @@
 //   * stale reference max: o and l share one reference m, and any reference
 //     gives the same O and lse (exact algebra), so p is formed against the
 //     current reference without first taking the new tile's row max.  No p may
-//     overflow the 16-bit P: a sum of at most 2^15 over keys 0-63 bounds each of
-//     their p, and a max score of keys 64-127 at most 15 above the reference
-//     bounds theirs.  Under the fixed assignment a unit whose first key tile is
+//     overflow the 16-bit P: with fp16 a sum of at most 2^15 over keys 0-63 bounds
+//     each of their p, and a max score of keys 64-127 at most 15 above the
+//     reference bounds theirs (bf16, with fp32's exponent range, takes 2^30 and 30,
+//     which only keep l and o in fp32 range).  Under the fixed assignment a unit whose first key tile is
 //     unmasked starts from a guessed reference, kept only if the row's sum of p
 //     over that tile is at least 1: then l >= 1 from the first tile on, as with
 //     the row max as reference, so a p that lands in fp16's subnormal range
@@ -84,7 +85,16 @@ constexpr int kBlockN = 128;            // keys per K/V tile
 constexpr int kSubTileBytes = 128 * 128;  // 128 rows x 64 16-bit elements (one 128-B swizzle span)
 constexpr int kThreads = 384;
 constexpr int kTmemCols = 512;
-constexpr float kMaxRowSum = 32768.0f;  // bound on sum_j p_ij that keeps every p in fp16 range
+// Bounds of the stale reference that keep every p in range of the 16-bit P: with
+// fp16, a sum of at most 2^15 over keys 0-63 bounds each of their p, and keys
+// 64-127 may score at most 15 above the reference.  bf16 has fp32's exponent range,
+// so P cannot overflow there; its looser bounds (2^30, 30) only keep the fp32 l and
+// o far from overflow (l stays below N 2^30), and let wide score distributions keep
+// the reference longer.
+template <bool BF16>
+__host__ __device__ constexpr float max_row_sum() { return BF16 ? 1073741824.0f : 32768.0f; }
+template <bool BF16>
+__host__ __device__ constexpr float max_lead() { return BF16 ? 30.0f : 15.0f; }
 constexpr float kGuessRef = 4.0f;       // first reference of a unit (scores times scale log2 e)
 constexpr float kMinGuessSum = 1.0f;    // a guess is kept only if the first tile's sum of p reaches this
 constexpr int kUnitQueue = 4;           // depth of the shared-memory queue of unit indices
@@ -853,7 +863,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           } else if (masked) {
             load_scores();
             row_sum = exponentiate(-m_ref);
-            move = !(row_sum <= kMaxRowSum);  // (also an inf sum)
+            move = !(row_sum <= max_row_sum<BF16>());  // (also an inf sum)
           } else {
             // Keys 64-127 load while keys 0-63 are exponentiated.
             tmem_ld_x32(t_s, s[0]);
@@ -878,11 +888,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             // Keys 0-63 are handed over before keys 64-127 are exponentiated, so the
             // reference must hold for the whole row now: keys 0-63 are safe when
             // their sum of p is at most the bound, keys 64-127 when their max score
-            // is at most log2(bound) = 15 above the reference.  A guess (first tile)
+            // is at most the lead bound (log2 of the sum bound) above the reference.  A guess (first tile)
             // also needs the row's sum of p to reach 1, which keys 0-63 show by their
             // sum and keys 64-127 by a max score at or above the reference (p >= 1).
             const float top_b = fmaxf(mx[0], mx[1]) * c - m_ref;
-            const bool fast = sum_a <= kMaxRowSum && top_b <= 15.f &&
+            const bool fast = sum_a <= max_row_sum<BF16>() && top_b <= max_lead<BF16>() &&
                               (j > 0 || sum_a >= kMinGuessSum || top_b >= 0.f);
             if (__all_sync(0xffffffffu, fast)) {
               tmem_st_x32(t_s, pk[0]);
@@ -901,10 +911,10 @@ __global__ void __launch_bounds__(kThreads, 1)
               l += sum_a + row_total(acc);
               continue;
             }
-            load_scores();
-            row_sum = exponentiate(-m_ref);
-            // A guess is kept only if the row's sum of p reaches 1 (an inf sum also moves).
-            move = !(row_sum <= kMaxRowSum) || (j == 0 && !(row_sum >= kMinGuessSum));
+            // A row that failed a bound, or whose guess fell short, takes the row max;
+            // the other rows keep their reference, which the checks above showed to
+            // hold for them (no second pass over the row to decide).
+            move = !fast;
           }
         }
         if (__any_sync(0xffffffffu, move)) {
