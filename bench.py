@@ -450,6 +450,46 @@ def bench_anatomy(eca, inputs, dev, stream, flush, n):
     return out
 
 
+def bench_workloads(eca, inputs, dev, stream, flush):
+    """Every parity workload (the page's configurations, bf16 and D = 64 included) timed as a
+    single call after an L2 flush (median of 10 after 3) and as 20 calls back to back;
+    TFLOP/s counts 2BHN²D causal and 4BHN²D non-causal, as the headline."""
+    import torch
+
+    out = {}
+    for name, w in inputs.WORKLOADS.items():
+        q, k, v = (x.to(dev) for x in inputs.workload_qkv(w))
+        o = torch.empty_like(q)
+        lse = torch.empty((w.B, w.H, w.N), dtype=torch.float32, device=dev)
+
+        def call():
+            eca.attn_fwd_into(q, k, v, o, lse, causal=w.causal, scale=w.scale, stream=stream)
+
+        for _ in range(3):
+            call()
+        single = []
+        for _ in range(13):
+            flush.zero_()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            call()
+            b.record(stream)
+            single.append((a, b))
+        flush.zero_()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(20):
+            call()
+        b.record(stream)
+        torch.cuda.synchronize(dev)
+        ms = sorted(x.elapsed_time(y) for x, y in single[3:])[5]
+        b2b = a.elapsed_time(b) / 20
+        out[name] = {"single_ms": round(ms, 4), "single_tflops": round(w.flops / (ms * 1e-3) / 1e12, 1),
+                     "back_to_back_ms": round(b2b, 4), "back_to_back_tflops": round(w.flops / (b2b * 1e-3) / 1e12, 1)}
+        del q, k, v, o, lse
+    return out
+
+
 def bench_gqa(eca, inputs, dev, stream, flush):
     """Grouped heads, causal B=1 H=32 Hkv=8 N=8192 D=128 fp16 (4 query heads per key/value head);
     L2 flushed before every call; TFLOP/s counts 2BHN²D."""
@@ -750,6 +790,7 @@ def bench_ours(args, w):
 
     # Grouped key/value heads (GQA, 4 query heads per key/value head), causal B=1 H=32 Hkv=8 N=8192 D=128.
     gqa = bench_gqa(eca, inputs, dev, stream, flush) if (not args.no_sweep and rank == 0) else {}
+    workloads = bench_workloads(eca, inputs, dev, stream, flush) if (not args.no_sweep and rank == 0) else {}
 
     # Online row softmax (fp32): an HBM-bound kernel, one read and one write per element.
     row_softmax = bench_row_softmax(eca, inputs, dev, stream, flush) if (not args.no_sweep and rank == 0) else {}
@@ -827,6 +868,7 @@ def bench_ours(args, w):
         "sweep_graph": sweep_graph,
         "splitkv": splitkv,
         "gqa": gqa,
+        "workloads": workloads,
         "row_softmax": row_softmax,
         "paged_decode": paged,
         "fp16_matmul_peak_tflops": fp16_peak,
