@@ -39,8 +39,8 @@ L2_FLUSH_BYTES = 256 << 20  # twice the 129 MB L2
 DATASHEET_DENSE_FP16_TFLOPS = 2250.0
 DATASHEET_SOURCE = "NVIDIA HGX B300 specification: FP16/BF16 tensor 36 PFLOPS per 8 GPUs with sparsity -> 2.25 dense per GPU"
 # Dense fp16 MMA work one SM retires per clock (a 128x128x16 tcgen05.mma every 64 cycles),
-# consistent with the ncu capture of the attention kernel (tensor pipe 76.7% active at
-# 1.816 GHz while executing 1.73 PFLOP/s over 152 SMs).
+# consistent with the ncu capture of the attention kernel (tensor pipe 77.1% active at
+# 1.781 GHz while executing 1.71 PFLOP/s over 152 SMs).
 MMA_FLOP_PER_CLK_PER_SM = 8192
 PROFILES = os.path.join(ROOT, "profiles")
 
