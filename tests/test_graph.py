@@ -99,8 +99,8 @@ def test_tensor_map_cache_follows_shape_changes(cuda_lib):
 def test_stream_order_launch_gives_the_same_results(cuda_lib, tmp_path):
     """The library launches with programmatic dependent launch by default; ECA_PDL=0
     launches in plain stream order.  Both orders must give bit-identical results for
-    back-to-back calls of every unit mode (a second process, since the switch is read
-    once per process)."""
+    back-to-back calls of every unit mode, the key split, and an append followed by a
+    split decode (a second process, since the switch is read once per process)."""
     import os
     import subprocess
     import sys
@@ -122,6 +122,18 @@ for i, (B, H, N, D) in enumerate(%r):
     assert eca.device_status() == 0
     np.save(sys.argv[2] + f"/o{i}.npy", o.view(torch.int16).cpu().numpy())
     np.save(sys.argv[2] + f"/l{i}.npy", lse.cpu().numpy())
+# the key split (attention and merge launches) and the paged append and decode
+q, k, v = (x.cuda() for x in inputs.make_qkv(1, 4, 2048, 128, "fp16", seed=731))
+o, lse = eca.attn_fwd_splitkv(q, k, v, kv_splits=3, causal=True)
+pq, cache, table, lens = inputs.paged_decode_inputs(4, 8, 2, 128, 16, [300, 17, 48, 1], "fp16", seed=732)
+new = torch.randn(4, 2, 2, 128, generator=torch.Generator().manual_seed(733), dtype=torch.float64).to(torch.float16)
+dc = cache.cuda()
+eca.paged_append(new.cuda(), dc, table.cuda(), lens.cuda())
+do, dl = eca.decode_paged(pq.cuda(), dc, table.cuda(), lens.cuda(), kv_splits=3)
+torch.cuda.synchronize()
+assert eca.device_status() == 0
+for name, t in (("so", o.view(torch.int16)), ("sl", lse), ("do", do.view(torch.int16)), ("dl", dl)):
+    np.save(sys.argv[2] + f"/{name}.npy", t.cpu().numpy())
 ''' % (shapes,)
     root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
     env = dict(os.environ, ECA_PDL="0")
@@ -136,6 +148,17 @@ for i, (B, H, N, D) in enumerate(%r):
         assert eca.device_status() == 0
         assert np.array_equal(o.view(torch.int16).cpu().numpy(), np.load(tmp_path / f"o{i}.npy")), (B, H, N, D)
         assert np.array_equal(lse.cpu().numpy(), np.load(tmp_path / f"l{i}.npy")), (B, H, N, D)
+    q, k, v = (x.cuda() for x in inputs.make_qkv(1, 4, 2048, 128, "fp16", seed=731))
+    so, sl = eca.attn_fwd_splitkv(q, k, v, kv_splits=3, causal=True)
+    pq, cache, table, lens = inputs.paged_decode_inputs(4, 8, 2, 128, 16, [300, 17, 48, 1], "fp16", seed=732)
+    new = torch.randn(4, 2, 2, 128, generator=torch.Generator().manual_seed(733), dtype=torch.float64).to(torch.float16)
+    dc = cache.cuda()
+    eca.paged_append(new.cuda(), dc, table.cuda(), lens.cuda())
+    do, dl = eca.decode_paged(pq.cuda(), dc, table.cuda(), lens.cuda(), kv_splits=3)
+    torch.cuda.synchronize()
+    assert eca.device_status() == 0
+    for name, t in (("so", so.view(torch.int16)), ("sl", sl), ("do", do.view(torch.int16)), ("dl", dl)):
+        assert np.array_equal(t.cpu().numpy(), np.load(tmp_path / f"{name}.npy")), name
 
 
 @pytest.mark.parametrize("B,H,N,D", [(1, 32, 512, 128), (2, 6, 1000, 64), (1, 40, 4096, 128)])
