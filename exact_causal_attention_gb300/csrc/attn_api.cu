@@ -937,42 +937,38 @@ int attn_row_softmax_f32(const float* x, float* y, long long M, int N, attn_stre
   const bool vec = (N % 4) == 0 && aligned(x, 16) && aligned(y, 16);
   const unsigned warp_blocks = static_cast<unsigned>((M + 7) / 8);  // 8 rows (warps) per block
   const unsigned row_blocks = static_cast<unsigned>(M);
-#define ECA_WARP_ROWS(ITEMS)                                                                          \
-  (vec ? eca::row_softmax_cached<32, ITEMS, true><<<warp_blocks, 256, 0, s>>>(x, y, M, N)            \
-       : eca::row_softmax_cached<32, ITEMS, false><<<warp_blocks, 256, 0, s>>>(x, y, M, N))
-#define ECA_BLOCK_ROWS(ITEMS)                                                                         \
-  (vec ? eca::row_softmax_cached<256, ITEMS, true><<<row_blocks, 256, 0, s>>>(x, y, M, N)            \
-       : eca::row_softmax_cached<256, ITEMS, false><<<row_blocks, 256, 0, s>>>(x, y, M, N))
+  cudaError_t err;
+#define ECA_ROWS(TPR, ITEMS, BLOCKS)                                                                   \
+  err = vec ? launch_pdl(eca::row_softmax_cached<TPR, ITEMS, true>, BLOCKS, 256, 0, s, x, y, M, N)    \
+            : launch_pdl(eca::row_softmax_cached<TPR, ITEMS, false>, BLOCKS, 256, 0, s, x, y, M, N)
   const unsigned pair_blocks = static_cast<unsigned>((M + 1) / 2);  // 2 rows (128 threads each) per block
   if (N <= 32 * 4) {
-    ECA_WARP_ROWS(4);
+    ECA_ROWS(32, 4, warp_blocks);
   } else if (N <= 32 * 8) {
-    ECA_WARP_ROWS(8);
+    ECA_ROWS(32, 8, warp_blocks);
   } else if (N <= 32 * 16) {
-    ECA_WARP_ROWS(16);
+    ECA_ROWS(32, 16, warp_blocks);
   } else if (N <= 32 * 32) {
-    ECA_WARP_ROWS(32);
+    ECA_ROWS(32, 32, warp_blocks);
   } else if (N <= 32 * 64) {
-    ECA_WARP_ROWS(64);
+    ECA_ROWS(32, 64, warp_blocks);
   } else if (N <= 128 * 32) {
     // 128 threads per row: a short matrix (such as 1024 x 4096) fits in one wave.
-    if (vec) {
-      eca::row_softmax_cached<128, 32, true><<<pair_blocks, 256, 0, s>>>(x, y, M, N);
-    } else {
-      eca::row_softmax_cached<128, 32, false><<<pair_blocks, 256, 0, s>>>(x, y, M, N);
-    }
+    ECA_ROWS(128, 32, pair_blocks);
   } else if (N <= 256 * 32) {
-    ECA_BLOCK_ROWS(32);
+    ECA_ROWS(256, 32, row_blocks);
   } else if (N <= 256 * 64) {
-    ECA_BLOCK_ROWS(64);
-  } else if (vec) {
-    eca::row_softmax_stream<true><<<row_blocks, 256, 0, s>>>(x, y, M, N);
+    ECA_ROWS(256, 64, row_blocks);
   } else {
-    eca::row_softmax_stream<false><<<row_blocks, 256, 0, s>>>(x, y, M, N);
+    err = vec ? launch_pdl(eca::row_softmax_stream<true>, row_blocks, 256, 0, s, x, y, M, N)
+              : launch_pdl(eca::row_softmax_stream<false>, row_blocks, 256, 0, s, x, y, M, N);
   }
-#undef ECA_WARP_ROWS
-#undef ECA_BLOCK_ROWS
-  return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_LAUNCH;
+#undef ECA_ROWS
+  if (err != cudaSuccess) {
+    cudaGetLastError();
+    return ATTN_ERR_LAUNCH;
+  }
+  return ATTN_OK;
 }
 
 int attn_device_status(attn_stream_t stream) {

@@ -15,8 +15,12 @@
 //   * 256-thread block per row, two passes over the row: larger N.
 // Loads and stores are 16-byte vectors when N is a multiple of 4 (rows then
 // start 16-byte aligned), scalar otherwise (the page's N = 257 case).
+// Launched with programmatic stream serialisation: each kernel lets the next grid
+// launch at once and waits for the grid ahead of it before touching memory.
 #pragma once
 #include <cstdint>
+
+#include "ptx.cuh"
 
 namespace eca {
 
@@ -76,6 +80,8 @@ __device__ __forceinline__ OnlineMD md_block_reduce(OnlineMD s, OnlineMD* smem) 
 template <int TPR, int ITEMS, bool VEC>
 __global__ void __launch_bounds__(256) row_softmax_cached(const float* x, float* y, long long M, int N) {
   __shared__ OnlineMD red[8];
+  grid_launch_dependents();
+  grid_dependency_wait();
   const int tid = threadIdx.x % TPR;
   const int rows_per_block = 256 / TPR;
   const long long row = static_cast<long long>(blockIdx.x) * rows_per_block + threadIdx.x / TPR;
@@ -131,6 +137,8 @@ __global__ void __launch_bounds__(256) row_softmax_cached(const float* x, float*
 template <bool VEC>
 __global__ void __launch_bounds__(256) row_softmax_stream(const float* x, float* y, long long M, int N) {
   __shared__ OnlineMD red[8];
+  grid_launch_dependents();
+  grid_dependency_wait();
   const long long row = blockIdx.x;
   if (row >= M) return;
   const float* xr = x + row * static_cast<long long>(N);

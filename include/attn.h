@@ -39,7 +39,8 @@
  * CTAs may be scheduled while the work ahead of it on the stream still runs, but
  * they touch no global memory before it has completed.  The attention and
  * decode kernels also let the next such launch on the stream be scheduled once
- * their set-up is done, so back-to-back calls lose less time between launches.
+ * their set-up is done (the row softmax at once), so back-to-back calls lose
+ * less time between launches.
  * A kernel of the caller's that is launched with the same attribute right after
  * one of these calls must likewise wait for the grid ahead of it
  * (griddepcontrol.wait / cudaGridDependencySynchronize) before reading its

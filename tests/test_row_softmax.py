@@ -90,3 +90,45 @@ def test_argument_errors(cuda_lib):
     assert lib.attn_row_softmax_f32(x.data_ptr(), x.data_ptr(), 4, 0, s) == -1
     assert lib.attn_row_softmax_f32(x.data_ptr(), x.data_ptr() + 4, 4, 8, s) == -1  # partial overlap
     assert lib.attn_row_softmax_f32(x.data_ptr() + 2, x.data_ptr() + 64, 1, 4, s) == -2
+
+
+@pytest.mark.parametrize("M,N", [(2048, 128), (1024, 4096), (64, 8192), (8, 20000)])
+def test_chained_calls_read_the_previous_output(cuda_lib, M, N):
+    """The kernels are launched programmatically (each may start while the kernel ahead
+    still runs, and waits for it before touching memory).  A chain on one stream where
+    each call reads the previous call's output, every third call in place, with a copy
+    kernel of torch's rewriting a buffer right behind some calls, must give the same bits
+    as the same chain with a synchronisation after every operation.  One shape per
+    schedule: warp per row, 128 threads per row, block per row, two passes."""
+    import exact_causal_attention_gb300 as eca
+
+    g = torch.Generator().manual_seed(1200 + N)
+    x0 = (torch.rand(M, N, generator=g, dtype=torch.float64) * 20 - 10).float().cuda()
+    fresh = (x0 * 0.5).contiguous()
+
+    def chain(sync):
+        bufs = [x0.clone(), torch.empty_like(x0)]
+        outs, src = [], 0
+        for i in range(6):
+            if i % 3 == 2:
+                eca.row_softmax(bufs[src], out=bufs[src])
+                dst = src
+            else:
+                eca.row_softmax(bufs[src], out=bufs[1 - src])
+                dst = 1 - src
+            if sync:
+                torch.cuda.synchronize()
+            outs.append(bufs[dst].clone())
+            if i == 3:
+                bufs[dst].copy_(fresh)  # the next call's input, rewritten right behind this call
+                if sync:
+                    torch.cuda.synchronize()
+            src = dst
+        torch.cuda.synchronize()
+        return outs
+
+    ref = chain(True)
+    for _ in range(2):
+        got = chain(False)
+        for a, b in zip(ref, got):
+            assert torch.equal(a, b)
