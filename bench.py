@@ -910,8 +910,8 @@ def bench_launch_cost():
 
 def bench_ingress():
     """csrc/ingress_probe.cu: the rate at which bulk copies fill one SM's shared memory, from HBM and
-    from L2, with 16, 64 and all SMs streaming: the ceiling on the K/V tile fills of the attention
-    kernel."""
+    from L2, with 16, 64 and all SMs streaming, each CTA alone or in multicast pairs: the ceiling on
+    the K/V tile fills of the attention kernel."""
     return run_probe("ingress_probe")
 
 
