@@ -88,6 +88,15 @@ def make_qkv(B: int, H: int, N: int, D: int, dtype: str, seed: int, qk_std: floa
     return tuple(x.to(torch.float32).to(t) for x in (q, k, v))
 
 
+def make_qkv_device(B: int, H: int, N: int, D: int, dtype: str, seed: int, device="cuda"):
+    """(q, k, v) of shape [B, H, N, D] in fp16 or bf16, N(0, 1) drawn by torch's generator on
+    `device`: for tensors too large to draw on the host.  The same seed gives the same bytes
+    for one device type and torch version; a test copies the slices it checks to the host."""
+    g = torch.Generator(device=device).manual_seed(int(seed))
+    t = TORCH_DTYPES[dtype]
+    return tuple(torch.randn(B, H, N, D, generator=g, device=device, dtype=t) for _ in range(3))
+
+
 def workload_qkv(w: Workload):
     return make_qkv(w.B, w.H, w.N, w.D, w.dtype, w.seed, w.qk_std)
 

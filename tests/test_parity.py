@@ -280,3 +280,31 @@ def test_counter_units_d64_ragged(cuda_lib, causal):
     ro, rl = oracle_full(q, k, v, "fp16", causal, scale)
     compare(o, lse, ro, rl, "fp16", None,
             name=f"counter_units_b4_h32_n4000_d64_fp16_{'causal' if causal else 'noncausal'}")
+
+
+@pytest.mark.parametrize("dtype,causal", [("fp16", True), ("bf16", False)])
+def test_tensors_past_4_gib(cuda_lib, dtype, causal):
+    """q, k, v and o of 2^31 elements each (4 GiB: B=128 H=128 N=1024 D=128), so element
+    offsets pass 2^31 and byte offsets 2^32; the units come from the launch's counter in head
+    groups.  Every element is written and finite; whole slices at the start, the middle and
+    the end are compared with the oracle on every row."""
+    import exact_causal_attention_gb300 as eca
+
+    B, H, N, D = 128, 128, 1024, 128
+    scale = 1.0 / math.sqrt(D)
+    q, k, v = inputs.make_qkv_device(B, H, N, D, dtype, seed=1400 + causal, device="cuda")
+    o = torch.full_like(q, float("nan"))
+    lse = torch.full((B, H, N), float("nan"), dtype=torch.float32, device="cuda")
+    eca.attn_fwd_into(q, k, v, o, lse, causal=causal, scale=scale)
+    torch.cuda.synchronize()
+    assert eca.device_status() == 0
+    assert bool(torch.isfinite(o).all()) and bool(torch.isfinite(lse).all())
+    for bh in (0, B * H // 2 + 17, B * H - 1):
+        b, h = divmod(bh, H)
+        qs, ks, vs = (x[b, h][None, None].cpu() for x in (q, k, v))
+        ro, rl = oracle_full(qs, ks, vs, dtype, causal, scale)
+        compare(o[b, h][None, None].double().cpu().numpy(), lse[b, h][None, None].double().cpu().numpy(), ro, rl,
+                dtype, p_rounding_term(qs, ks, vs, dtype, causal, scale),
+                name=f"{'causal' if causal else 'noncausal'}_b128_h128_n1024_d128_{dtype}_slice{bh}")
+    del q, k, v, o, lse
+    torch.cuda.empty_cache()
