@@ -634,8 +634,10 @@ int check_paged_args(const void* cache, const int* block_table, const int* lengt
   if (D != 64 && D != 128) return ATTN_ERR_UNSUPPORTED_D;
   if (page_size != 8 && page_size != 16 && page_size != 32 && page_size != 64) return ATTN_ERR_INVALID_ARG;
   if (!aligned(cache, 16) || !aligned(block_table, 4) || !aligned(lengths, 4)) return ATTN_ERR_UNALIGNED;
+  // The decode kernel addresses the cache's (page, kind, token) rows with a signed 32-bit tensor
+  // coordinate, so there must be fewer than 2^31 of them.
   const uint64_t rows = static_cast<uint64_t>(num_pages) * 2 * static_cast<uint64_t>(page_size);
-  if (rows > 0xffffffffull || static_cast<uint64_t>(max_pages) * page_size > 0x7fffffffull) return ATTN_ERR_INVALID_ARG;
+  if (rows > 0x7fffffffull || static_cast<uint64_t>(max_pages) * page_size > 0x7fffffffull) return ATTN_ERR_INVALID_ARG;
   if (static_cast<uint64_t>(B) * static_cast<uint64_t>(max_pages) > 0x7fffffffull) return ATTN_ERR_INVALID_ARG;
   return ATTN_OK;
 }

@@ -215,6 +215,8 @@ int attn_splitkv_default_splits(int B, int H, int N, int D);
  *   out         : device, [B, Hq, D] fp16, written in full.
  *   lse         : device, [B, Hq] fp32 natural-log log-sum-exp, or NULL.
  *   Hq % Hkv == 0.  D : 64 or 128.  page_size : 8, 16, 32 or 64.
+ *   num_pages * 2 * page_size < 2^31 (the cache's token rows are addressed with
+ *   32-bit tensor coordinates); max_pages * page_size < 2^31.
  *   scale       : finite and > 0.
  *   kv_splits   : 1 .. 64 segments of the context (see attn_decode_default_splits);
  *                 more than one needs `workspace` (256-byte aligned, at least

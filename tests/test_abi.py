@@ -194,6 +194,11 @@ def test_row_softmax_argument_errors_without_gpu(lib):
     assert f(A, A + 16, 4, 8, None) == -1  # y overlaps x without being x
 
 
+def g_rows_limit(lib, C, BT, LN):
+    """attn_paged_append on a cache of 2^31 token rows (checked before any CUDA call)."""
+    return lib.attn_paged_append(A, C, BT, LN, 2, 2, 128, 64, 4, 1 << 24, None)
+
+
 def test_paged_argument_errors_without_gpu(lib):
     f = lib.attn_decode_paged
     Q, C, BT, LN, O, W = A, A + SZ, A + 2 * SZ, A + 3 * SZ, A + 4 * SZ, A + 6 * SZ
@@ -211,6 +216,8 @@ def test_paged_argument_errors_without_gpu(lib):
     assert c(scale=-1.0) == -1
     assert c(q=Q + 2) == -2
     assert c(bt=BT + 2) == -2
+    assert c(T=64, np_=1 << 24) == -1  # 2^31 token rows: past 32-bit tensor coordinates
+    assert g_rows_limit(lib, C, BT, LN) == -1
     assert lib.attn_decode_workspace_bytes(2, 8, 128, 1) == 0
     assert lib.attn_decode_workspace_bytes(2, 8, 128, 4) == 4 * 2 * 8 * 128 * 4 + 256
     g = lib.attn_paged_append
