@@ -269,8 +269,13 @@ struct KeySplit {
   int splits;
 };
 
+// 128-row tiles of a sequence of N rows (N up to INT_MAX without overflow).
+int tiles_of(int N) {
+  return static_cast<int>((static_cast<long long>(N) + eca::kBlockN - 1) / eca::kBlockN);
+}
+
 KeySplit key_split(int N, int requested) {
-  const int n_tiles = (N + eca::kBlockN - 1) / eca::kBlockN;
+  const int n_tiles = tiles_of(N);
   const int r = requested < 1 ? 1 : (requested > n_tiles ? n_tiles : requested);
   const int seg = (n_tiles + r - 1) / r;
   return KeySplit{seg, (n_tiles + seg - 1) / seg};
@@ -300,7 +305,7 @@ int unit_group_heads(int BH, int q_per_kv, int units_per_slice, int sm_count, un
 // unit boundary about three of those, the merge about 4 TB/s); only their
 // ratios matter.  Without a shortage of units the answer is 1.
 int predicted_best_splits(int B, int H, int N, int D, int sm_count) {
-  const int n_tiles = (N + eca::kBlockN - 1) / eca::kBlockN;
+  const int n_tiles = tiles_of(N);
   const int n_pairs = (n_tiles + 1) / 2;
   const long long bh = static_cast<long long>(B) * H;
   if (static_cast<long long>(n_pairs) * bh >= 2LL * sm_count) return 1;
@@ -447,7 +452,8 @@ int launch(const void* q, const void* k, const void* v, void* o, float* lse, int
   p.part_lse = part_lse;
   p.status = st->status;
   p.N = N;
-  p.n_tiles = (N + eca::kBlockM - 1) / eca::kBlockM;
+  static_assert(eca::kBlockM == eca::kBlockN, "query and key tiles have the same height");
+  p.n_tiles = tiles_of(N);
   // Causal grouped heads pair two heads of a key/value group at one query tile:
   // both tiles then need the same key tiles.
   p.head_pair = (part_o == nullptr && causal && (H / Hkv) % 2 == 0) ? 1 : 0;
@@ -535,7 +541,7 @@ int attn_fwd_impl(bool bf16, const void* q, const void* k, const void* v, void* 
   if (Hkv == 0) Hkv = H;
   int rc = check_args(q, k, v, o, lse, B, H, N, D, scale, Hkv);
   if (rc != ATTN_OK) return rc;
-  KeySplit ks{(N + eca::kBlockN - 1) / eca::kBlockN, 1};
+  KeySplit ks{tiles_of(N), 1};
   float* part_o = nullptr;
   float* part_lse = nullptr;
   if (kv_splits > 0) {

@@ -116,6 +116,9 @@ def test_splitkv_workspace_size_without_gpu(lib):
     assert ws(1, 1, 1000, 64, 64) == 8 * 1000 * 64 * 4 + ((8 * 1000 * 4 + 255) // 256) * 256  # 8 key tiles
     assert ws(0, 1, 256, 64, 2) == 0 and ws(1, 1, 256, 96, 2) == 0 and ws(1, 1, 256, 64, 0) == 0
     assert ws(1, 1, 256, 64, 65) == 0
+    # the longest sequence an int holds: 2^24 key tiles (tile counts taken without overflow)
+    n = 2 ** 31 - 1
+    assert ws(1, 1, n, 64, 2) == 2 * n * 64 * 4 + ((2 * n * 4 + 255) // 256) * 256
 
 
 @pytest.mark.parametrize("fn", ["attn_fwd_splitkv", "attn_fwd_splitkv_bf16"])
