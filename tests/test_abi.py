@@ -227,3 +227,24 @@ def test_paged_argument_errors_without_gpu(lib):
     assert g(None, C, BT, LN, 2, 2, 128, 16, 4, 8, None) == -1
     assert g(A + 8, C, BT, LN, 2, 2, 128, 16, 4, 8, None) == -2
     assert g(A, C, BT, LN, 2, 2, 128, 24, 4, 8, None) == -1
+
+
+def test_header_compiles_as_c_and_links_every_entry_point(lib, tmp_path):
+    """A plain C11 program (tests/host/c_abi_check.c) includes include/attn.h, takes the
+    address of every declared entry point from the built library and calls those that
+    need no GPU."""
+    import shutil
+    import subprocess
+
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if cc is None:
+        pytest.skip("no C compiler")
+    so_dir = os.path.dirname(build.LIB_PATH)
+    exe = str(tmp_path / "c_abi_check")
+    src = os.path.join(os.path.dirname(os.path.abspath(__file__)), "host", "c_abi_check.c")
+    subprocess.run([cc, "-std=c11", "-Wall", "-Wextra", "-Werror", "-pedantic", "-I", build.INCLUDE, "-o", exe, src,
+                    "-L", so_dir, "-l:" + os.path.basename(build.LIB_PATH), f"-Wl,-rpath,{so_dir}"], check=True)
+    out = subprocess.run([exe], capture_output=True, text=True, timeout=60)
+    assert out.returncode == 0, (out.returncode, out.stdout, out.stderr)
+    names = declared_functions()
+    assert f"entry points {len(names)}," in out.stdout, (out.stdout, names)
