@@ -190,9 +190,9 @@ size_t attn_splitkv_workspace_bytes(int B, int H, int N, int D, int kv_splits);
 
 /* A split count for the current device: 1 when there are at least two work
  * units (pairs of 128-row query tiles of one head) per SM; otherwise the count
- * whose predicted time is shortest, from a replay of the kernel's static
- * assignment of units to SMs plus the merge kernel's traffic (1 .. 64, at most
- * the number of 128-key tiles).  Negative attn_status on bad sizes or a non-sm_103
+ * whose predicted time is shortest, from a replay of the kernel's schedule
+ * (units taken in order by whichever SM is free first) plus the merge kernel's
+ * traffic (1 .. 64, at most the number of 128-key tiles).  Negative attn_status on bad sizes or a non-sm_103
  * device. */
 int attn_splitkv_default_splits(int B, int H, int N, int D);
 
