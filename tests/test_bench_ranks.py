@@ -90,3 +90,21 @@ def test_clock_normalised_rate():
     assert r["tflops_per_ghz"] == pytest.approx(1700.0 / 2.07)
     assert bench.clock_normalised(1700.0, {"sm_mhz": None}, 152) is None
     assert bench.clock_normalised(1700.0, None, 152) is None
+
+
+def test_traffic_record_matches_the_kernel_sources(tmp_path, monkeypatch):
+    """roofline.traffic comes from the committed ncu record only while the attention
+    kernel's sources hash to the value the record was captured with: the committed
+    record matches the tree, and a changed source or another workload reads as null."""
+    rec = open(os.path.join(bench.PROFILES, "attn_fwd_n8192_traffic.txt")).read()
+    assert f"kernel_source_sha256_16: {bench.kernel_source_hash()}" in rec, \
+        "the attention kernel changed since its traffic was captured: re-capture and update the record"
+    recorded = int(rec.split("dram_bytes_per_launch:")[1].split()[0])
+    assert bench.recorded_traffic() == recorded
+    stale = tmp_path / "profiles"
+    stale.mkdir()
+    (stale / "attn_fwd_n8192_traffic.txt").write_text(rec.replace(bench.kernel_source_hash(), "0" * 16))
+    monkeypatch.setattr(bench, "PROFILES", str(stale))
+    assert bench.recorded_traffic() is None
+    (stale / "attn_fwd_n8192_traffic.txt").write_text(rec.replace(bench.WORKLOAD, "another_workload"))
+    assert bench.recorded_traffic() is None
