@@ -248,3 +248,14 @@ def test_header_compiles_as_c_and_links_every_entry_point(lib, tmp_path):
     assert out.returncode == 0, (out.returncode, out.stdout, out.stderr)
     names = declared_functions()
     assert f"entry points {len(names)}," in out.stdout, (out.stdout, names)
+
+
+@pytest.mark.parametrize("probe", ["launch_cost_probe", "ingress_probe"])
+def test_measurement_probes_compile(tmp_path, probe):
+    """The probes `bench.py --launch-cost` and `--ingress` build and run on the GPU machine
+    compile for sm_103a here (no GPU needed to compile)."""
+    import subprocess
+
+    src = os.path.join(build.CSRC, probe + ".cu")
+    subprocess.run([build._nvcc(), *build.ARCH_FLAGS, "-O2", "-std=c++17", "-o", str(tmp_path / probe), src],
+                   check=True)
